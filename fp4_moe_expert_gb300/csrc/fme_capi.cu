@@ -1,0 +1,223 @@
+// extern "C" entry points of libfme.so: argument checks, status codes and the
+// small helpers (workspace clear / error word, UE8M0 scale unpacking).
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "fme_common.cuh"
+#include "fme_internal.h"
+
+namespace fme {
+
+static thread_local char g_last_error[512] = "";
+
+int set_last_error(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+int device_sm_count(int dev) {
+  static int cache[64] = {0};
+  if (dev < 0 || dev >= 64) return -1;
+  if (cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  cache[dev] = n;
+  return n;
+}
+
+bool ensure_smem_attr(int dev, const void* kernel, size_t bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<int, const void*>> done;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({dev, kernel})) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) !=
+      cudaSuccess)
+    return false;
+  done.insert({dev, kernel});
+  return true;
+}
+
+unsigned long long wait_timeout_ns() {
+  const char* env = std::getenv("FME_WAIT_TIMEOUT_MS");
+  long long ms = 1000;
+  if (env != nullptr) {
+    const long long v = std::atoll(env);
+    if (v > 0) ms = v;
+  }
+  return static_cast<unsigned long long>(ms) * 1000000ull;
+}
+
+// ---------------------------------------------------------------- UE8M0 unpack
+// "shared_expert" block_scales: byte g % 4 of column g // 4 of row r holds the
+// exponent of K group g; the FP32 scale of row block i is exponent << 23.
+__global__ void ue8m0_unpack_kernel(const int32_t* packed, int n, int k, float* dst, int check, int* mismatch) {
+  const int groups = k / 128;
+  const int cols = k / 512;
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (n / 128) * groups) return;
+  const int i = idx / groups, g = idx % groups;
+  auto exponent = [&](int row) {
+    const uint32_t w = static_cast<uint32_t>(__ldg(packed + static_cast<size_t>(row) * cols + g / 4));
+    return (w >> (8 * (g % 4))) & 0xFFu;
+  };
+  const uint32_t e = exponent(128 * i);
+  dst[idx] = __uint_as_float(e << 23);
+  if (check) {
+    for (int r = 1; r < 128; ++r)
+      if (exponent(128 * i + r) != e) {
+        atomicExch(mismatch, 1);
+        break;
+      }
+  }
+}
+
+int ue8m0_unpack(const int32_t* packed, int n, int k, float* dst, int check, int* mismatch, cudaStream_t st) {
+  const int total = (n / 128) * (k / 128);
+  const int threads = 128;
+  ue8m0_unpack_kernel<<<(total + threads - 1) / threads, threads, 0, st>>>(packed, n, k, dst, check, mismatch);
+  const cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return set_last_error(FME_ECUDA, "ue8m0 unpack launch: %s", cudaGetErrorString(err));
+  return FME_OK;
+}
+
+}  // namespace fme
+
+using namespace fme;
+
+static bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+#define FME_REQUIRE(cond, status, ...)                   \
+  do {                                                   \
+    if (!(cond)) return set_last_error(status, __VA_ARGS__); \
+  } while (0)
+
+extern "C" {
+
+const char* fme_last_error(void) { return g_last_error; }
+
+int fme_version(void) { return 100; }
+
+int fme_sm_count(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return device_sm_count(dev);
+}
+
+static int check_fp8_shapes(int M, int H, int I, int E, int top_k, float limit) {
+  FME_REQUIRE(M >= 1 && M <= kMaxTokens, FME_EUNSUPPORTED, "M=%d outside [1, %d]", M, kMaxTokens);
+  FME_REQUIRE(H >= 128 && H % 128 == 0 && I >= 128 && I % 128 == 0, FME_EINVAL,
+              "H=%d and I=%d must be positive multiples of 128", H, I);
+  FME_REQUIRE(H <= 16 * kComputeThreads * kMaxSlicesPerThread && I <= 16 * kComputeThreads * kMaxSlicesPerThread,
+              FME_EUNSUPPORTED, "H=%d or I=%d above %d", H, I, 16 * kComputeThreads * kMaxSlicesPerThread);
+  FME_REQUIRE(E >= 1 && E <= kMaxExperts, FME_EUNSUPPORTED, "E=%d outside [1, %d]", E, kMaxExperts);
+  FME_REQUIRE(top_k >= 1 && top_k <= E && top_k <= kMaxTopK, FME_EINVAL, "top_k=%d outside [1, min(E=%d, %d)]",
+              top_k, E, kMaxTopK);
+  FME_REQUIRE(limit > 0.0f, FME_EINVAL, "limit must be > 0 (got %g)", static_cast<double>(limit));
+  return FME_OK;
+}
+
+size_t fme_moe_routed_fp8_workspace(int M, int H, int I, int E, int top_k) {
+  if (check_fp8_shapes(M, H, I, E, top_k, 1.0f) != FME_OK) return 0;
+  return fp8_workspace_bytes(M * top_k, I, E);
+}
+
+int fme_moe_routed_fp8(const void* x, const void* logits, int logits_dtype, const float* bias, const uint8_t* w13,
+                       const float* s13, const uint8_t* w2, const float* s2, int M, int H, int I, int E, int top_k,
+                       float limit, float scale, int ue8m0, void* out, int32_t* ids, float* weights,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  FME_REQUIRE(x && logits && bias && w13 && s13 && w2 && s2 && out && ids && weights, FME_EINVAL,
+              "null pointer argument");
+  const int st = check_fp8_shapes(M, H, I, E, top_k, limit);
+  if (st != FME_OK) return st;
+  FME_REQUIRE(logits_dtype == FME_F32 || logits_dtype == FME_BF16, FME_EINVAL, "logits_dtype=%d", logits_dtype);
+  FME_REQUIRE(std::isfinite(scale), FME_EINVAL, "scale must be finite");
+  FME_REQUIRE(!misaligned(x) && !misaligned(logits) && !misaligned(bias) && !misaligned(w13) && !misaligned(s13) &&
+                  !misaligned(w2) && !misaligned(s2) && !misaligned(out) && !misaligned(ids) &&
+                  !misaligned(weights) && !misaligned(workspace),
+              FME_EALIGN, "every pointer must be 16-byte aligned");
+  return routed_fp8(x, logits, logits_dtype, bias, w13, s13, w2, s2, M, H, I, E, top_k, limit, scale, ue8m0, out,
+                    ids, weights, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+size_t fme_shared_expert_fp8_workspace(int M, int H, int I) {
+  if (check_fp8_shapes(M, H, I, 1, 1, 1.0f) != FME_OK) return 0;
+  return fp8_workspace_bytes(M, I, 1);
+}
+
+int fme_shared_expert_fp8(const void* x, const uint8_t* w13, const float* s13, const uint8_t* w2, const float* s2,
+                          int M, int H, int I, float limit, int ue8m0, void* gate_up, void* out, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  FME_REQUIRE(x && w13 && s13 && w2 && s2 && out, FME_EINVAL, "null pointer argument");
+  const int st = check_fp8_shapes(M, H, I, 1, 1, limit);
+  if (st != FME_OK) return st;
+  FME_REQUIRE(!misaligned(x) && !misaligned(w13) && !misaligned(s13) && !misaligned(w2) && !misaligned(s2) &&
+                  !misaligned(out) && !misaligned(gate_up) && !misaligned(workspace),
+              FME_EALIGN, "every pointer must be 16-byte aligned");
+  return shared_fp8(x, w13, s13, w2, s2, M, H, I, limit, ue8m0, gate_up, out, workspace, workspace_bytes,
+                    static_cast<cudaStream_t>(stream));
+}
+
+int fme_ue8m0_unpack(const int32_t* packed, int n, int k, float* dst, int check, int* mismatch, void* stream) {
+  FME_REQUIRE(packed && dst && (!check || mismatch), FME_EINVAL, "null pointer argument");
+  FME_REQUIRE(n >= 128 && n % 128 == 0 && k >= 512 && k % 512 == 0, FME_EINVAL,
+              "n=%d must be a multiple of 128 and k=%d of 512", n, k);
+  FME_REQUIRE(!misaligned(packed) && !misaligned(dst), FME_EALIGN, "pointers must be 16-byte aligned");
+  return ue8m0_unpack(packed, n, k, dst, check, mismatch, static_cast<cudaStream_t>(stream));
+}
+
+size_t fme_moe_routed_nvfp4_workspace(int M, int H, int N, int L, int top_k) {
+  if (M < 1 || M > kMaxTokens || H < 128 || H % 128 || N < 128 || N % 128 || L < 1 || L > kMaxExperts ||
+      top_k < 1 || top_k > kMaxTopK || H > 16384 || N > 16384)
+    return 0;
+  return nvfp4_workspace_bytes(M, H, N, L, top_k);
+}
+
+int fme_moe_routed_nvfp4(const void* x, const int32_t* topk_ids, const float* topk_weights, const uint8_t* w13,
+                         const uint8_t* s13, const uint8_t* w2, const uint8_t* s2, int M, int H, int N, int L,
+                         int e0, int top_k, float limit, void* y, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  FME_REQUIRE(x && topk_ids && topk_weights && w13 && s13 && w2 && s2 && y, FME_EINVAL, "null pointer argument");
+  FME_REQUIRE(M >= 1 && M <= kMaxTokens, FME_EUNSUPPORTED, "M=%d outside [1, %d]", M, kMaxTokens);
+  FME_REQUIRE(H >= 128 && H % 128 == 0 && N >= 128 && N % 128 == 0, FME_EINVAL,
+              "H=%d and N=%d must be positive multiples of 128", H, N);
+  FME_REQUIRE(H <= 16384 && N <= 16384, FME_EUNSUPPORTED, "H=%d or N=%d above 16384", H, N);
+  FME_REQUIRE(L >= 1 && L <= kMaxExperts, FME_EUNSUPPORTED, "L=%d outside [1, %d]", L, kMaxExperts);
+  FME_REQUIRE(top_k >= 1 && top_k <= kMaxTopK, FME_EINVAL, "top_k=%d outside [1, %d]", top_k, kMaxTopK);
+  FME_REQUIRE(limit > 0.0f, FME_EINVAL, "limit must be > 0");
+  FME_REQUIRE(!misaligned(x) && !misaligned(topk_ids) && !misaligned(topk_weights) && !misaligned(w13) &&
+                  !misaligned(s13) && !misaligned(w2) && !misaligned(s2) && !misaligned(y) &&
+                  !misaligned(workspace),
+              FME_EALIGN, "every pointer must be 16-byte aligned");
+  return routed_nvfp4(x, topk_ids, topk_weights, w13, s13, w2, s2, M, H, N, L, e0, top_k, limit, y, workspace,
+                      workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int fme_workspace_clear(void* workspace, size_t workspace_bytes, void* stream) {
+  FME_REQUIRE(workspace != nullptr, FME_EINVAL, "null workspace");
+  const cudaError_t err = cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return set_last_error(FME_ECUDA, "cudaMemsetAsync: %s", cudaGetErrorString(err));
+  return FME_OK;
+}
+
+int fme_workspace_error(void* workspace, int* code, void* stream) {
+  FME_REQUIRE(workspace != nullptr && code != nullptr, FME_EINVAL, "null argument");
+  uint32_t word = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t err = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, st);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(st);
+  if (err == cudaSuccess && word != 0u) err = cudaMemsetAsync(workspace, 0, sizeof(word), st);
+  if (err != cudaSuccess) return set_last_error(FME_ECUDA, "reading the error word: %s", cudaGetErrorString(err));
+  *code = static_cast<int>(word);
+  if (word != 0u) return set_last_error(FME_ETIMEOUT, "device error word 0x%x", word);
+  return FME_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,155 @@
+// Inline-PTX building blocks for the sm_103a kernels of this library:
+// mbarriers, bulk global->shared copies, FP8/FP4 conversions, the mixed
+// f16-product / f32-sum FMA, gpu-scope acquire/release and bounded waits.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+
+namespace fme {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ------------------------------------------------------------------ mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits until the phase with the given parity has completed. Gives up after
+// limit_ns of wall time or once *abort (when given) becomes non-zero; returns
+// false then.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                          const volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (abort != nullptr && *abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses (after a
+// CTA barrier: every thread's) before later async-proxy (bulk copy) writes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ bulk copy
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// Contiguous global -> shared copy completing on an mbarrier (bytes: multiple
+// of 16; both addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+      "%4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// ------------------------------------------------------------------ gpu-scope sync
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ------------------------------------------------------------------ conversions
+// Four E4M3 bytes (low byte first) -> two f16x2 words holding the same values.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{ .reg .b16 a, b; mov.b32 {a, b}, %2; cvt.rn.f16x2.e4m3x2 %0, a; cvt.rn.f16x2.e4m3x2 %1, b; }"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+// Two E2M1 nibbles (low nibble first) in the low byte of w -> one f16x2 word.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t w) {
+  uint32_t d;
+  asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(d) : "r"(w));
+  return d;
+}
+// (lo, hi) -> E4M3 bytes, lo in the low byte: round to nearest even, finite
+// values beyond 448 saturate.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// (lo, hi) -> E2M1 nibbles, lo in the low nibble: nearest even, saturating at 6.
+__device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// c + a.lo * b.lo + a.hi * b.hi: each f16 product exact, each add rounded in f32.
+__device__ __forceinline__ float fma_f16x2_f32(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{ .reg .b16 al, ah, bl, bh; .reg .f32 t; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2; "
+      "fma.rn.f32.f16 t, al, bl, %3; fma.rn.f32.f16 %0, ah, bh, t; }"
+      : "=f"(d)
+      : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+// Float value of an E4M3 byte (exact).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
+  uint32_t lo, hi;
+  e4m3x4_to_f16x2x2(byte & 0xFF, lo, hi);
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(lo & 0xFFFF)));
+}
+
+// Monotone uint32 key of a float (negative: all bits flipped; else the sign
+// bit set), so unsigned order equals float order for non-NaN values.
+__device__ __forceinline__ uint32_t ordered_key(float v) {
+  const uint32_t b = __float_as_uint(v);
+  const uint32_t m = static_cast<uint32_t>(static_cast<int32_t>(b) >> 31) | 0x80000000u;
+  return b ^ m;
+}
+
+// Power-of-two round-up of a positive float32 scale (UE8M0): the exponent field
+// of max(s, 1e-10) plus one when any mantissa bit is set.
+__device__ __forceinline__ float ue8m0_ceil(float s) {
+  const uint32_t b = __float_as_uint(fmaxf(s, 1e-10f));
+  const uint32_t e = (b >> 23) + ((b & 0x7FFFFFu) != 0u);
+  return __uint_as_float(e << 23);
+}
+
+}  // namespace fme

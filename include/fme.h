@@ -1,0 +1,187 @@
+/*
+ * fme.h -- C ABI of libfme.so: the routed-expert MoE decode layer (FP8 and
+ * NVFP4) and the FP8 shared expert, as hand-written sm_103a CUDA kernels.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers named x, logits, bias, w13, s13, w2, s2, topk_ids, topk_weights,
+ *   packed (inputs) and out, ids, weights, y, gate_up, dst (outputs) are
+ *   DEVICE pointers; the caller owns every buffer. The library never
+ *   allocates, frees or caches device memory.
+ * - Matrices are dense row-major (last index fastest). Every device pointer
+ *   must be 16-byte aligned.
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *   stream). Calls are asynchronous on it and never synchronise the host.
+ * - Return value: FME_OK, or a negative fme_status when the host-side checks
+ *   reject the arguments or the launch fails. fme_last_error() then holds a
+ *   one-line reason (thread-local). Device-side faults of the bounded waits
+ *   are reported through the workspace error word (fme_workspace_error).
+ * - Workspace: caller-owned device scratch of at least the size the matching
+ *   *_workspace() function returns. It must be zero-filled before its first
+ *   use (fme_workspace_clear). Every successful call leaves its counters at
+ *   zero again, so one workspace serves any number of calls issued in stream
+ *   order. Two calls that overlap on the GPU need two workspaces. After a
+ *   device-side error, clear it again before reuse.
+ * - BF16 is IEEE bfloat16 (uint16 bit patterns). FP8 is E4M3 ("e4m3fn": no
+ *   infinities, 0x7F/0xFF are NaN). FP4 is E2M1, sign in bit 3.
+ */
+#ifndef FME_H_
+#define FME_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FME_OK = 0,
+  FME_EINVAL = -1,       /* bad shape, count or null pointer */
+  FME_EUNSUPPORTED = -2, /* valid request outside the supported shape range */
+  FME_EALIGN = -3,       /* a pointer is not 16-byte aligned */
+  FME_ECUDA = -4,        /* a CUDA runtime call failed (message has the name) */
+  FME_ETIMEOUT = -5,     /* a device-side bounded wait gave up */
+  FME_EWORKSPACE = -6    /* workspace missing or too small */
+} fme_status;
+
+typedef enum { FME_F32 = 0, FME_BF16 = 1 } fme_dtype;
+
+/* One-line reason for the last non-OK status returned on this host thread. */
+const char* fme_last_error(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int fme_version(void);
+
+/*
+ * Routed FP8 MoE layer for M decode tokens.
+ *
+ * Source: "vllm.models.glm5next.nvidia.specialized_decode.mega_moe",
+ * MegaExperts.__call__ and _MegaKernel (top_k_pick, the epilogue x-quant,
+ * GEMM1 and GEMM2 epilogues, hidden_block). Per token t and pick r:
+ *   routing  s = sigmoid(logits[t]); key = s + bias; the top_k largest keys
+ *            (ties: lower expert) in descending key order -> ids[t, r];
+ *            weights[t, r] = s_r / (float sum of picked s) * scale (bias is
+ *            used for selection only).
+ *   x-quant  per 128-block of x[t]: sx = max(amax, 1e-10) / 448 (rounded up to
+ *            a power of two when ue8m0), q = e4m3(x * (1 / sx)).
+ *   GEMM1    y[n] = sum_b (sum_{k in b} W13[e, n, k] q[k]) * (s13[e, n/128, b] * sx[b]),
+ *            n < 2I; rows [0, I) are "up", rows [I, 2I) are "gate".
+ *   SwiGLU   h = silu(min(gate, limit)) * clamp(up, -limit, limit).
+ *   h-quant  per 128-block of h: sh = max(amax, 1e-10) / 448 (power of two when
+ *            ue8m0), qh = e4m3(h / sh).
+ *   GEMM2    out[t*top_k + r, m] = bf16(sum_b (sum_j W2[e, m, j] qh[j]) * (s2[e, m/128, b] * sh[b])).
+ * The route rows are NOT multiplied by the routing weights.
+ *
+ * Arguments:
+ *   x       [M, H] BF16 tokens.
+ *   logits  [M, E] router logits, dtype logits_dtype (FME_F32 or FME_BF16).
+ *   bias    [E] FP32 score-correction bias.
+ *   w13     [E, 2I, H] E4M3 (up rows, then gate rows); s13 [E, 2I/128, H/128] FP32.
+ *   w2      [E, H, I] E4M3; s2 [E, H/128, I/128] FP32.
+ *   M in [1, 64], H and I multiples of 128 with H, I <= 8192, E in [1, 1024],
+ *   top_k in [1, min(E, 32)], limit > 0 (+inf allowed), scale finite.
+ *   out     [M*top_k, H] BF16 (row t*top_k + r), ids [M, top_k] int32,
+ *   weights [M, top_k] FP32.
+ *   workspace / workspace_bytes: see fme_moe_routed_fp8_workspace.
+ * Each touched expert's weights are read from HBM once per call, whatever
+ * the number of routes that picked it.
+ */
+int fme_moe_routed_fp8(const void* x, const void* logits, int logits_dtype, const float* bias,
+                       const uint8_t* w13, const float* s13, const uint8_t* w2, const float* s2,
+                       int M, int H, int I, int E, int top_k, float limit, float scale, int ue8m0,
+                       void* out, int32_t* ids, float* weights, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/* Workspace bytes fme_moe_routed_fp8 needs for these sizes (0 on bad sizes). */
+size_t fme_moe_routed_fp8_workspace(int M, int H, int I, int E, int top_k);
+
+/*
+ * FP8 shared expert for M decode tokens.
+ *
+ * Source: "vllm.models.glm5next.nvidia.specialized_decode.shared_expert",
+ * SharedExpert.__call__, _GateUpKernel, _DownKernel and _group_scale:
+ *   x-quant per 128 as in fme_moe_routed_fp8 (scale rule _group_scale);
+ *   gate_up[t, n] = bf16(sum_b P[n, b] * (sx[b] * s13[n/128, b])), rows [0, I)
+ *     are "gate", rows [I, 2I) are "up";
+ *   h = bf16(silu(min(g, limit)) * clamp(u, -limit, limit)) (IEEE divide);
+ *   h-quant per 128 by _group_scale (ue8m0 per flag), q = e4m3(h * (1 / sh));
+ *   out[t, m] = bf16(sum_b P[m, b] * (sh[b] * s2[m/128, b])).
+ *
+ * Arguments: x [M, H] BF16; w13 [2I, H] E4M3; s13 [2I/128, H/128] FP32;
+ *   w2 [H, I] E4M3; s2 [H/128, I/128] FP32 (fme_ue8m0_unpack converts packed
+ *   UE8M0 scales); limits as fme_moe_routed_fp8 (E = 1, top_k = 1).
+ *   gate_up: optional [M, 2I] BF16 output of the gate/up GEMV (NULL: not
+ *   written). out [M, H] BF16.
+ */
+int fme_shared_expert_fp8(const void* x, const uint8_t* w13, const float* s13, const uint8_t* w2,
+                          const float* s2, int M, int H, int I, float limit, int ue8m0,
+                          void* gate_up, void* out, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+size_t fme_shared_expert_fp8_workspace(int M, int H, int I);
+
+/*
+ * Packed UE8M0 block scales -> FP32 block scales.
+ *
+ * Source: "vllm.models.glm5next.nvidia.specialized_decode.shared_expert",
+ * block_scales: packed int32 [n, k/512], byte g % 4 of column g // 4 holds the
+ * exponent of K group g; dst [n/128, k/128] FP32 with bits exponent << 23.
+ * The exponent must be the same on all 128 rows of a row block: the kernel
+ * reads row 128*i of each block and, when check != 0, compares every row and
+ * sets *mismatch (device int, may be NULL when check == 0) to 1 on any
+ * difference. n and k multiples of 128 and 512.
+ */
+int fme_ue8m0_unpack(const int32_t* packed, int n, int k, float* dst, int check, int* mismatch,
+                     void* stream);
+
+/*
+ * NVFP4 slot MoE over the local experts [e0, e0 + L).
+ *
+ * Source: "nvfp4-megamoe-kernel README.md" (slot representation; Data Formats;
+ * Bugs Found & Fixed 2, 4, 6, 7). A slot is a (token, pick) pair whose expert
+ * is local; other picks are dropped. Per slot s of token t, local expert le:
+ *   x-quant per 16: sc = e4m3(amax / 6) (stored UE4M3, also the divisor),
+ *     q = e2m1(x / sc) (zeros when sc decodes to 0);
+ *   g1[n] = bf16(sum_k dq(q_k) dq(W13[le, n, k])), dq = E2M1 value times its
+ *     group-16 UE4M3 scale; rows [0, N) "gate", [N, 2N) "up";
+ *   h = bf16(silu(min(gate, limit)) * clamp(up, -limit, limit)) per slot;
+ *   h re-quantised like x; o[m] = bf16(sum_j dq(qh_j) dq(W2[le, m, j]));
+ *   y[t, m] = bf16(sum over t's local slots, ascending pick, of
+ *     topk_weights[t, r] * o[m]) accumulated in FP32: the routing weights
+ *     are applied exactly once. Tokens with no local slot get zeros.
+ * Arguments: x [M, H] BF16; topk_ids [M, top_k] int32 (global ids; negative
+ *   or out-of-range ids are simply non-local); topk_weights [M, top_k] FP32;
+ *   w13 [L, 2N, H/2] packed E2M1 (element 2i in the low nibble), s13
+ *   [L, 2N, H/16] UE4M3 bytes; w2 [L, H, N/2], s2 [L, H, N/16]; limit > 0
+ *   (+inf: no clamp). M in [1, 64], H multiple of 128 and <= 16384, N
+ *   multiple of 128 and <= 16384, L in [1, 1024], top_k in [1, 32].
+ *   y [M, H] BF16.
+ */
+int fme_moe_routed_nvfp4(const void* x, const int32_t* topk_ids, const float* topk_weights,
+                         const uint8_t* w13, const uint8_t* s13, const uint8_t* w2,
+                         const uint8_t* s2, int M, int H, int N, int L, int e0, int top_k,
+                         float limit, void* y, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+size_t fme_moe_routed_nvfp4_workspace(int M, int H, int N, int L, int top_k);
+
+/* Zero a workspace (cudaMemsetAsync on stream). */
+int fme_workspace_clear(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Read and clear the device error word of a workspace (synchronises stream).
+ * *code receives 0 or a bit set: 1 = a ring wait timed out, 2 = a cross-CTA
+ * wait timed out, 4 = the producer could not drain its copies. Returns
+ * FME_ETIMEOUT when *code != 0, FME_OK otherwise.
+ */
+int fme_workspace_error(void* workspace, int* code, void* stream);
+
+/* Number of streaming multiprocessors the kernels size their grids to. */
+int fme_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FME_H_ */

@@ -155,3 +155,57 @@ def to_bf16_values(v) -> np.ndarray:
 
     return torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).to(torch.bfloat16) \
         .to(torch.float32).numpy()
+
+
+# --------------------------------------------------------------------------- device fill
+_HERE = __import__("os").path.dirname(__import__("os").path.abspath(__file__))
+SYNTH_LIB = __import__("os").path.join(_HERE, "libfme_synth.so")
+_synth = None
+
+
+def build_device_lib(force=False):
+    """Compile synth/csrc/synth.cu -> synth/libfme_synth.so (sm_103a)."""
+    import os
+    import subprocess
+
+    src = os.path.join(_HERE, "csrc", "synth.cu")
+    if not force and os.path.exists(SYNTH_LIB) and os.path.getmtime(SYNTH_LIB) >= os.path.getmtime(src):
+        return SYNTH_LIB
+    cmd = [os.environ.get("NVCC", "nvcc"), "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-shared",
+           "-Xcompiler", "-fPIC", "-o", SYNTH_LIB + ".tmp", src]
+    subprocess.run(cmd, check=True, capture_output=True)
+    os.replace(SYNTH_LIB + ".tmp", SYNTH_LIB)
+    return SYNTH_LIB
+
+
+def _lib():
+    global _synth
+    if _synth is None:
+        import ctypes
+
+        build_device_lib()
+        _synth = ctypes.CDLL(SYNTH_LIB)
+        _synth.fme_synth_fill_codes.restype = ctypes.c_int
+        _synth.fme_synth_fill_codes.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_longlong,
+                                                ctypes.c_uint, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                                ctypes.c_void_p]
+    return _synth
+
+
+def fill_codes_device(out, seed, tensor, table, expert0=0):
+    """Fill a CUDA uint8 tensor [E, ...] in place: expert e (the first dim,
+    offset by expert0) gets exactly ``expert_bytes(seed, tensor, e + expert0, ...)``."""
+    import ctypes
+
+    import torch
+
+    assert out.dtype == torch.uint8 and out.is_cuda and out.is_contiguous()
+    t = torch.as_tensor(np.asarray(table, dtype=np.uint64).view(np.int64), device=out.device)
+    n_experts = out.shape[0]
+    per = out.numel() // n_experts
+    rc = _lib().fme_synth_fill_codes(ctypes.c_void_p(out.data_ptr()), n_experts, per, int(seed) & 0xFFFFFFFF,
+                                     int(tensor), ctypes.c_void_p(t.data_ptr()), int(expert0),
+                                     ctypes.c_void_p(torch.cuda.current_stream(out.device).cuda_stream))
+    if rc != 0:
+        raise RuntimeError(f"synth fill failed: cuda error {rc}")
+    return out

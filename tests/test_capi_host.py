@@ -1,0 +1,79 @@
+"""CPU-only checks of the C ABI: libfme.so loads, exports every entry point
+include/fme.h declares, and its host-side argument checks reject bad calls
+before touching the GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fme.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fme_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def fme():
+    from fp4_moe_expert_gb300 import build
+    build.build()
+    import fp4_moe_expert_gb300 as m
+    return m
+
+
+def test_every_declared_symbol_is_exported(fme):
+    names = _declared()
+    assert "fme_moe_routed_fp8" in names and "fme_moe_routed_nvfp4" in names
+    for n in names:
+        assert hasattr(fme.lib, n), n
+        assert n in fme.SIGNATURES, f"binding lacks {n}"
+    # and the binding exposes nothing the header does not declare
+    assert set(fme.SIGNATURES) == set(names)
+
+
+def test_version_and_workspace_sizes(fme):
+    assert fme.lib.fme_version() >= 100
+    assert fme.moe_routed_fp8_workspace(8, 7168, 2048, 256, 8) > 64 * 2048 * 4
+    assert fme.moe_routed_fp8_workspace(0, 7168, 2048, 256, 8) == 0
+    assert fme.moe_routed_fp8_workspace(1, 7168, 2000, 256, 8) == 0
+    assert fme.moe_routed_fp8_workspace(1, 7168, 2048, 256, 300) == 0
+    assert fme.moe_routed_nvfp4_workspace(64, 7168, 3072, 48, 6) > 0
+
+
+def _routed(fme, **kw):
+    vp = ctypes.c_void_p
+    args = dict(x=vp(16), logits=vp(16), dt=0, bias=vp(16), w13=vp(16), s13=vp(16), w2=vp(16), s2=vp(16),
+                M=1, H=512, I=256, E=8, k=2, limit=7.0, scale=1.0, ue=0, out=vp(16), ids=vp(16),
+                weights=vp(16), ws=vp(16), wsb=1 << 20, st=None)
+    args.update(kw)
+    return fme.lib.fme_moe_routed_fp8(*args.values())
+
+
+def test_host_validation_rejects_bad_calls(fme):
+    assert _routed(fme, x=None) == -1                 # null pointer
+    assert _routed(fme, M=0) == -2                    # M outside [1, 64]
+    assert _routed(fme, M=65) == -2
+    assert _routed(fme, H=500) == -1                  # not a multiple of 128
+    assert _routed(fme, I=100) == -1
+    assert _routed(fme, k=9) == -1                    # top_k > E
+    assert _routed(fme, E=2000) == -2
+    assert _routed(fme, limit=0.0) == -1
+    assert _routed(fme, dt=7) == -1
+    assert _routed(fme, scale=float("inf")) == -1
+    assert _routed(fme, w13=ctypes.c_void_p(17)) == -3  # misaligned
+    msg = fme.lib.fme_last_error().decode()
+    assert "aligned" in msg
+
+
+def test_nvfp4_and_unpack_validation(fme):
+    vp = ctypes.c_void_p
+    rc = fme.lib.fme_moe_routed_nvfp4(vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), 1, 7168, 3000,
+                                      48, 0, 6, float("inf"), vp(16), vp(16), 1 << 20, None)
+    assert rc == -1
+    assert fme.lib.fme_ue8m0_unpack(vp(16), 100, 512, vp(16), 0, None, None) == -1
+    assert fme.lib.fme_ue8m0_unpack(None, 128, 512, vp(16), 0, None, None) == -1

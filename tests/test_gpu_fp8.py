@@ -1,0 +1,179 @@
+"""GPU parity of the routed FP8 layer and the FP8 shared expert against the
+oracle, through the C ABI (via the thin binding)."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_fp8, routing
+from synth import workloads as W
+from tests.parity import assert_outputs, assert_routing
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def fme():
+    import fp4_moe_expert_gb300 as m
+    return m
+
+
+def _device_problem(cfg, M, seed, step=0):
+    w13h, w2h = W.fp8_weights_host(cfg, seed)
+    s13, s2 = W.fp8_weight_scales(cfg, seed)
+    x, logits, bias = W.fp8_activations(cfg, M, seed, step)
+    return w13h, w2h, s13, s2, x, logits, bias
+
+
+def _to_dev(cfg, x, logits, bias):
+    xd = torch.from_numpy(x).to(DEV).to(torch.bfloat16)
+    ld = torch.from_numpy(logits).to(DEV)
+    if cfg.logits_bf16:
+        ld = ld.to(torch.bfloat16)
+    return xd, ld, torch.from_numpy(bias).to(DEV)
+
+
+def _run_small(fme, cfg, M, seed, top_k=None, **over):
+    top_k = top_k or cfg.top_k
+    w13h, w2h, s13, s2, x, logits, bias = _device_problem(cfg, M, seed)
+    w13 = torch.from_numpy(w13h.full()).to(DEV)
+    w2 = torch.from_numpy(w2h.full()).to(DEV)
+    xd, ld, bd = _to_dev(cfg, x, logits, bias)
+    out, ids, wts = fme.moe_routed_fp8(xd, ld, bd, w13, torch.from_numpy(s13).to(DEV), w2,
+                                       torch.from_numpy(s2).to(DEV), top_k, cfg.limit, cfg.scale, cfg.ue8m0)
+    torch.cuda.synchronize()
+    ref, rids, rw, keys = moe_fp8.routed_fp8(x, logits, bias, w13h, s13, w2h, s2, top_k, cfg.limit, cfg.scale,
+                                             cfg.ue8m0)
+    gaps = routing.selection_gap(keys, rids)
+    assert_routing(ids.cpu().numpy(), wts.cpu().numpy(), rids, rw, gaps)
+    got = out.float().cpu().numpy()
+    return got, ref, ids.cpu().numpy(), rids
+
+
+@pytest.mark.parametrize("cfg_name,M", [("tiny_fp8", 1), ("ragged_fp8", 5)])
+@pytest.mark.parametrize("ue8m0", [False, True])
+def test_routed_small_full_parity(fme, cfg_name, M, ue8m0):
+    import dataclasses
+    cfg = dataclasses.replace(W.FP8_CONFIGS[cfg_name], ue8m0=ue8m0)
+    got, ref, ids, rids = _run_small(fme, cfg, M, seed=3)
+    assert_outputs(got, ref)
+
+
+def test_routed_top_k_equals_E_and_max_tokens(fme):
+    import dataclasses
+    cfg = dataclasses.replace(W.TINY, H=256, I=128, E=8, top_k=8, name="topk_all")
+    got, ref, ids, _ = _run_small(fme, cfg, 3, seed=4)
+    assert_outputs(got, ref)
+    assert sorted(ids[0].tolist()) == list(range(8))
+    cfg = dataclasses.replace(W.TINY, H=256, I=128, E=16, top_k=4, name="max_tokens")
+    got, ref, _, _ = _run_small(fme, cfg, 64, seed=5)
+    assert_outputs(got, ref)
+
+
+def test_routed_deterministic_and_identical_tokens(fme):
+    cfg = W.RAGGED
+    w13h, w2h, s13, s2, x, logits, bias = _device_problem(cfg, 4, 6)
+    x[2] = x[0]
+    logits[2] = logits[0]
+    w13 = torch.from_numpy(w13h.full()).to(DEV)
+    w2 = torch.from_numpy(w2h.full()).to(DEV)
+    xd, ld, bd = _to_dev(cfg, x, logits, bias)
+    args = (xd, ld, bd, w13, torch.from_numpy(s13).to(DEV), w2, torch.from_numpy(s2).to(DEV), cfg.top_k,
+            cfg.limit, cfg.scale, cfg.ue8m0)
+    outs = [fme.moe_routed_fp8(*args)[0].clone() for _ in range(5)]
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    k = cfg.top_k
+    assert torch.equal(outs[0][0:k], outs[0][2 * k:3 * k])
+
+
+def test_routed_workspace_stays_clean(fme):
+    cfg = W.TINY
+    w13h, w2h, s13, s2, x, logits, bias = _device_problem(cfg, 1, 7)
+    ws = fme.Workspace(fme.moe_routed_fp8_workspace(1, cfg.H, cfg.I, cfg.E, cfg.top_k), DEV)
+    w13 = torch.from_numpy(w13h.full()).to(DEV)
+    w2 = torch.from_numpy(w2h.full()).to(DEV)
+    xd, ld, bd = _to_dev(cfg, x, logits, bias)
+    for _ in range(3):
+        fme.moe_routed_fp8(xd, ld, bd, w13, torch.from_numpy(s13).to(DEV), w2, torch.from_numpy(s2).to(DEV),
+                           cfg.top_k, cfg.limit, cfg.scale, cfg.ue8m0, workspace=ws)
+    torch.cuda.synchronize()
+    assert ws.error() == 0
+    counters = ws.buf[256:256 + 2 * 256].view(torch.int32)
+    assert int(counters.abs().sum().item()) == 0
+
+
+def _full_size(fme, cfg, M, seed, routes, rows):
+    w13, s13, w2, s2 = W.fp8_weights_device(cfg, seed, DEV)
+    s13h, s2h = s13.cpu().numpy(), s2.cpu().numpy()
+    w13h, w2h = W.fp8_weights_host(cfg, seed)
+    x, logits, bias = W.fp8_activations(cfg, M, seed)
+    xd, ld, bd = _to_dev(cfg, x, logits, bias)
+    out, ids, wts = fme.moe_routed_fp8(xd, ld, bd, w13, s13, w2, s2, cfg.top_k, cfg.limit, cfg.scale, cfg.ue8m0)
+    torch.cuda.synchronize()
+    ref, rids, rw, keys = moe_fp8.routed_fp8(x, logits, bias, w13h, s13h, w2h, s2h, cfg.top_k, cfg.limit,
+                                             cfg.scale, cfg.ue8m0, routes=routes, rows=rows)
+    assert_routing(ids.cpu().numpy(), wts.cpu().numpy(), rids, rw, routing.selection_gap(keys, rids))
+    # the device-filled weights are the generator's bytes
+    e = int(rids.reshape(-1)[routes[0]])
+    assert np.array_equal(w13[e, :64].cpu().numpy(), w13h[e][:64])
+    got = out.float().cpu().numpy()
+    assert_outputs(got[routes][:, rows], ref[routes][:, rows])
+    return out
+
+
+def test_dsv3_m1_full_size_all_routes(fme):
+    _full_size(fme, W.DSV3, 1, seed=11, routes=list(range(8)), rows=np.arange(7168))
+
+
+def test_dsv3_m8_sampled_routes(fme):
+    rng = np.random.default_rng(1)
+    routes = sorted(rng.choice(64, 4, replace=False).tolist())
+    _full_size(fme, W.DSV3, 8, seed=12, routes=routes, rows=np.arange(7168))
+
+
+def test_dsv3_ue8m0_m4_sampled(fme):
+    _full_size(fme, W.DSV3_UE8M0, 4, seed=13, routes=[0, 13, 31], rows=np.arange(0, 7168, 7))
+
+
+def test_latent_m32_sampled_routes(fme):
+    rng = np.random.default_rng(2)
+    routes = sorted(rng.choice(32 * 16, 5, replace=False).tolist())
+    _full_size(fme, W.LATENT, 32, seed=14, routes=routes, rows=np.arange(3584))
+
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_shared_expert_full_size(fme, M):
+    cfg = W.SHARED
+    w13, s13, w2, s2 = W.shared_weights_host(cfg, seed=21)
+    x, _, _ = W.fp8_activations(W.DSV3, M, seed=21)
+    out, gu = fme.shared_expert_fp8(torch.from_numpy(x).to(DEV).to(torch.bfloat16), torch.from_numpy(w13).to(DEV),
+                                    torch.from_numpy(s13).to(DEV), torch.from_numpy(w2).to(DEV),
+                                    torch.from_numpy(s2).to(DEV), cfg.limit, cfg.ue8m0, want_gate_up=True)
+    torch.cuda.synchronize()
+    ref, ref_gu = moe_fp8.shared_fp8(x, w13, s13, w2, s2, cfg.limit, cfg.ue8m0)
+    assert_outputs(gu.float().cpu().numpy(), ref_gu, "gate_up")
+    assert_outputs(out.float().cpu().numpy(), ref, "out")
+
+
+def test_shared_expert_small_non_ue8m0(fme):
+    cfg = W.SharedConfig("small_shared", 1024, 384, 7.0, False)
+    w13, s13, w2, s2 = W.shared_weights_host(cfg, seed=22)
+    x, _, _ = W.fp8_activations(W.RAGGED, 5, seed=22)
+    out = fme.shared_expert_fp8(torch.from_numpy(x).to(DEV).to(torch.bfloat16), torch.from_numpy(w13).to(DEV),
+                                torch.from_numpy(s13).to(DEV), torch.from_numpy(w2).to(DEV),
+                                torch.from_numpy(s2).to(DEV), cfg.limit, cfg.ue8m0)
+    torch.cuda.synchronize()
+    ref, _ = moe_fp8.shared_fp8(x, w13, s13, w2, s2, cfg.limit, cfg.ue8m0)
+    assert_outputs(out.float().cpu().numpy(), ref)
+
+
+def test_device_generator_matches_host(fme):
+    import synth
+    t = synth.e4m3_normal_table()
+    buf = torch.empty(3, 40, 96, dtype=torch.uint8, device=DEV)
+    synth.fill_codes_device(buf, 5, synth.T_W2, t, expert0=7)
+    for e in range(3):
+        assert np.array_equal(buf[e].cpu().numpy(), synth.expert_bytes(5, synth.T_W2, 7 + e, 40, 96, t))
