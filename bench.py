@@ -1,0 +1,404 @@
+"""Benchmark of the routed FP8 MoE decode layer (DeepSeek-V3 shape) on GB300.
+
+One step = one routed-FP8 layer call at each of M = 1, 2, 4, 8 decode tokens
+(hidden 7168, inter 2048, 256 experts, top_k 8, BF16 logits), every call with
+fresh router logits so the touched expert set changes as in real decode. The
+metric is the weight-stream bandwidth: the bytes of every unique expert the
+calls touched (W13 + W2 + FP32 block scales, counted from the kernel's own
+ids) over the device time. All weights (11.3 GB) are resident in HBM; each
+call reads >= 352 MB of them, well above the 129 MB L2, so no flush is needed.
+
+Launch: python bench.py [--gpus N --steps K --warmup W] (N > 1 under
+torch.distributed.run: one independent replica per GPU, no collective on the
+data path; the value is the sum over ranks of bytes over the max time).
+--impl reference times the CPU oracle instead (host cores, bounded sample).
+Prints one JSON line on rank 0.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+MS = (1, 2, 4, 8)
+EXPERT_BYTES = 4096 * 7168 + 7168 * 2048 + 4 * (32 * 56 + 56 * 16)  # 44,050,944
+METRIC = "routed-MoE layer weight-stream HBM GB/s at M=1-8 tokens (DSv3-shaped routed FP8)"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="fme", choices=["fme", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-extras", action="store_true", help="skip the shared-expert / NVFP4 side measurements")
+    ap.add_argument("--ref-seconds", type=float, default=10.0)
+    ap.add_argument("--experts", type=int, default=256,
+                    help="experts resident on the device (smaller for profiler captures; 32 x 44 MB = 1.4 GB)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------- CPU oracle leg
+def oracle_sample(seconds, seed=0):
+    """Time the CPU oracle on whole DSv3 routes (one expert's GEMM1 + SwiGLU +
+    GEMM2 for one token) until `seconds` of work; weights are generated before
+    the clock starts. Returns (GB/s of weight stream, routes, seconds)."""
+    from oracle import moe_fp8
+    from synth import workloads as W
+
+    cfg = W.DSV3
+    w13h, w2h = W.fp8_weights_host(cfg, seed)
+    s13, s2 = W.fp8_weight_scales(cfg, seed)
+    done, t_total, step = 0, 0.0, 0
+    while t_total < seconds and done < 64:
+        x, logits, bias = W.fp8_activations(cfg, 1, seed, step)
+        from oracle import routing
+        ids, _, _ = routing.route(logits, bias, cfg.top_k, cfg.scale)
+        e = int(ids[0, 0])
+        w13h[e], w2h[e]  # materialise this expert's bytes outside the timed region
+        t0 = time.perf_counter()
+        moe_fp8.routed_fp8(x, logits, bias, w13h, s13, w2h, s2, cfg.top_k, cfg.limit, cfg.scale, cfg.ue8m0,
+                           routes=[0])
+        t_total += time.perf_counter() - t0
+        done += 1
+        step += 1
+    return done * EXPERT_BYTES / t_total / 1e9, done, t_total
+
+
+def run_oracle_subprocess(seconds):
+    """Run the oracle sample in a child pinned to one thread; returns its dict."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; g,n,t=bench.oracle_sample(%f); "
+            "print(json.dumps({'gbs': g, 'routes': n, 'seconds': t}))" % (ROOT, seconds))
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, check=True)
+    return json.loads(out.stdout.strip().splitlines()[-1])
+
+
+def reference_arm(args, rank):
+    if rank != 0:
+        return
+    steps = max(1, min(args.steps, 6))
+    per = max(2.0, args.ref_seconds / steps)
+    vals = []
+    t0 = time.time()
+    for _ in range(steps):
+        r = run_oracle_subprocess(per)
+        vals.append(r)
+    gbs = sum(v["routes"] for v in vals) * EXPERT_BYTES / sum(v["seconds"] for v in vals) / 1e9
+    ms_per_route = 1e3 * sum(v["seconds"] for v in vals) / sum(v["routes"] for v in vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": steps, "warmup": 0, "ms_per_step": round(ms_per_route, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "dsv3_routed_fp8 (H 7168, I 2048, E 256, top_k 8)", "sample": "one route per "
+                   "oracle call (one expert: 44,050,944 weight+scale bytes)", "parallelism": "replicas"},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{sum(v['routes'] for v in vals)} DSv3 routes, {time.time() - t0:.1f} s wall"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            self.proc.wait(timeout=10)
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- GPU arm
+def gpu_arm(args, rank, world, local_rank):
+    import torch
+
+    import fp4_moe_expert_gb300 as fme
+    from synth import workloads as W
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    import dataclasses
+    cfg = dataclasses.replace(W.DSV3, E=args.experts)
+    w13, s13, w2, s2 = W.fp8_weights_device(cfg, args.seed, dev)
+    n_calls = (args.warmup + args.steps) * len(MS)
+    pool = 64
+    # Fresh logits for every call (a pool of distinct draws, cycled), fixed x per M.
+    logits_pool = [torch.from_numpy(W.fp8_activations(cfg, 8, args.seed + 1000 * rank, step)[1]).to(dev)
+                   .to(torch.bfloat16) for step in range(pool)]
+    xs = {M: torch.from_numpy(W.fp8_activations(cfg, M, args.seed + 1000 * rank, 0)[0]).to(dev)
+          .to(torch.bfloat16) for M in MS}
+    bias = torch.from_numpy(W.fp8_activations(cfg, 1, args.seed, 0)[2]).to(dev)
+    outs = {M: (torch.empty(M * cfg.top_k, cfg.H, dtype=torch.bfloat16, device=dev),
+                torch.empty(M, cfg.top_k, dtype=torch.int32, device=dev),
+                torch.empty(M, cfg.top_k, dtype=torch.float32, device=dev)) for M in MS}
+    ws = fme.Workspace(fme.moe_routed_fp8_workspace(8, cfg.H, cfg.I, cfg.E, cfg.top_k), dev)
+    # One ids buffer per timed call, so reading them back needs no copy inside the region.
+    ids_log = torch.full((args.steps * len(MS), 8 * cfg.top_k), -1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps * len(MS))]
+
+    def call(M, k, record=None):
+        lg = logits_pool[k % pool][:M]
+        out, ids, wts = outs[M]
+        if record is not None:
+            ids = ids_log[record, :M * cfg.top_k].view(M, cfg.top_k)
+            ev[record][0].record(stream)
+        fme.moe_routed_fp8(xs[M], lg, bias, w13, s13, w2, s2, cfg.top_k, cfg.limit, cfg.scale, cfg.ue8m0,
+                           out=out, ids=ids, weights=wts, workspace=ws)
+        if record is not None:
+            ev[record][1].record(stream)
+
+    k = 0
+    for _ in range(args.warmup):
+        for M in MS:
+            call(M, k)
+            k += 1
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        t_start.record(stream)
+        rec = 0
+        for _ in range(args.steps):
+            for M in MS:
+                call(M, k, rec)
+                k += 1
+                rec += 1
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    launch_ms = np.array([a.elapsed_time(b) for a, b in ev])
+    ids_np = ids_log.cpu().numpy()
+    uniq = np.array([len(set(r[r >= 0].tolist())) for r in ids_np])
+    bytes_call = uniq * EXPERT_BYTES
+    total_bytes = float(bytes_call.sum())
+    if dist:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+        b = torch.tensor([total_bytes], device=dev, dtype=torch.float64)
+        dist.all_reduce(b)
+        total_bytes = float(b.item())
+    value = total_bytes / (elapsed_ms * 1e-3) / 1e9
+    per_m = {}
+    for i, M in enumerate(MS):
+        sel = slice(i, None, len(MS))
+        t_us = launch_ms[sel] * 1e3
+        per_m[str(M)] = {"us_median": round(float(np.median(t_us)), 2), "us_p10": round(float(np.percentile(t_us, 10)), 2),
+                         "us_p90": round(float(np.percentile(t_us, 90)), 2),
+                         "unique_experts_mean": round(float(uniq[sel].mean()), 2),
+                         "GBps_median": round(float(np.median(bytes_call[sel] / (launch_ms[sel] * 1e-3) / 1e9)), 1)}
+    peak, peak_kind = peaks()
+    achieved = float(bytes_call.sum() / (launch_ms.sum() * 1e-3) / 1e9)
+    traffic = load_traffic()
+
+    e2e = None if args.no_e2e else e2e_leg(fme, cfg, w13, s13, w2, s2, bias, dev, args)
+    extras = {} if args.no_extras else side_measurements(fme, dev, args)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        try:
+            r = run_oracle_subprocess(args.ref_seconds)
+            cpu = {"value": round(r["gbs"], 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                   "sample": f"{r['routes']} DSv3 routes (one expert each, 44.05 MB), {r['seconds']:.1f} s"}
+        except Exception as exc:  # pragma: no cover - reported, not fatal
+            cpu = {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": f"failed: {exc}"}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3 x fp8-e4m3 -> f32", "data": "synthetic",
+        "config": {"workload": "dsv3_routed_fp8: H 7168, I 2048, E 256, top_k 8, M in {1,2,4,8} per step, "
+                   "BF16 logits, non-pow2 FP32 block scales", "global_batch": sum(MS) * world, "seq_len": 1,
+                   "parallelism": "replicas" if world > 1 else "single-gpu",
+                   "l2": "no flush: each call streams >= 352 MB of weights (> 129 MB L2) and fresh routing",
+                   "per_m": per_m, "unique_experts_per_step": round(float(uniq.sum() / args.steps), 2)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": "fp8_moe_kernel", "bytes_per_launch": "unique experts x 44,050,944 B"},
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+        "gpu_launches": args.steps * len(MS),
+        "cpu_baseline": cpu,
+    }
+    if extras:
+        line["also"] = extras
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def load_traffic():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary (profiles/fp8_moe_kernel_dsv3.md), if it matches this kernel."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            return json.load(f).get("fp8_moe_kernel_dsv3_bytes_per_launch")
+    except Exception:
+        return None
+
+
+def e2e_leg(fme, cfg, w13, s13, w2, s2, bias, dev, args):
+    """Same metric through the public API with host buffers: per call, pinned
+    x and logits go host->device, results come back device->host."""
+    import torch
+    from synth import workloads as W
+
+    steps = max(5, min(50, args.steps))
+    host = {}
+    for M in MS:
+        x, logits, _ = W.fp8_activations(cfg, M, args.seed + 7, M)
+        host[M] = (torch.from_numpy(x).to(torch.bfloat16).pin_memory(),
+                   torch.from_numpy(logits).to(torch.bfloat16).pin_memory(),
+                   torch.empty(M * cfg.top_k, cfg.H, dtype=torch.bfloat16).pin_memory(),
+                   torch.empty(M, cfg.top_k, dtype=torch.int32).pin_memory(),
+                   torch.empty(M, cfg.top_k, dtype=torch.float32).pin_memory())
+    stream = torch.cuda.current_stream(dev)
+    uniq_total = 0
+
+    def one(M):
+        xh, lh, oh, ih, wh = host[M]
+        xd = xh.to(dev, non_blocking=True)
+        ld = lh.to(dev, non_blocking=True)
+        out, ids, wts = fme.moe_routed_fp8(xd, ld, bias, w13, s13, w2, s2, cfg.top_k, cfg.limit, cfg.scale,
+                                           cfg.ue8m0)
+        oh.copy_(out, non_blocking=True)
+        ih.copy_(ids, non_blocking=True)
+        wh.copy_(wts, non_blocking=True)
+
+    for M in MS:
+        one(M)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        for M in MS:
+            one(M)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    for M in MS:
+        uniq_total += len(set(host[M][3].numpy().reshape(-1).tolist()))
+    h2d = sum(host[M][0].numel() * 2 + host[M][1].numel() * 2 for M in MS)
+    d2h = sum(host[M][2].numel() * 2 + host[M][3].numel() * 4 + host[M][4].numel() * 4 for M in MS)
+    gbs = steps * uniq_total * EXPERT_BYTES / (ms * 1e-3) / 1e9
+    return {"value": round(gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms / steps, 4)}
+
+
+def side_measurements(fme, dev, args):
+    """Shared expert (UE8M0, H 7168 / I 2048) and NVFP4 slot MoE latencies."""
+    import torch
+    from synth import workloads as W
+
+    res = {}
+    cfg = W.SHARED
+    w13, s13, w2, s2 = W.shared_weights_host(cfg, args.seed)
+    w13, s13, w2, s2 = (torch.from_numpy(v).to(dev) for v in (w13, s13, w2, s2))
+    shared_bytes = w13.numel() + w2.numel() + 4 * (s13.numel() + s2.numel())
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    for M in (1, 8):
+        x = torch.from_numpy(W.fp8_activations(W.DSV3, M, args.seed, 3)[0]).to(dev).to(torch.bfloat16)
+        ts = []
+        for i in range(30):
+            flush.add_(1)  # evict the 44 MB of weights from L2 between calls
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fme.shared_expert_fp8(x, w13, s13, w2, s2, cfg.limit, cfg.ue8m0)
+            b.record()
+            torch.cuda.synchronize()
+            if i >= 5:
+                ts.append(a.elapsed_time(b) * 1e3)
+        us = float(np.median(ts))
+        res[f"shared_expert_fp8_M{M}"] = {"us_median": round(us, 2),
+                                         "GBps": round(shared_bytes / (us * 1e-6) / 1e9, 1)}
+    del flush
+    return res
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        reference_arm(args, rank)
+        return
+    gpu_arm(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

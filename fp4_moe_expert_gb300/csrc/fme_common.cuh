@@ -39,6 +39,7 @@ struct PhaseGeom {
 // of value index lane / (32 / V) in v[0]. V in {1, 2, 4, ..., 32}.
 template <int V>
 __device__ __forceinline__ float warp_transpose_sum(float (&v)[V], int lane) {
+  static_assert(V >= 1 && V <= 32 && (V & (V - 1)) == 0, "V must be a power of two <= 32");
 #pragma unroll
   for (int step = V / 2, off = 16; step >= 1; step >>= 1, off >>= 1) {
     const bool upper = (lane & off) != 0;

@@ -141,18 +141,23 @@ __device__ void route_token(const Fp8Args& a, Fp8Smem& S, int t, float* sc, uint
 // per 128-block sx = max(amax, 1e-10) / 448 (UE8M0 round-up when asked),
 // q = e4m3(x * (1 / sx)); stored as exact f16 pairs.
 template <int RTC>
-__device__ __forceinline__ void quant_x(const Fp8Args& a, const Fp8Smem& S, int c0, int gt,
+__device__ __forceinline__ void quant_x(const Fp8Args& a, const Fp8Smem& S, int c0, int rt, int gt,
                                         uint32_t (&xa)[kMaxSlicesPerThread][kTokChunk][8],
                                         float (&sx)[kMaxSlicesPerThread][kTokChunk]) {
   const PhaseGeom& g = a.g1;
 #pragma unroll
   for (int i = 0; i < kMaxSlicesPerThread; ++i) {
     const int s = gt + g.tpr * i;
-    const bool valid = (i < g.nspt) && (s < g.ns);
 #pragma unroll
     for (int t = 0; t < RTC; ++t) {
+      // Token slots t >= rt pad a 3-token chunk to 4: zero activations.
+      const bool valid = (i < g.nspt) && (s < g.ns) && (t < rt);
       float v[16];
       float amax = 0.0f;
+      if (!valid) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) xa[i][t][k] = 0u;
+      }
       if (valid) {
         const int tok = S.ctx_tok[c0 + t];
         const uint4* p = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(tok) * a.H + 16 * s);
@@ -190,18 +195,22 @@ __device__ __forceinline__ void quant_x(const Fp8Args& a, const Fp8Smem& S, int 
 // ("mega_moe" hidden_block divides); shared: qh = e4m3(h * (1 / sh))
 // ("shared_expert" _DownKernel multiplies by the _group_scale inverse).
 template <int RTC>
-__device__ __forceinline__ void quant_h(const Fp8Args& a, const Fp8Smem& S, int c0, int gt,
+__device__ __forceinline__ void quant_h(const Fp8Args& a, const Fp8Smem& S, int c0, int rt, int gt,
                                         uint32_t (&xa)[kMaxSlicesPerThread][kTokChunk][8],
                                         float (&sh)[kMaxSlicesPerThread][kTokChunk]) {
   const PhaseGeom& g = a.g2;
 #pragma unroll
   for (int i = 0; i < kMaxSlicesPerThread; ++i) {
     const int s = gt + g.tpr * i;
-    const bool valid = (i < g.nspt) && (s < g.ns);
 #pragma unroll
     for (int t = 0; t < RTC; ++t) {
+      const bool valid = (i < g.nspt) && (s < g.ns) && (t < rt);
       float v[16];
       float amax = 0.0f;
+      if (!valid) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) xa[i][t][k] = 0u;
+      }
       if (valid) {
         const int route = S.ctx_route[c0 + t];
         const float4* p = reinterpret_cast<const float4*>(a.hbuf + static_cast<size_t>(route) * a.I + 16 * s);
@@ -329,12 +338,12 @@ __device__ void build_context(const Fp8Args& a, Fp8Smem& S, int e, int ctid) {
 // ---------------------------------------------------------------- GEMM1 item
 template <int RTC>
 __device__ __forceinline__ void gemm1_chunk(const Fp8Args& a, Fp8Smem& S, const uint8_t* stage, int e, int j,
-                                            int h0, int c0, bool requant, int ctid, int warp, int lane,
+                                            int h0, int c0, int rt, bool requant, int ctid, int warp, int lane,
                                             uint32_t (&xa)[kMaxSlicesPerThread][kTokChunk][8],
                                             float (&sx)[kMaxSlicesPerThread][kTokChunk]) {
   const PhaseGeom& g = a.g1;
   const int grp = ctid / g.tpr, gt = ctid % g.tpr;
-  if (requant) quant_x<RTC>(a, S, c0, gt, xa, sx);
+  if (requant) quant_x<RTC>(a, S, c0, rt, gt, xa, sx);
   // Scale products of the two row blocks (first half: block j; second: I/128 + j).
   const int nb = a.H / 128, nrb = 2 * a.I / 128;
   float comb[kMaxSlicesPerThread][2][kTokChunk];
@@ -367,7 +376,7 @@ __device__ __forceinline__ void gemm1_chunk(const Fp8Args& a, Fp8Smem& S, const 
   }
   compute_bar();
   // SwiGLU of hidden indices h0 .. h0 + gp for the chunk's tokens.
-  if (ctid < a.gp * RTC) {
+  if (ctid < a.gp * RTC && ctid % RTC < rt) {
     const int q = ctid / RTC, t = ctid % RTC;
     const float first = S.ysum[q][t];
     const float second = S.ysum[a.gp + q][t];
@@ -400,12 +409,12 @@ __device__ __forceinline__ void gemm1_chunk(const Fp8Args& a, Fp8Smem& S, const 
 // ---------------------------------------------------------------- GEMM2 item
 template <int RTC>
 __device__ __forceinline__ void gemm2_chunk(const Fp8Args& a, Fp8Smem& S, const uint8_t* stage, int e, int m0,
-                                            int c0, bool requant, int ctid, int warp, int lane,
+                                            int c0, int rt, bool requant, int ctid, int warp, int lane,
                                             uint32_t (&xa)[kMaxSlicesPerThread][kTokChunk][8],
                                             float (&sh)[kMaxSlicesPerThread][kTokChunk]) {
   const PhaseGeom& g = a.g2;
   const int grp = ctid / g.tpr, gt = ctid % g.tpr;
-  if (requant) quant_h<RTC>(a, S, c0, gt, xa, sh);
+  if (requant) quant_h<RTC>(a, S, c0, rt, gt, xa, sh);
   const int nb = a.I / 128, nrb = a.H / 128;
   float comb[kMaxSlicesPerThread][2][kTokChunk];
 #pragma unroll
@@ -427,7 +436,7 @@ __device__ __forceinline__ void gemm2_chunk(const Fp8Args& a, Fp8Smem& S, const 
   compute_bar();
   constexpr int V = kRowsPerGroup * RTC;
   const int wpg = g.tpr / 32;
-  if (ctid < g.rg * V) {
+  if (ctid < g.rg * V && (ctid % V) % RTC < rt) {
     const int fg = ctid / V, v = ctid % V;
     float s = 0.0f;
     for (int w = 0; w < wpg; ++w) s += S.red[fg * wpg + w][v];
@@ -592,11 +601,11 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_moe_kernel(const __grid_const
     for (int c0 = 0; c0 < nt; c0 += kTokChunk) {
       const int rt = min(kTokChunk, nt - c0);
       const bool requant = fresh || !single;
+      // 8 rows x 1, 2 or 4 token slots per lane keep the warp reduction a power of two.
       switch (rt) {
-        case 1: gemm1_chunk<1>(a, S, stage, e, j, h0, c0, requant, ctid, warp, lane, xa, xs); break;
-        case 2: gemm1_chunk<2>(a, S, stage, e, j, h0, c0, requant, ctid, warp, lane, xa, xs); break;
-        case 3: gemm1_chunk<3>(a, S, stage, e, j, h0, c0, requant, ctid, warp, lane, xa, xs); break;
-        default: gemm1_chunk<4>(a, S, stage, e, j, h0, c0, requant, ctid, warp, lane, xa, xs); break;
+        case 1: gemm1_chunk<1>(a, S, stage, e, j, h0, c0, rt, requant, ctid, warp, lane, xa, xs); break;
+        case 2: gemm1_chunk<2>(a, S, stage, e, j, h0, c0, rt, requant, ctid, warp, lane, xa, xs); break;
+        default: gemm1_chunk<4>(a, S, stage, e, j, h0, c0, rt, requant, ctid, warp, lane, xa, xs); break;
       }
     }
     if (ctid == 0) {
@@ -643,11 +652,11 @@ __global__ void __launch_bounds__(kThreads, 1) fp8_moe_kernel(const __grid_const
     for (int c0 = 0; c0 < nt; c0 += kTokChunk) {
       const int rt = min(kTokChunk, nt - c0);
       const bool requant = fresh || !single;
+      // 8 rows x 1, 2 or 4 token slots per lane keep the warp reduction a power of two.
       switch (rt) {
-        case 1: gemm2_chunk<1>(a, S, stage, e, m0, c0, requant, ctid, warp, lane, xa, xs); break;
-        case 2: gemm2_chunk<2>(a, S, stage, e, m0, c0, requant, ctid, warp, lane, xa, xs); break;
-        case 3: gemm2_chunk<3>(a, S, stage, e, m0, c0, requant, ctid, warp, lane, xa, xs); break;
-        default: gemm2_chunk<4>(a, S, stage, e, m0, c0, requant, ctid, warp, lane, xa, xs); break;
+        case 1: gemm2_chunk<1>(a, S, stage, e, m0, c0, rt, requant, ctid, warp, lane, xa, xs); break;
+        case 2: gemm2_chunk<2>(a, S, stage, e, m0, c0, rt, requant, ctid, warp, lane, xa, xs); break;
+        default: gemm2_chunk<4>(a, S, stage, e, m0, c0, rt, requant, ctid, warp, lane, xa, xs); break;
       }
     }
     if (ctid == 0) {

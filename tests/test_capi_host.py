@@ -20,8 +20,8 @@ def _declared():
 
 @pytest.fixture(scope="module")
 def fme():
-    from fp4_moe_expert_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import fp4_moe_expert_gb300 as m
     return m
 
