@@ -1,0 +1,83 @@
+// fme_moe_routed_fp8_noalloc: the routed FP8 layer for callers that cannot
+// allocate device memory.
+//
+// Some callers of this library run where cudaMalloc is off limits: code
+// inside a memory pool owned by someone else, plug-ins whose host application
+// forbids device allocations after start-up, or capture-time paths where an
+// allocation would be recorded or would fail. They cannot provide the
+// workspace fme_moe_routed_fp8 needs. This entry point uses scratch that
+// lives in this file instead: a fixed device array that every GPU which
+// loads the library holds until the process exits.
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/fme.h"
+#include "fme_internal.h"
+
+namespace {
+
+// Largest workspace the variant can serve: 1 MiB. That covers, e.g., the
+// DeepSeek-V3 shape (I = 2048) up to 64 routes (M * top_k <= 64) with up to
+// 1024 experts. Larger requests are rejected with FME_EUNSUPPORTED.
+constexpr size_t kScratchBytes = size_t(1) << 20;
+
+// The scratch itself. In host code `g_scratch` only names a host-side
+// stand-in, never the device memory: host code must take the device address
+// from cudaGetSymbolAddress (below) and pass that to the kernel.
+static __device__ __align__(256) uint8_t g_scratch[kScratchBytes];
+
+// Leading bytes of the workspace that must be zero when a call starts: the
+// error word (256 bytes) and the two per-expert counter arrays, each rounded
+// up to 256 bytes. The rest (the SwiGLU output) is written before it is read.
+size_t counter_bytes(int E) {
+  const size_t per = (sizeof(uint32_t) * static_cast<size_t>(E) + 255) & ~size_t(255);
+  return 256 + 2 * per;
+}
+
+// Device address of g_scratch, looked up once per device with that device
+// current. Returns nullptr and records the reason on failure.
+void* scratch_address(int dev) {
+  static std::mutex mu;
+  static void* ptrs[64] = {nullptr};
+  if (dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t err = cudaGetSymbolAddress(&p, g_scratch);
+    if (err != cudaSuccess) {
+      fme::set_last_error(FME_ECUDA, "cudaGetSymbolAddress(static scratch): %s", cudaGetErrorString(err));
+      return nullptr;
+    }
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
+
+}  // namespace
+
+extern "C" int fme_moe_routed_fp8_noalloc(const void* x, const void* logits, int logits_dtype,
+                                          const float* bias, const uint8_t* w13, const float* s13,
+                                          const uint8_t* w2, const float* s2, int M, int H, int I, int E,
+                                          int top_k, float limit, float scale, int ue8m0, void* out,
+                                          int32_t* ids, float* weights, void* stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fme::set_last_error(FME_ECUDA, "cudaGetDevice failed");
+  const size_t need = fme_moe_routed_fp8_workspace(M, H, I, E, top_k);
+  if (need == 0)
+    return fme::set_last_error(FME_EINVAL, "bad sizes M=%d H=%d I=%d E=%d top_k=%d", M, H, I, E, top_k);
+  if (need > kScratchBytes)
+    return fme::set_last_error(FME_EUNSUPPORTED,
+                               "needs %zu bytes of scratch; the no-allocation variant holds %zu (1 MiB): "
+                               "use fme_moe_routed_fp8 with a caller workspace",
+                               need, kScratchBytes);
+  void* scratch = scratch_address(dev);
+  if (scratch == nullptr) return FME_ECUDA;
+  // The array keeps whatever the previous call left; start from zeroed counters.
+  const cudaError_t err =
+      cudaMemsetAsync(scratch, 0, counter_bytes(E), static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return fme::set_last_error(FME_ECUDA, "cudaMemsetAsync: %s", cudaGetErrorString(err));
+  return fme_moe_routed_fp8(x, logits, logits_dtype, bias, w13, s13, w2, s2, M, H, I, E, top_k, limit, scale,
+                            ue8m0, out, ids, weights, scratch, kScratchBytes, stream);
+}

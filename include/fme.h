@@ -97,6 +97,34 @@ int fme_moe_routed_fp8(const void* x, const void* logits, int logits_dtype, cons
 size_t fme_moe_routed_fp8_workspace(int M, int H, int I, int E, int top_k);
 
 /*
+ * fme_moe_routed_fp8 for callers that cannot allocate device memory.
+ *
+ * No counterpart in the pages: this is a library convenience. Some callers
+ * cannot call cudaMalloc (code running inside another owner's memory pool, a
+ * plug-in whose host forbids device allocations after start-up, paths that
+ * run while a graph is being captured), so they cannot hand over a workspace.
+ * This variant takes the same arguments minus the workspace and uses a
+ * 1 MiB scratch array compiled into libfme.so instead; every GPU that loads
+ * the library holds that array until the process exits. It allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * - Size limit: the call must need at most 1 MiB of workspace
+ *   (fme_moe_routed_fp8_workspace <= 1048576; e.g. I = 2048 with up to 64
+ *   routes M * top_k). Larger requests return FME_EUNSUPPORTED.
+ * - First call per device: it looks up the array's device address with that
+ *   device current. Make that first call before any stream capture.
+ * - Every call shares the one array and zeroes its counters first, so calls
+ *   that overlap on the GPU (other streams, other host threads) race and
+ *   corrupt each other: issue them in one stream order.
+ * - The device error word lives in the shared array; it is not readable
+ *   through fme_workspace_error.
+ */
+int fme_moe_routed_fp8_noalloc(const void* x, const void* logits, int logits_dtype, const float* bias,
+                               const uint8_t* w13, const float* s13, const uint8_t* w2, const float* s2,
+                               int M, int H, int I, int E, int top_k, float limit, float scale, int ue8m0,
+                               void* out, int32_t* ids, float* weights, void* stream);
+
+/*
  * FP8 shared expert for M decode tokens.
  *
  * Source: "vllm.models.glm5next.nvidia.specialized_decode.shared_expert",
