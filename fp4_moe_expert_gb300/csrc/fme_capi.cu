@@ -175,7 +175,7 @@ int fme_ue8m0_unpack(const int32_t* packed, int n, int k, float* dst, int check,
 
 size_t fme_moe_routed_nvfp4_workspace(int M, int H, int N, int L, int top_k) {
   if (M < 1 || M > kMaxTokens || H < 128 || H % 128 || N < 128 || N % 128 || L < 1 || L > kMaxExperts ||
-      top_k < 1 || top_k > kMaxTopK || H > 16384 || N > 16384)
+      top_k < 1 || top_k > kMaxTopK || H > 8192 || N > 8192)
     return 0;
   return nvfp4_workspace_bytes(M, H, N, L, top_k);
 }
@@ -188,7 +188,7 @@ int fme_moe_routed_nvfp4(const void* x, const int32_t* topk_ids, const float* to
   FME_REQUIRE(M >= 1 && M <= kMaxTokens, FME_EUNSUPPORTED, "M=%d outside [1, %d]", M, kMaxTokens);
   FME_REQUIRE(H >= 128 && H % 128 == 0 && N >= 128 && N % 128 == 0, FME_EINVAL,
               "H=%d and N=%d must be positive multiples of 128", H, N);
-  FME_REQUIRE(H <= 16384 && N <= 16384, FME_EUNSUPPORTED, "H=%d or N=%d above 16384", H, N);
+  FME_REQUIRE(H <= 8192 && N <= 8192, FME_EUNSUPPORTED, "H=%d or N=%d above 8192", H, N);
   FME_REQUIRE(L >= 1 && L <= kMaxExperts, FME_EUNSUPPORTED, "L=%d outside [1, %d]", L, kMaxExperts);
   FME_REQUIRE(top_k >= 1 && top_k <= kMaxTopK, FME_EINVAL, "top_k=%d outside [1, %d]", top_k, kMaxTopK);
   FME_REQUIRE(limit > 0.0f, FME_EINVAL, "limit must be > 0");

@@ -182,8 +182,8 @@ int fme_ue8m0_unpack(const int32_t* packed, int n, int k, float* dst, int check,
  *   or out-of-range ids are simply non-local); topk_weights [M, top_k] FP32;
  *   w13 [L, 2N, H/2] packed E2M1 (element 2i in the low nibble), s13
  *   [L, 2N, H/16] UE4M3 bytes; w2 [L, H, N/2], s2 [L, H, N/16]; limit > 0
- *   (+inf: no clamp). M in [1, 64], H multiple of 128 and <= 16384, N
- *   multiple of 128 and <= 16384, L in [1, 1024], top_k in [1, 32].
+ *   (+inf: no clamp). M in [1, 64], H and N multiples of 128 and <= 8192,
+ *   L in [1, 1024], top_k in [1, 32]; a token's ids must be distinct.
  *   y [M, H] BF16.
  */
 int fme_moe_routed_nvfp4(const void* x, const int32_t* topk_ids, const float* topk_weights,

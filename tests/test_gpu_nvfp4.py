@@ -1,0 +1,102 @@
+"""GPU parity of the NVFP4 slot MoE and of the packed-UE8M0 scale unpacking
+against the oracle, through the C ABI."""
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_fp8, moe_nvfp4, routing
+from synth import workloads as W
+from tests.parity import assert_outputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def fme():
+    import fp4_moe_expert_gb300 as m
+    return m
+
+
+def _host_weights(cfg, seed):
+    w13, s13, w2, s2 = W.nvfp4_weights_host(cfg, seed)
+    return w13, s13, w2, s2
+
+
+def _run(fme, cfg, M, seed, weights_scale=1.0, tokens=None, device_weights=False):
+    w13h, s13h, w2h, s2h = _host_weights(cfg, seed)
+    if device_weights:
+        w13, s13, w2, s2 = W.nvfp4_weights_device(cfg, seed, DEV)
+    else:
+        w13, s13, w2, s2 = (torch.from_numpy(h.full()).to(DEV) for h in (w13h, s13h, w2h, s2h))
+    x, logits, bias = W.nvfp4_activations(cfg, M, seed)
+    ids, wts, _ = routing.route(logits, bias, cfg.top_k, 1.0)
+    wts = (wts * np.float32(weights_scale)).astype(np.float32)
+    y = fme.moe_routed_nvfp4(torch.from_numpy(x).to(DEV).to(torch.bfloat16), torch.from_numpy(ids).to(DEV),
+                             torch.from_numpy(wts).to(DEV), w13, s13, w2, s2, cfg.e0, cfg.limit)
+    torch.cuda.synchronize()
+    sel = np.arange(M) if tokens is None else np.asarray(tokens)
+    ref = moe_nvfp4.routed_nvfp4(x[sel], ids[sel], wts[sel], w13h, s13h, w2h, s2h, cfg.e0, cfg.L, cfg.limit)
+    return y.float().cpu().numpy()[sel], ref, ids
+
+
+SMALL = W.Nvfp4Config("nvfp4_small", 256, 128, 6, 12, 3, 3, float("inf"), (5,))
+RAGGED = W.Nvfp4Config("nvfp4_ragged", 1024, 384, 10, 40, 20, 4, float("inf"), (7,))
+
+
+@pytest.mark.parametrize("cfg,M", [(SMALL, 5), (RAGGED, 7), (dataclasses.replace(SMALL, limit=2.0), 6)])
+def test_nvfp4_small_full_parity(fme, cfg, M):
+    got, ref, ids = _run(fme, cfg, M, seed=41)
+    local = ((ids >= cfg.e0) & (ids < cfg.e0 + cfg.L)).any(axis=1)
+    assert (got[~local] == 0).all()
+    nz = local
+    if nz.any():
+        assert_outputs(got[nz], ref[nz])
+
+
+def test_nvfp4_weights_applied_once_on_gpu(fme):
+    got1, ref1, _ = _run(fme, RAGGED, 6, seed=42)
+    got2, ref2, _ = _run(fme, RAGGED, 6, seed=42, weights_scale=2.0)
+    assert np.array_equal(got2, 2 * got1)  # exact: power-of-two scaling of FP32 sums before one BF16 rounding
+    assert np.array_equal(ref2, 2 * ref1)
+
+
+def test_nvfp4_no_local_slots_gives_zeros(fme):
+    cfg = dataclasses.replace(SMALL, e0=100)
+    got, ref, _ = _run(fme, cfg, 4, seed=43)
+    assert (got == 0).all() and (ref == 0).all()
+
+
+def test_nvfp4_full_size_m8(fme):
+    got, ref, ids = _run(fme, W.NVFP4, 8, seed=44, device_weights=True)
+    local = ((ids >= 0) & (ids < W.NVFP4.L)).any(axis=1)
+    assert local.any()
+    assert_outputs(got[local], ref[local])
+
+
+def test_nvfp4_full_size_m64_sampled_tokens(fme):
+    got, ref, ids = _run(fme, W.NVFP4, 64, seed=45, tokens=[3, 40], device_weights=True)
+    for i, t in enumerate([3, 40]):
+        if ((ids[t] >= 0) & (ids[t] < W.NVFP4.L)).any():
+            assert_outputs(got[i:i + 1], ref[i:i + 1])
+        else:
+            assert (got[i] == 0).all()
+
+
+def test_ue8m0_unpack_matches_oracle_and_detects_mismatch(fme):
+    rng = np.random.default_rng(46)
+    n, k = 512, 2048
+    exps = rng.integers(100, 140, size=(n // 128, k // 128)).astype(np.uint32)
+    per_row = np.repeat(exps, 128, axis=0)  # uniform inside each 128-row block
+    packed = np.zeros((n, k // 512), np.uint32)
+    for g in range(k // 128):
+        packed[:, g // 4] |= per_row[:, g] << np.uint32(8 * (g % 4))
+    dev = torch.from_numpy(packed.view(np.int32)).to(DEV)
+    got = fme.ue8m0_unpack(dev, n, k).cpu().numpy()
+    assert np.array_equal(got, moe_fp8.ue8m0_unpack(packed.view(np.int32), n, k))
+    packed[300, 1] ^= np.uint32(1 << 8)
+    with pytest.raises(ValueError):
+        fme.ue8m0_unpack(torch.from_numpy(packed.view(np.int32)).to(DEV), n, k)
