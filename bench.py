@@ -219,6 +219,9 @@ def gpu_arm(args, rank, world, local_rank):
             call(M, k)
             k += 1
     torch.cuda.synchronize()
+    code = ws.error()
+    if code:
+        raise SystemExit(f"device error word 0x{code:x} during warm-up: refusing to time a failing kernel")
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -237,6 +240,9 @@ def gpu_arm(args, rank, world, local_rank):
     if dist:
         dist.barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
+    code = ws.error()
+    if code:
+        raise SystemExit(f"device error word 0x{code:x} in the timed region")
     launch_ms = np.array([a.elapsed_time(b) for a, b in ev])
     ids_np = ids_log.cpu().numpy()
     uniq = np.array([len(set(r[r >= 0].tolist())) for r in ids_np])

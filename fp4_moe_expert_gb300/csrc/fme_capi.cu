@@ -126,7 +126,7 @@ static int check_fp8_shapes(int M, int H, int I, int E, int top_k, float limit) 
 
 size_t fme_moe_routed_fp8_workspace(int M, int H, int I, int E, int top_k) {
   if (check_fp8_shapes(M, H, I, E, top_k, 1.0f) != FME_OK) return 0;
-  return fp8_workspace_bytes(M * top_k, I, E);
+  return fp8_workspace_bytes(M, M * top_k, H, I, E);
 }
 
 int fme_moe_routed_fp8(const void* x, const void* logits, int logits_dtype, const float* bias, const uint8_t* w13,
@@ -149,7 +149,7 @@ int fme_moe_routed_fp8(const void* x, const void* logits, int logits_dtype, cons
 
 size_t fme_shared_expert_fp8_workspace(int M, int H, int I) {
   if (check_fp8_shapes(M, H, I, 1, 1, 1.0f) != FME_OK) return 0;
-  return fp8_workspace_bytes(M, I, 1);
+  return fp8_workspace_bytes(M, M, H, I, 1);
 }
 
 int fme_shared_expert_fp8(const void* x, const uint8_t* w13, const float* s13, const uint8_t* w2, const float* s2,

@@ -20,6 +20,7 @@ constexpr int kMaxSlicesPerThread = 2;             // 16-byte K slices per threa
 constexpr int kMaxTokens = 64;                     // token bit masks are uint64
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
+constexpr int kFp8MaxCtas = 160;                 // grid cap of the FP8 kernel (partial slots)
 
 // Device error bits (workspace error word).
 constexpr uint32_t kErrRingWait = 1u;  // a ring stage never landed

@@ -22,7 +22,9 @@ bool ensure_smem_attr(int dev, const void* kernel, size_t bytes);
 // override, default 1000 ms).
 unsigned long long wait_timeout_ns();
 
-size_t fp8_workspace_bytes(int routes, int I, int E);
+size_t fp8_workspace_bytes(int M, int routes, int H, int I, int E);
+// Leading workspace bytes (error word and counters) that must be zero when a call starts.
+size_t fp8_workspace_zero_bytes(int M, int routes, int H, int I, int E);
 size_t nvfp4_workspace_bytes(int M, int H, int N, int L, int top_k);
 
 int routed_fp8(const void* x, const void* logits, int logits_dtype, const float* bias, const uint8_t* w13,

@@ -18,23 +18,15 @@
 
 namespace {
 
-// Largest workspace the variant can serve: 1 MiB. That covers, e.g., the
-// DeepSeek-V3 shape (I = 2048) up to 64 routes (M * top_k <= 64) with up to
-// 1024 experts. Larger requests are rejected with FME_EUNSUPPORTED.
-constexpr size_t kScratchBytes = size_t(1) << 20;
+// Largest workspace the variant can serve: 8 MiB. That covers, e.g., the
+// DeepSeek-V3 shape (H = 7168, I = 2048, 256 experts, top_k 8) up to M = 16
+// tokens. Larger requests are rejected with FME_EUNSUPPORTED.
+constexpr size_t kScratchBytes = size_t(8) << 20;
 
 // The scratch itself. In host code `g_scratch` only names a host-side
 // stand-in, never the device memory: host code must take the device address
 // from cudaGetSymbolAddress (below) and pass that to the kernel.
 static __device__ __align__(256) uint8_t g_scratch[kScratchBytes];
-
-// Leading bytes of the workspace that must be zero when a call starts: the
-// error word (256 bytes) and the two per-expert counter arrays, each rounded
-// up to 256 bytes. The rest (the SwiGLU output) is written before it is read.
-size_t counter_bytes(int E) {
-  const size_t per = (sizeof(uint32_t) * static_cast<size_t>(E) + 255) & ~size_t(255);
-  return 256 + 2 * per;
-}
 
 // Device address of g_scratch, looked up once per device with that device
 // current. Returns nullptr and records the reason on failure.
@@ -69,14 +61,16 @@ extern "C" int fme_moe_routed_fp8_noalloc(const void* x, const void* logits, int
     return fme::set_last_error(FME_EINVAL, "bad sizes M=%d H=%d I=%d E=%d top_k=%d", M, H, I, E, top_k);
   if (need > kScratchBytes)
     return fme::set_last_error(FME_EUNSUPPORTED,
-                               "needs %zu bytes of scratch; the no-allocation variant holds %zu (1 MiB): "
+                               "needs %zu bytes of scratch; the no-allocation variant holds %zu (8 MiB): "
                                "use fme_moe_routed_fp8 with a caller workspace",
                                need, kScratchBytes);
   void* scratch = scratch_address(dev);
   if (scratch == nullptr) return FME_ECUDA;
-  // The array keeps whatever the previous call left; start from zeroed counters.
+  // The array keeps whatever the previous call left; start from a zeroed
+  // error word and zeroed counters (the rest is written before it is read).
   const cudaError_t err =
-      cudaMemsetAsync(scratch, 0, counter_bytes(E), static_cast<cudaStream_t>(stream));
+      cudaMemsetAsync(scratch, 0, fme::fp8_workspace_zero_bytes(M, M * top_k, H, I, E),
+                      static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return fme::set_last_error(FME_ECUDA, "cudaMemsetAsync: %s", cudaGetErrorString(err));
   return fme_moe_routed_fp8(x, logits, logits_dtype, bias, w13, s13, w2, s2, M, H, I, E, top_k, limit, scale,
                             ue8m0, out, ids, weights, scratch, kScratchBytes, stream);

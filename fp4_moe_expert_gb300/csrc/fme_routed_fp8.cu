@@ -1,32 +1,35 @@
-// Routed FP8 MoE layer and FP8 shared expert: one persistent sm_103a kernel.
+// Routed FP8 MoE layer and FP8 shared expert on the sm_103a tensor cores.
 //
 // Computes what "vllm.models.glm5next.nvidia.specialized_decode.mega_moe"
 // (MegaExperts / _MegaKernel) and ".../shared_expert" (SharedExpert,
-// _GateUpKernel, _DownKernel, _group_scale) define; the design is this
+// _GateUpKernel, _DownKernel, _group_scale) define. The design is this
 // library's own:
 //
-// * One CTA per SM. Every CTA redoes the routing of all M tokens (warp per
-//   token) and derives the same ascending list of the unique experts touched,
-//   so each touched expert's weights stream from HBM once per call whatever
-//   the number of routes that picked it (the page streams per route).
-// * Work items: GEMM1 items are 4*rg rows of "first half" W13 rows plus the
-//   matching 4*rg rows of the second half (so SwiGLU finishes inside the
-//   item); GEMM2 items are 8*rg rows of W2. Every CTA owns an equal slice of
-//   the GEMM1 items, then an equal slice of the GEMM2 items.
-// * Thread 0 streams each item's rows with cp.async.bulk into a 3-stage
-//   shared-memory ring (one mbarrier per stage, L2 evict-first), kStages
-//   items ahead of the compute; every item ends on a CTA barrier, after which
-//   its stage is refilled, also across the GEMM1 -> GEMM2 boundary.
-// * Eight warps hold the quantised activations of up to four tokens
-//   in registers (as exact f16 pairs) and stream weight rows from the ring:
-//   cvt.rn.f16x2.e4m3x2 then fma.rn.f32.f16 (exact products, f32 sums); each
-//   16-element partial is multiplied by its block's (weight scale * activation
-//   scale) product, and a warp transpose-reduction plus a fixed-order
-//   cross-warp sum give each row's dot product.
-// * GEMM1 items write the SwiGLU output (f32) to the workspace and release a
-//   per-expert counter; GEMM2 items wait (bounded) for all GEMM1 items of
-//   their expert, then quantise the hidden per 128 themselves.
-#include <cstdio>
+// * One persistent CTA per SM, six warps: warp 0 streams weight tiles with
+//   TMA (128-byte swizzle, 8 x 16 KB ring, L2 evict-first); warp 1 owns the
+//   tensor memory and issues tcgen05.mma kind::f8f6f4 (M = 128 weight rows,
+//   N = 16 * ceil(tokens / 16), K = 32); warps 2-5 quantise the activations
+//   into the B operand and run the epilogue. Every warp first redoes the
+//   routing of all tokens, so each CTA derives the same list of the unique
+//   experts touched and each expert's weights stream from HBM once.
+// * The block scales are FP32 and not powers of two, so the MMA cannot apply
+//   them: each 128-wide K block accumulates into its own group of TMEM
+//   columns, and the epilogue multiplies every block's partial by
+//   (weight scale x activation scale) and sums (the page's one-column-per-K-
+//   block idea, with the tokens as the columns of one group).
+// * Work is split stream-K style: GEMM1 is (expert, tile of 64 first-half
+//   rows + the 64 matching second-half rows, K block) slots, GEMM2 is
+//   (expert, tile of 128 rows, K block) slots; every CTA owns an equal
+//   contiguous slice of each phase. A tile cut by slice boundaries is summed
+//   by its last contributor, in CTA order, from partials in the workspace.
+// * A finished GEMM1 tile writes its SwiGLU output (f32) to the workspace and
+//   releases a per-expert counter; GEMM2 work of that expert waits for all of
+//   its GEMM1 tiles (bounded wait), then quantises the hidden per 128 itself.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
 
 #include "fme_common.cuh"
 #include "fme_internal.h"
@@ -35,60 +38,75 @@ namespace fme {
 
 enum : int { kModeRouted = 0, kModeShared = 1 };
 
-struct Fp8Args {
+constexpr int kTcThreads = 192;
+constexpr int kTcStages = 8;
+constexpr int kAStageBytes = 128 * 128;  // one 128-row x 128-byte K block of weights
+constexpr int kBBufBytes = 256 * 128;    // K blocks x N token rows x 128 bytes <= 256 rows
+constexpr int kTmemCols = 512;
+constexpr int kTmemBuf = 256;            // two accumulator buffers
+constexpr int kMaxKc = 16;
+constexpr int kTokGroups = kMaxTokens / 16;
+
+struct TcArgs {
+  CUtensorMap map13;  // W13 as [E * 2I rows, H bytes], box 64 rows x 128 bytes
+  CUtensorMap map2;   // W2 as [E * H rows, I bytes]
   const __nv_bfloat16* x;
   const void* logits;
   const float* bias;
-  const uint8_t* w13;
   const float* s13;
-  const uint8_t* w2;
   const float* s2;
   __nv_bfloat16* out;
   int32_t* ids;
   float* weights;
-  __nv_bfloat16* gate_up;  // shared mode, optional
+  __nv_bfloat16* gate_up;
   uint32_t* err;
-  uint32_t* done;      // [E] GEMM1 items completed per expert
-  uint32_t* consumed;  // [E] GEMM2 items that passed the wait
-  float* hbuf;         // [routes, I] SwiGLU output
+  uint32_t* done;    // [E] GEMM1 tiles finished per expert
+  uint32_t* passed;  // [E] CTAs whose GEMM2 work passed the wait
+  uint32_t* cnt1;    // [E * I/64] contributors arrived per GEMM1 tile (expert id, tile)
+  uint32_t* cnt2;    // [E * H/128] per GEMM2 tile
+  float* hbuf;       // [routes, I] SwiGLU output
+  float* part;       // [2 phases][kFp8MaxCtas][2 slots][tokens][128 rows] split-tile partials
   int M, H, I, E, top_k;
+  int ptok;          // token rows of one partial slot (min(M, 64))
   float limit, scale;
   int ue8m0, logits_f32, mode;
-  PhaseGeom g1, g2;
-  int gp;  // first-half rows per GEMM1 item (the item has 2 * gp rows)
-  int r2;  // rows per GEMM2 item
   unsigned long long timeout_ns;
 };
 
-struct Fp8Smem {
-  uint8_t ring[kStages][kStageBytes];
-  uint64_t full[kStages];
+struct TcSmem {
+  uint8_t A[kTcStages][kAStageBytes];
+  uint8_t B[2][kBBufBytes];
+  float xs[2][kMaxTokens][kMaxKc];  // activation block scales per B buffer
+  float ysm[16][64];                // SwiGLU exchange (16 tokens x 64 rows)
+  uint64_t full[kTcStages], empty[kTcStages];
+  uint64_t bfull[2], accfull[2], tmemfree[2], final_bar;
   unsigned long long tokmask[kMaxExperts];
   int16_t rid[kMaxTokens * kMaxTopK];
   int16_t ulist[kMaxExperts];
-  float red[kComputeWarps][32];
-  float ysum[64][kTokChunk];
-  int16_t ctx_route[kMaxTokens];
-  int16_t ctx_tok[kMaxTokens];
-  int ctx_n;
-  int U;
+  int16_t ctx_route[2][kMaxTokens];  // routes of each B buffer's expert, in token order
+  int ctx_n[2];
+  int dirty[2];  // B rows >= dirty[b] are zero in every K block of buffer b
+  uint32_t tmem_base;
+  int U, rmax;
+  int flag;
   volatile int abort;
 };
 
-constexpr size_t kFp8SmemBytes = sizeof(Fp8Smem) + 1024;
+constexpr size_t kTcSmemBytes = sizeof(TcSmem) + 1024;
 
-__device__ __forceinline__ void set_error(const Fp8Args& a, Fp8Smem& S, uint32_t bit) {
+__device__ __forceinline__ void tc_error(const TcArgs& a, TcSmem& S, uint32_t bit) {
   atomicOr(a.err, bit);
   S.abort = 1;
 }
+
+__device__ __forceinline__ void epi_bar() { named_bar_sync(1, 128); }
 
 // ---------------------------------------------------------------- routing
 // One warp routes token t ("mega_moe" _MegaKernel.top_k_pick): sigmoid scores
 // (accurate expf, IEEE divide), keys score + bias as monotone uint32, top_k
 // rounds of warp max key then lowest expert among equals, weights
 // score / (float sum in pick order) * scale.
-__device__ void route_token(const Fp8Args& a, Fp8Smem& S, int t, float* sc, uint32_t* ky, int lane,
-                            bool write_out) {
+__device__ void route_token(const TcArgs& a, TcSmem& S, int t, float* sc, uint32_t* ky, int lane, bool write_out) {
   const int E = a.E;
   for (int e = lane; e < E; e += 32) {
     float l;
@@ -101,8 +119,7 @@ __device__ void route_token(const Fp8Args& a, Fp8Smem& S, int t, float* sc, uint
     ky[e] = ordered_key(__fadd_rn(s, __ldg(a.bias + e)));
   }
   __syncwarp();
-  float total = 0.0f;
-  float mine = 0.0f;
+  float total = 0.0f, mine = 0.0f;
   int mine_e = 0;
   for (int r = 0; r < a.top_k; ++r) {
     uint32_t best = 0u;
@@ -136,183 +153,79 @@ __device__ void route_token(const Fp8Args& a, Fp8Smem& S, int t, float* sc, uint
   }
 }
 
-// ---------------------------------------------------------------- activations
-// Quantise the x slices this thread owns for tokens ctx_tok[c0 .. c0+RTC):
-// per 128-block sx = max(amax, 1e-10) / 448 (UE8M0 round-up when asked),
-// q = e4m3(x * (1 / sx)); stored as exact f16 pairs.
-template <int RTC>
-__device__ __forceinline__ void quant_x(const Fp8Args& a, const Fp8Smem& S, int c0, int rt, int gt,
-                                        uint32_t (&xa)[kMaxSlicesPerThread][kTokChunk][8],
-                                        float (&sx)[kMaxSlicesPerThread][kTokChunk]) {
-  const PhaseGeom& g = a.g1;
-#pragma unroll
-  for (int i = 0; i < kMaxSlicesPerThread; ++i) {
-    const int s = gt + g.tpr * i;
-#pragma unroll
-    for (int t = 0; t < RTC; ++t) {
-      // Token slots t >= rt pad a 3-token chunk to 4: zero activations.
-      const bool valid = (i < g.nspt) && (s < g.ns) && (t < rt);
-      float v[16];
-      float amax = 0.0f;
-      if (!valid) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) xa[i][t][k] = 0u;
+// ---------------------------------------------------------------- work plan
+// Each phase's slots are split over Ge = min(G, n) CTAs: CTA c < Ge owns
+// [n*c/Ge, n*(c+1)/Ge), never empty; CTAs c >= Ge own nothing.
+struct PhasePlan {
+  long long n, lo, hi;
+  int Ge, tiles, nb;
+  __device__ long long lo_of(int c) const { return c >= Ge ? n : n * c / Ge; }
+  // The CTA whose slice holds slot x.
+  __device__ int cta_of(long long x) const { return static_cast<int>(((x + 1) * Ge + n - 1) / n) - 1; }
+};
+
+struct Plan {
+  int U, N, kcmax, c;
+  PhasePlan p[2];
+};
+
+__device__ void make_phase(PhasePlan& pp, long long n, int tiles, int nb, int G, int c) {
+  pp.n = n;
+  pp.tiles = tiles;
+  pp.nb = nb;
+  pp.Ge = static_cast<int>(min(static_cast<long long>(G), n));
+  pp.lo = pp.lo_of(c);
+  pp.hi = pp.lo_of(c + 1 > pp.Ge ? pp.Ge : c + 1);
+  if (c >= pp.Ge) pp.lo = pp.hi = n;
+}
+
+struct Chunk {
+  int phase, u, T, kb0, kc;
+  long long tile, t0;  // global tile index and its first slot
+  bool last_of_seg;
+};
+
+// Walks this CTA's slots of both phases in chunks of at most kcmax K blocks
+// that never cross a tile.
+struct Cursor {
+  long long pos;
+  int phase;
+  __device__ bool next(const Plan& P, Chunk& ch) {
+    while (true) {
+      const PhasePlan& pp = P.p[phase - 1];
+      if (pos < pp.lo) pos = pp.lo;
+      if (pos < pp.hi) {
+        const long long tile = pos / pp.nb;
+        const long long t0 = tile * pp.nb;
+        const long long seg1 = min(pp.hi, t0 + pp.nb);
+        ch.phase = phase;
+        ch.u = static_cast<int>(tile / pp.tiles);
+        ch.T = static_cast<int>(tile % pp.tiles);
+        ch.tile = tile;
+        ch.t0 = t0;
+        ch.kb0 = static_cast<int>(pos - t0);
+        ch.kc = static_cast<int>(min(static_cast<long long>(P.kcmax), seg1 - pos));
+        ch.last_of_seg = pos + ch.kc == seg1;
+        pos += ch.kc;
+        return true;
       }
-      if (valid) {
-        const int tok = S.ctx_tok[c0 + t];
-        const uint4* p = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(tok) * a.H + 16 * s);
-        const uint4 q0 = __ldg(p), q1 = __ldg(p + 1);
-        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          v[2 * k] = __uint_as_float(w[k] << 16);
-          v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-        }
-#pragma unroll
-        for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(v[k]));
-      }
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
-      if (valid) {
-        float scale = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
-        if (a.ue8m0) scale = ue8m0_ceil(scale);
-        const float inv = __fdiv_rn(1.0f, scale);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t lo = f32x2_to_e4m3x2(__fmul_rn(v[4 * k], inv), __fmul_rn(v[4 * k + 1], inv));
-          const uint32_t hi = f32x2_to_e4m3x2(__fmul_rn(v[4 * k + 2], inv), __fmul_rn(v[4 * k + 3], inv));
-          e4m3x4_to_f16x2x2(lo | (hi << 16), xa[i][t][2 * k], xa[i][t][2 * k + 1]);
-        }
-        sx[i][t] = scale;
-      }
+      if (phase == 2) return false;
+      phase = 2;
+      pos = P.p[1].lo;
     }
   }
-}
+};
 
-// Quantise the hidden slices this thread owns for routes ctx_route[c0 ..):
-// sh = max(amax, 1e-10) / 448 (UE8M0 when asked); routed: qh = e4m3(h / sh)
-// ("mega_moe" hidden_block divides); shared: qh = e4m3(h * (1 / sh))
-// ("shared_expert" _DownKernel multiplies by the _group_scale inverse).
-template <int RTC>
-__device__ __forceinline__ void quant_h(const Fp8Args& a, const Fp8Smem& S, int c0, int rt, int gt,
-                                        uint32_t (&xa)[kMaxSlicesPerThread][kTokChunk][8],
-                                        float (&sh)[kMaxSlicesPerThread][kTokChunk]) {
-  const PhaseGeom& g = a.g2;
-#pragma unroll
-  for (int i = 0; i < kMaxSlicesPerThread; ++i) {
-    const int s = gt + g.tpr * i;
-#pragma unroll
-    for (int t = 0; t < RTC; ++t) {
-      const bool valid = (i < g.nspt) && (s < g.ns) && (t < rt);
-      float v[16];
-      float amax = 0.0f;
-      if (!valid) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) xa[i][t][k] = 0u;
-      }
-      if (valid) {
-        const int route = S.ctx_route[c0 + t];
-        const float4* p = reinterpret_cast<const float4*>(a.hbuf + static_cast<size_t>(route) * a.I + 16 * s);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float4 f = __ldcg(p + k);
-          v[4 * k] = f.x;
-          v[4 * k + 1] = f.y;
-          v[4 * k + 2] = f.z;
-          v[4 * k + 3] = f.w;
-        }
-#pragma unroll
-        for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(v[k]));
-      }
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
-      if (valid) {
-        float scale = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
-        if (a.ue8m0) scale = ue8m0_ceil(scale);
-        float q[16];
-        if (a.mode == kModeRouted) {
-#pragma unroll
-          for (int k = 0; k < 16; ++k) q[k] = __fdiv_rn(v[k], scale);
-        } else {
-          const float inv = __fdiv_rn(1.0f, scale);
-#pragma unroll
-          for (int k = 0; k < 16; ++k) q[k] = __fmul_rn(v[k], inv);
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t lo = f32x2_to_e4m3x2(q[4 * k], q[4 * k + 1]);
-          const uint32_t hi = f32x2_to_e4m3x2(q[4 * k + 2], q[4 * k + 3]);
-          e4m3x4_to_f16x2x2(lo | (hi << 16), xa[i][t][2 * k], xa[i][t][2 * k + 1]);
-        }
-        sh[i][t] = scale;
-      }
-    }
-  }
-}
-
-// ---------------------------------------------------------------- row dot products
-// acc[q * RTC + t] += sum over this thread's slices of the 16-element dot of
-// row (row0 + q) with token t's activations, times the slice's scale product.
-// `split`: rows >= split use comb[.][1], others comb[.][0].
-template <int RTC>
-__device__ __forceinline__ void dot_rows(const uint8_t* stage, int rowbytes, int row0, int split, int gt,
-                                         const PhaseGeom& g,
-                                         const uint32_t (&xa)[kMaxSlicesPerThread][kTokChunk][8],
-                                         const float (&comb)[kMaxSlicesPerThread][2][kTokChunk],
-                                         float (&acc)[kRowsPerGroup * RTC]) {
-#pragma unroll
-  for (int q = 0; q < kRowsPerGroup; ++q) {
-    const int row = row0 + q;
-    const bool second = row >= split;
-    const uint8_t* rp = stage + static_cast<size_t>(row) * rowbytes;
-#pragma unroll
-    for (int i = 0; i < kMaxSlicesPerThread; ++i) {
-      const int s = gt + g.tpr * i;
-      if ((i < g.nspt) && (s < g.ns)) {
-        const uint4 w = *reinterpret_cast<const uint4*>(rp + 16 * s);
-        uint32_t wf[8];
-        e4m3x4_to_f16x2x2(w.x, wf[0], wf[1]);
-        e4m3x4_to_f16x2x2(w.y, wf[2], wf[3]);
-        e4m3x4_to_f16x2x2(w.z, wf[4], wf[5]);
-        e4m3x4_to_f16x2x2(w.w, wf[6], wf[7]);
-#pragma unroll
-        for (int t = 0; t < RTC; ++t) {
-          float p = 0.0f;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) p = fma_f16x2_f32(wf[k], xa[i][t][k], p);
-          const float c = second ? comb[i][1][t] : comb[i][0][t];
-          acc[q * RTC + t] = fmaf(p, c, acc[q * RTC + t]);
-        }
-      }
-    }
-  }
-}
-
-// Reduce acc over the threads of each row group; results land in
-// S.red[warp][v] (v = q * RTC + t) for the group's warps. Caller syncs.
-template <int RTC>
-__device__ __forceinline__ void reduce_to_smem(Fp8Smem& S, float (&acc)[kRowsPerGroup * RTC], int warp,
-                                               int lane) {
-  constexpr int V = kRowsPerGroup * RTC;
-  const float s = warp_transpose_sum<V>(acc, lane);
-  if ((lane % (32 / V)) == 0) S.red[warp][lane / (32 / V)] = s;
-}
-
-__device__ __forceinline__ void compute_bar() { named_bar_sync(1, kComputeThreads); }
-
-// ---------------------------------------------------------------- context (routes of an expert)
-__device__ void build_context(const Fp8Args& a, Fp8Smem& S, int e, int ctid) {
-  if (ctid < 32) {
-    const int lane = ctid;
+// ---------------------------------------------------------------- B operand fill
+// Routes of expert u (token order) into ctx_route[b].
+__device__ void fill_context(const TcArgs& a, TcSmem& S, int u, int b, int etid) {
+  if (etid < 32) {
+    const int lane = etid;
     if (a.mode == kModeShared) {
-      for (int t = lane; t < a.M; t += 32) {
-        S.ctx_route[t] = static_cast<int16_t>(t);
-        S.ctx_tok[t] = static_cast<int16_t>(t);
-      }
-      if (lane == 0) S.ctx_n = a.M;
+      for (int t = lane; t < a.M; t += 32) S.ctx_route[b][t] = static_cast<int16_t>(t);
+      if (lane == 0) S.ctx_n[b] = a.M;
     } else {
+      const int e = S.ulist[u];
       const unsigned long long mask = S.tokmask[e];
       int base = 0;
       for (int t0 = 0; t0 < a.M; t0 += 32) {
@@ -320,429 +233,616 @@ __device__ void build_context(const Fp8Args& a, Fp8Smem& S, int e, int ctid) {
         const bool has = (t < a.M) && ((mask >> t) & 1ull);
         const uint32_t bal = __ballot_sync(0xFFFFFFFFu, has);
         if (has) {
-          const int pos = base + __popc(bal & ((1u << lane) - 1u));
           int r = 0;
           for (int k = 0; k < a.top_k; ++k)
             if (S.rid[t * a.top_k + k] == e) r = k;
-          S.ctx_route[pos] = static_cast<int16_t>(t * a.top_k + r);
-          S.ctx_tok[pos] = static_cast<int16_t>(t);
+          S.ctx_route[b][base + __popc(bal & ((1u << lane) - 1u))] = static_cast<int16_t>(t * a.top_k + r);
         }
         base += __popc(bal);
       }
-      if (lane == 0) S.ctx_n = base;
+      if (lane == 0) S.ctx_n[b] = base;
     }
   }
-  compute_bar();
+  epi_bar();
 }
 
-// ---------------------------------------------------------------- GEMM1 item
-template <int RTC>
-__device__ __forceinline__ void gemm1_chunk(const Fp8Args& a, Fp8Smem& S, const uint8_t* stage, int e, int j,
-                                            int h0, int c0, int rt, bool requant, int ctid, int warp, int lane,
-                                            uint32_t (&xa)[kMaxSlicesPerThread][kTokChunk][8],
-                                            float (&sx)[kMaxSlicesPerThread][kTokChunk]) {
-  const PhaseGeom& g = a.g1;
-  const int grp = ctid / g.tpr, gt = ctid % g.tpr;
-  if (requant) quant_x<RTC>(a, S, c0, rt, gt, xa, sx);
-  // Scale products of the two row blocks (first half: block j; second: I/128 + j).
-  const int nb = a.H / 128, nrb = 2 * a.I / 128;
-  float comb[kMaxSlicesPerThread][2][kTokChunk];
+// Quantise the activations of chunk `ch` into B buffer b: for each token row
+// t < r and K block j of the chunk, 128 values -> E4M3 by the pages' rule.
+// Phase 1 reads x (BF16): sx = max(amax, 1e-10) / 448 [UE8M0], q = e4m3(x * (1/sx)).
+// Phase 2 reads the SwiGLU output: sh likewise; routed q = e4m3(h / sh)
+// ("mega_moe" hidden_block), shared q = e4m3(h * (1/sh)) ("shared_expert" _DownKernel).
+// Row t of K block j sits at j*N*128 + t*128, its 16-byte chunk c at c ^ (t % 8)
+// (the 128-byte swizzle the MMA descriptor names).
+__device__ void fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& ch, int b, int etid) {
+  const int r = S.ctx_n[b];
+  const int N = P.N;
+  uint8_t* B = S.B[b];
+  const int items = ch.kc * r * 8;
+  const int K = ch.phase == 1 ? a.H : a.I;
+  for (int base = 0; base < items; base += 128) {
+    const int w = base + etid;
+    const bool valid = w < items;
+    const int p = w >> 3, sub = w & 7;
+    const int t = valid ? p % r : 0, j = valid ? p / r : 0;
+    float v[16];
+    float amax = 0.0f;
+    if (valid) {
+      const int route = S.ctx_route[b][t];
+      const int col = (ch.kb0 + j) * 128 + sub * 16;
+      if (ch.phase == 1) {
+        const int tok = a.mode == kModeShared ? route : route / a.top_k;
+        const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(tok) * K + col);
+        const uint4 q0 = __ldg(src), q1 = __ldg(src + 1);
+        const uint32_t wd[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
-  for (int i = 0; i < kMaxSlicesPerThread; ++i) {
-    const int s = gt + g.tpr * i;
-    const int b = min(s, g.ns - 1) / 8;
-    const float w0 = __ldg(a.s13 + (static_cast<size_t>(e) * nrb + j) * nb + b);
-    const float w1 = __ldg(a.s13 + (static_cast<size_t>(e) * nrb + a.I / 128 + j) * nb + b);
+        for (int k = 0; k < 8; ++k) {
+          v[2 * k] = __uint_as_float(wd[k] << 16);
+          v[2 * k + 1] = __uint_as_float(wd[k] & 0xFFFF0000u);
+        }
+      } else {
+        const float4* src = reinterpret_cast<const float4*>(a.hbuf + static_cast<size_t>(route) * K + col);
 #pragma unroll
-    for (int t = 0; t < RTC; ++t) {
-      comb[i][0][t] = __fmul_rn(w0, sx[i][t]);
-      comb[i][1][t] = __fmul_rn(w1, sx[i][t]);
-    }
-  }
-  float acc[kRowsPerGroup * RTC];
-#pragma unroll
-  for (int v = 0; v < kRowsPerGroup * RTC; ++v) acc[v] = 0.0f;
-  dot_rows<RTC>(stage, a.H, grp * kRowsPerGroup, a.gp, gt, g, xa, comb, acc);
-  reduce_to_smem<RTC>(S, acc, warp, lane);
-  compute_bar();
-  // Fixed-order sum over the group's warps -> S.ysum[row][t].
-  constexpr int V = kRowsPerGroup * RTC;
-  const int wpg = g.tpr / 32;
-  if (ctid < g.rg * V) {
-    const int fg = ctid / V, v = ctid % V;
-    float s = 0.0f;
-    for (int w = 0; w < wpg; ++w) s += S.red[fg * wpg + w][v];
-    S.ysum[fg * kRowsPerGroup + v / RTC][v % RTC] = s;
-  }
-  compute_bar();
-  // SwiGLU of hidden indices h0 .. h0 + gp for the chunk's tokens.
-  if (ctid < a.gp * RTC && ctid % RTC < rt) {
-    const int q = ctid / RTC, t = ctid % RTC;
-    const float first = S.ysum[q][t];
-    const float second = S.ysum[a.gp + q][t];
-    const int route = S.ctx_route[c0 + t];
-    const float L = a.limit;
-    float h;
-    if (a.mode == kModeRouted) {
-      // W31: up rows first, then gate rows ("mega_moe" module docstring).
-      const float gate = fminf(second, L);
-      const float up = fmaxf(fminf(first, L), -L);
-      h = __fmul_rn(__fdiv_rn(gate, __fadd_rn(1.0f, expf(-gate))), up);
-    } else {
-      // Shared gate_up: gate rows first, BF16 gate_up and BF16 h.
-      const __nv_bfloat16 gb = __float2bfloat16_rn(first);
-      const __nv_bfloat16 ub = __float2bfloat16_rn(second);
-      if (a.gate_up != nullptr) {
-        a.gate_up[static_cast<size_t>(route) * 2 * a.I + h0 + q] = gb;
-        a.gate_up[static_cast<size_t>(route) * 2 * a.I + a.I + h0 + q] = ub;
+        for (int k = 0; k < 4; ++k) {
+          const float4 f = __ldcg(src + k);
+          v[4 * k] = f.x;
+          v[4 * k + 1] = f.y;
+          v[4 * k + 2] = f.z;
+          v[4 * k + 3] = f.w;
+        }
       }
-      const float gate = fminf(__bfloat162float(gb), L);
-      const float up = fmaxf(fminf(__bfloat162float(ub), L), -L);
-      const float silu = __fdiv_rn(gate, __fadd_rn(1.0f, expf(-gate)));
-      h = __bfloat162float(__float2bfloat16_rn(__fmul_rn(silu, up)));
+#pragma unroll
+      for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(v[k]));
     }
-    a.hbuf[static_cast<size_t>(route) * a.I + h0 + q] = h;
-  }
-  compute_bar();
-}
-
-// ---------------------------------------------------------------- GEMM2 item
-template <int RTC>
-__device__ __forceinline__ void gemm2_chunk(const Fp8Args& a, Fp8Smem& S, const uint8_t* stage, int e, int m0,
-                                            int c0, int rt, bool requant, int ctid, int warp, int lane,
-                                            uint32_t (&xa)[kMaxSlicesPerThread][kTokChunk][8],
-                                            float (&sh)[kMaxSlicesPerThread][kTokChunk]) {
-  const PhaseGeom& g = a.g2;
-  const int grp = ctid / g.tpr, gt = ctid % g.tpr;
-  if (requant) quant_h<RTC>(a, S, c0, rt, gt, xa, sh);
-  const int nb = a.I / 128, nrb = a.H / 128;
-  float comb[kMaxSlicesPerThread][2][kTokChunk];
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+    if (valid) {
+      float scale = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+      if (a.ue8m0) scale = ue8m0_ceil(scale);
+      float q[16];
+      if (ch.phase == 2 && a.mode == kModeRouted) {
 #pragma unroll
-  for (int i = 0; i < kMaxSlicesPerThread; ++i) {
-    const int s = gt + g.tpr * i;
-    const int b = min(s, g.ns - 1) / 8;
-    const float w = __ldg(a.s2 + (static_cast<size_t>(e) * nrb + m0 / 128) * nb + b);
+        for (int k = 0; k < 16; ++k) q[k] = __fdiv_rn(v[k], scale);
+      } else {
+        const float inv = __fdiv_rn(1.0f, scale);
 #pragma unroll
-    for (int t = 0; t < RTC; ++t) {
-      comb[i][0][t] = a.mode == kModeRouted ? __fmul_rn(w, sh[i][t]) : __fmul_rn(sh[i][t], w);
-      comb[i][1][t] = comb[i][0][t];
+        for (int k = 0; k < 16; ++k) q[k] = __fmul_rn(v[k], inv);
+      }
+      uint32_t wq[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        wq[k] = f32x2_to_e4m3x2(q[4 * k], q[4 * k + 1]) | (f32x2_to_e4m3x2(q[4 * k + 2], q[4 * k + 3]) << 16);
+      uint8_t* dst = B + j * N * 128 + t * 128 + ((sub ^ (t & 7)) << 4);
+      *reinterpret_cast<uint4*>(dst) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+      if (sub == 0) S.xs[b][t][j] = scale;
     }
   }
-  float acc[kRowsPerGroup * RTC];
+  // Rows [r, dirty) of the chunk's K blocks may hold an earlier expert's tokens.
+  const int dirty = S.dirty[b];
+  if (dirty > r) {
+    const int zr = dirty - r;
+    for (int w = etid; w < ch.kc * zr * 8; w += 128) {
+      const int j = w / (zr * 8), rem = w % (zr * 8);
+      const int t = r + rem / 8, c16 = rem % 8;
+      *reinterpret_cast<uint4*>(B + j * N * 128 + t * 128 + c16 * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  fence_proxy_async_smem();
+  epi_bar();
+  if (etid == 0) {
+    S.dirty[b] = max(dirty, r);
+    mbar_arrive(&S.bfull[b]);
+  }
+}
+
+// ---------------------------------------------------------------- epilogue pieces
+// Finish one GEMM1 tile: y of a first-half row (threads 0..63) or a
+// second-half row (64..127) -> SwiGLU of hidden 64T + q -> hbuf, then release
+// the expert counter.
+__device__ void finish_gemm1(const TcArgs& a, TcSmem& S, const Chunk& ch, int b, const float (&y)[kMaxTokens],
+                             int row, int etid) {
+  const int r = S.ctx_n[b];
+  const bool second = row >= 64;
+  const int q = row & 63;
+  const float L = a.limit;
 #pragma unroll
-  for (int v = 0; v < kRowsPerGroup * RTC; ++v) acc[v] = 0.0f;
-  dot_rows<RTC>(stage, a.I, grp * kRowsPerGroup, 1 << 30, gt, g, xa, comb, acc);
-  reduce_to_smem<RTC>(S, acc, warp, lane);
-  compute_bar();
-  constexpr int V = kRowsPerGroup * RTC;
-  const int wpg = g.tpr / 32;
-  if (ctid < g.rg * V && (ctid % V) % RTC < rt) {
-    const int fg = ctid / V, v = ctid % V;
-    float s = 0.0f;
-    for (int w = 0; w < wpg; ++w) s += S.red[fg * wpg + w][v];
-    const int m = m0 + fg * kRowsPerGroup + v / RTC;
-    const int route = S.ctx_route[c0 + v % RTC];
-    a.out[static_cast<size_t>(route) * a.H + m] = __float2bfloat16_rn(s);
+  for (int g = 0; g < kTokGroups; ++g) {
+    if (g * 16 < r) {
+      if (second) {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) S.ysm[t][q] = y[g * 16 + t];
+      }
+      epi_bar();
+      if (!second) {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          if (g * 16 + t < r) {
+            const int route = S.ctx_route[b][g * 16 + t];
+            const float first = y[g * 16 + t], sec = S.ysm[t][q];
+            float h;
+            if (a.mode == kModeRouted) {
+              // W31: up rows first, then gate rows ("mega_moe" module docstring).
+              const float gate = fminf(sec, L);
+              const float up = fmaxf(fminf(first, L), -L);
+              h = __fmul_rn(__fdiv_rn(gate, __fadd_rn(1.0f, expf(-gate))), up);
+            } else {
+              // Shared gate_up: gate rows first; BF16 gate_up and BF16 h.
+              const __nv_bfloat16 gb = __float2bfloat16_rn(first);
+              const __nv_bfloat16 ub = __float2bfloat16_rn(sec);
+              if (a.gate_up != nullptr) {
+                a.gate_up[static_cast<size_t>(route) * 2 * a.I + 64 * ch.T + q] = gb;
+                a.gate_up[static_cast<size_t>(route) * 2 * a.I + a.I + 64 * ch.T + q] = ub;
+              }
+              const float gate = fminf(__bfloat162float(gb), L);
+              const float up = fmaxf(fminf(__bfloat162float(ub), L), -L);
+              const float silu = __fdiv_rn(gate, __fadd_rn(1.0f, expf(-gate)));
+              h = __bfloat162float(__float2bfloat16_rn(__fmul_rn(silu, up)));
+            }
+            a.hbuf[static_cast<size_t>(route) * a.I + 64 * ch.T + q] = h;
+          }
+        }
+      }
+      epi_bar();
+    }
   }
-  compute_bar();
-}
-
-// ---------------------------------------------------------------- kernel
-__device__ __forceinline__ void item_range(long long n, int c, int G, long long& lo, long long& hi) {
-  lo = n * c / G;
-  hi = n * (c + 1) / G;
-}
-
-struct ItemPlan {
-  long long lo1, hi1, lo2, hi2;
-  int per_u1, parts, per_u2;
-  __device__ int count() const { return static_cast<int>((hi1 - lo1) + (hi2 - lo2)); }
-};
-
-// Issue the bulk copies of the CTA's item number `it` into stage it % kStages.
-__device__ void issue_item(const Fp8Args& a, Fp8Smem& S, const ItemPlan& P, int it, uint64_t pol) {
-  const int s = it % kStages;
-  uint8_t* dst = S.ring[s];
-  if (it < P.hi1 - P.lo1) {
-    const long long i = P.lo1 + it;
-    const int u = static_cast<int>(i / P.per_u1), rem = static_cast<int>(i % P.per_u1);
-    const int e = S.ulist[u];
-    const int h0 = (rem / P.parts) * 128 + (rem % P.parts) * a.gp;
-    const uint32_t half_bytes = static_cast<uint32_t>(a.gp) * a.H;
-    mbar_arrive_expect_tx(&S.full[s], 2 * half_bytes);
-    const uint8_t* base = a.w13 + static_cast<size_t>(e) * 2 * a.I * a.H;
-    bulk_g2s(dst, base + static_cast<size_t>(h0) * a.H, half_bytes, &S.full[s], pol);
-    bulk_g2s(dst + half_bytes, base + static_cast<size_t>(a.I + h0) * a.H, half_bytes, &S.full[s], pol);
-  } else {
-    const long long i = P.lo2 + (it - (P.hi1 - P.lo1));
-    const int u = static_cast<int>(i / P.per_u2), rb = static_cast<int>(i % P.per_u2);
-    const int e = S.ulist[u];
-    const uint32_t bytes = static_cast<uint32_t>(a.r2) * a.I;
-    mbar_arrive_expect_tx(&S.full[s], bytes);
-    bulk_g2s(dst, a.w2 + (static_cast<size_t>(e) * a.H + static_cast<size_t>(rb) * a.r2) * a.I, bytes,
-             &S.full[s], pol);
+  if (etid == 0) {
+    __threadfence();
+    red_release_gpu_add(a.done + (a.mode == kModeShared ? 0 : S.ulist[ch.u]), 1u);
   }
 }
 
-// Wait (all threads) for item `it`'s stage; false (uniformly) on abort.
-__device__ __forceinline__ bool wait_stage(const Fp8Args& a, Fp8Smem& S, int it) {
-  const int s = it % kStages;
-  if (!mbar_wait(&S.full[s], (it / kStages) & 1, a.timeout_ns, &S.abort)) {
-    if (!S.abort) set_error(a, S, kErrRingWait);
+__device__ void finish_gemm2(const TcArgs& a, TcSmem& S, const Chunk& ch, int b, const float (&y)[kMaxTokens],
+                             int row) {
+  const int r = S.ctx_n[b];
+  const int m = 128 * ch.T + row;
+#pragma unroll
+  for (int t = 0; t < kMaxTokens; ++t)
+    if (t < r) a.out[static_cast<size_t>(S.ctx_route[b][t]) * a.H + m] = __float2bfloat16_rn(y[t]);
+}
+
+__device__ __forceinline__ float* part_slot(const TcArgs& a, int phase, int c, int slot) {
+  return a.part + ((static_cast<size_t>(phase - 1) * kFp8MaxCtas + c) * 2 + slot) * a.ptok * 128;
+}
+
+// End of a segment: finish the tile directly when this CTA owns all of it,
+// else publish the partial; the last contributor sums all partials in CTA
+// order and finishes the tile.
+__device__ void end_segment(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& ch, int b, float (&y)[kMaxTokens],
+                            int row, int etid) {
+  const PhasePlan& pp = P.p[ch.phase - 1];
+  const int cf = pp.cta_of(ch.t0), cl = pp.cta_of(ch.t0 + pp.nb - 1);
+  const int r = S.ctx_n[b];
+  if (cf != cl) {
+    float* mine = part_slot(a, ch.phase, P.c, pp.lo >= ch.t0 ? 0 : 1);
+#pragma unroll
+    for (int t = 0; t < kMaxTokens; ++t)
+      if (t < r) mine[t * 128 + row] = y[t];
+    __threadfence();
+    epi_bar();
+    if (etid == 0) {
+      const int e = a.mode == kModeShared ? 0 : S.ulist[ch.u];
+      uint32_t* cnt = ch.phase == 1 ? a.cnt1 + static_cast<size_t>(e) * pp.tiles + ch.T
+                                    : a.cnt2 + static_cast<size_t>(e) * pp.tiles + ch.T;
+      const uint32_t old = atomicAdd(cnt, 1u);
+      const bool last = old + 1u == static_cast<uint32_t>(cl - cf + 1);
+      if (last) atomicExch(cnt, 0u);
+      S.flag = last ? 1 : 0;
+    }
+    epi_bar();
+    if (!S.flag) return;
+    __threadfence();
+#pragma unroll
+    for (int t = 0; t < kMaxTokens; ++t) y[t] = 0.0f;
+    for (int cc = cf; cc <= cl; ++cc) {
+      const float* src = part_slot(a, ch.phase, cc, pp.lo_of(cc) >= ch.t0 ? 0 : 1);
+#pragma unroll
+      for (int t = 0; t < kMaxTokens; ++t)
+        if (t < r) y[t] += __ldcg(src + t * 128 + row);
+    }
   }
-  compute_bar();
+  if (ch.phase == 1)
+    finish_gemm1(a, S, ch, b, y, row, etid);
+  else
+    finish_gemm2(a, S, ch, b, y, row);
+}
+
+// Wait until every GEMM1 tile of expert u is finished, then count this CTA in;
+// the last CTA with GEMM2 work on it re-arms the counters for the next call.
+__device__ bool wait_hidden(const TcArgs& a, TcSmem& S, const Plan& P, int u, int etid) {
+  if (etid == 0) {
+    const int e = a.mode == kModeShared ? 0 : S.ulist[u];
+    const uint32_t target = static_cast<uint32_t>(P.p[0].tiles);
+    const uint64_t t0 = globaltimer_ns();
+    bool ok = true;
+    while (ld_acquire_gpu(a.done + e) < target) {
+      if (S.abort || globaltimer_ns() - t0 > a.timeout_ns) {
+        ok = false;
+        break;
+      }
+      __nanosleep(64);
+    }
+    if (!ok) {
+      if (!S.abort) tc_error(a, S, kErrCrossWait);
+    } else {
+      const PhasePlan& p2 = P.p[1];
+      const long long s0 = static_cast<long long>(u) * p2.tiles * p2.nb;
+      const long long s1 = s0 + static_cast<long long>(p2.tiles) * p2.nb - 1;
+      const uint32_t ctas = static_cast<uint32_t>(p2.cta_of(s1) - p2.cta_of(s0) + 1);
+      const uint32_t old = atomicAdd(a.passed + e, 1u);
+      if (old + 1u == ctas) {
+        atomicExch(a.done + e, 0u);
+        atomicExch(a.passed + e, 0u);
+      }
+    }
+  }
+  epi_bar();
   return !S.abort;
 }
 
-// After item `it` (ends on a CTA barrier): thread 0 refills its stage with
-// item it + kStages.
-__device__ __forceinline__ void refill(const Fp8Args& a, Fp8Smem& S, const ItemPlan& P, int it, uint64_t pol) {
-  if (threadIdx.x == 0 && it + kStages < P.count()) {
-    fence_proxy_async_smem();
-    issue_item(a, S, P, it + kStages, pol);
-  }
-}
-
-// Before exit: thread 0 waits until every copy it issued has landed.
-__device__ void drain(const Fp8Args& a, Fp8Smem& S, const ItemPlan& P, int consumed) {
-  if (threadIdx.x != 0) return;
-  const int issued = min(P.count(), consumed + kStages);
-  for (int k = consumed; k < issued; ++k)
-    if (!mbar_wait(&S.full[k % kStages], (k / kStages) & 1, a.timeout_ns, nullptr)) atomicOr(a.err, kErrDrain);
-}
-
-__global__ void __launch_bounds__(kThreads, 1) fp8_moe_kernel(const __grid_constant__ Fp8Args a) {
+// ---------------------------------------------------------------- kernel
+__global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_constant__ TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  Fp8Smem& S = *reinterpret_cast<Fp8Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  TcSmem& S = *reinterpret_cast<TcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&S.full[s], 1);
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&S.bfull[b], 1);
+      mbar_init(&S.accfull[b], 1);
+      mbar_init(&S.tmemfree[b], 4);
+      S.dirty[b] = 0;
+    }
+    mbar_init(&S.final_bar, 1);
     fence_mbar_init();
     S.abort = 0;
+    prefetch_tmap(&a.map13);
+    prefetch_tmap(&a.map2);
   }
-  for (int e = tid; e < a.E; e += kThreads) S.tokmask[e] = 0ull;
+  if (warp == 1) {
+    tmem_alloc(&S.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  for (int e = tid; e < a.E; e += kTcThreads) S.tokmask[e] = 0ull;
+  {  // B buffers start zero
+    uint4* z = reinterpret_cast<uint4*>(&S.B[0][0]);
+    for (int i = tid; i < 2 * kBBufBytes / 16; i += kTcThreads) z[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
   griddep_wait();
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
 
-  // ---- routing and the unique-expert list (scratch overlays the ring)
+  // ---- routing and the unique-expert list (scratch overlays the A ring)
   if (a.mode == kModeRouted) {
-    float* sc = reinterpret_cast<float*>(&S.ring[0][0]) + warp * 2 * kMaxExperts;
+    float* sc = reinterpret_cast<float*>(&S.A[0][0]) + warp * 2 * kMaxExperts;
     uint32_t* ky = reinterpret_cast<uint32_t*>(sc + kMaxExperts);
-    for (int t = warp; t < a.M; t += kThreads / 32) route_token(a, S, t, sc, ky, lane, blockIdx.x == 0);
+    for (int t = warp; t < a.M; t += kTcThreads / 32) route_token(a, S, t, sc, ky, lane, blockIdx.x == 0);
     __syncthreads();
     if (warp == 0) {
-      int U = 0;
+      int U = 0, rmax = 0;
       for (int b = 0; b < a.E; b += 32) {
         const int e = b + lane;
-        const bool has = (e < a.E) && (S.tokmask[e] != 0ull);
+        const unsigned long long m = e < a.E ? S.tokmask[e] : 0ull;
+        const bool has = m != 0ull;
         const uint32_t bal = __ballot_sync(0xFFFFFFFFu, has);
         if (has) S.ulist[U + __popc(bal & ((1u << lane) - 1u))] = static_cast<int16_t>(e);
         U += __popc(bal);
+        rmax = max(rmax, static_cast<int>(__reduce_max_sync(0xFFFFFFFFu, static_cast<uint32_t>(__popcll(m)))));
       }
-      if (lane == 0) S.U = U;
+      if (lane == 0) {
+        S.U = U;
+        S.rmax = rmax;
+      }
     }
   } else if (tid == 0) {
     S.U = 1;
     S.ulist[0] = 0;
+    S.rmax = a.M;
   }
   __syncthreads();
 
-  const int U = S.U;
-  const int G = gridDim.x, c = blockIdx.x;
-  ItemPlan P;
-  P.per_u1 = a.I / a.gp;  // GEMM1 items per expert (I/128 blocks x 128/gp parts)
-  P.parts = 128 / a.gp;
-  P.per_u2 = a.H / a.r2;  // GEMM2 items per expert
-  item_range(static_cast<long long>(U) * P.per_u1, c, G, P.lo1, P.hi1);
-  item_range(static_cast<long long>(U) * P.per_u2, c, G, P.lo2, P.hi2);
-  const int n_items = P.count();
-  if (n_items == 0) return;
+  Plan P;
+  P.U = S.U;
+  P.N = 16 * ((S.rmax + 15) / 16);
+  P.kcmax = min(kMaxKc, kTmemBuf / P.N);
+  P.c = blockIdx.x;
+  make_phase(P.p[0], static_cast<long long>(P.U) * (a.I / 64) * (a.H / 128), a.I / 64, a.H / 128, gridDim.x,
+             blockIdx.x);
+  make_phase(P.p[1], static_cast<long long>(P.U) * (a.H / 128) * (a.I / 128), a.H / 128, a.I / 128, gridDim.x,
+             blockIdx.x);
+  const uint32_t tmem = S.tmem_base;
 
-  uint64_t pol = 0;
-  if (tid == 0) {
-    pol = l2_evict_first_policy();
-    fence_proxy_async_smem();  // the routing scratch overlaid the ring
-    for (int it = 0; it < min(kStages, n_items); ++it) issue_item(a, S, P, it, pol);
-  }
-
-  const int ctid = tid;
-  uint32_t xa[kMaxSlicesPerThread][kTokChunk][8];
-  float xs[kMaxSlicesPerThread][kTokChunk];
-#pragma unroll
-  for (int i = 0; i < kMaxSlicesPerThread; ++i)
-#pragma unroll
-    for (int t = 0; t < kTokChunk; ++t) {
-      xs[i][t] = 0.0f;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) xa[i][t][k] = 0u;
-    }
-
-  int it = 0;
-  int cur_u = -1;
-  for (long long i = P.lo1; i < P.hi1; ++i, ++it) {
-    const int u = static_cast<int>(i / P.per_u1), rem = static_cast<int>(i % P.per_u1);
-    const int e = S.ulist[u];
-    const int j = rem / P.parts;
-    const int h0 = j * 128 + (rem % P.parts) * a.gp;
-    bool fresh = false;
-    if (u != cur_u) {
-      build_context(a, S, e, ctid);
-      cur_u = u;
-      fresh = true;
-    }
-    if (!wait_stage(a, S, it)) {
-      drain(a, S, P, it);
-      return;
-    }
-    const int nt = S.ctx_n;
-    const bool single = nt <= kTokChunk;
-    const uint8_t* stage = S.ring[it % kStages];
-    for (int c0 = 0; c0 < nt; c0 += kTokChunk) {
-      const int rt = min(kTokChunk, nt - c0);
-      const bool requant = fresh || !single;
-      // 8 rows x 1, 2 or 4 token slots per lane keep the warp reduction a power of two.
-      switch (rt) {
-        case 1: gemm1_chunk<1>(a, S, stage, e, j, h0, c0, rt, requant, ctid, warp, lane, xa, xs); break;
-        case 2: gemm1_chunk<2>(a, S, stage, e, j, h0, c0, rt, requant, ctid, warp, lane, xa, xs); break;
-        default: gemm1_chunk<4>(a, S, stage, e, j, h0, c0, rt, requant, ctid, warp, lane, xa, xs); break;
-      }
-    }
-    if (ctid == 0) {
-      __threadfence();
-      red_release_gpu_add(a.done + e, 1u);
-    }
-    refill(a, S, P, it, pol);
-  }
-
-  cur_u = -1;
-  for (long long i = P.lo2; i < P.hi2; ++i, ++it) {
-    const int u = static_cast<int>(i / P.per_u2), rb = static_cast<int>(i % P.per_u2);
-    const int e = S.ulist[u];
-    const int m0 = rb * a.r2;
-    bool fresh = false;
-    if (u != cur_u) {
-      build_context(a, S, e, ctid);
-      if (ctid == 0) {
-        const uint32_t target = static_cast<uint32_t>(P.per_u1);
-        const uint64_t t0 = globaltimer_ns();
-        while (ld_acquire_gpu(a.done + e) < target) {
-          if (globaltimer_ns() - t0 > a.timeout_ns) {
-            set_error(a, S, kErrCrossWait);
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      fence_proxy_async_smem();  // routing scratch overlaid the ring
+      Cursor cur{P.p[0].lo, 1};
+      Chunk ch;
+      int k = 0;
+      bool ok = true;
+      while (ok && cur.next(P, ch)) {
+        const int e = a.mode == kModeShared ? 0 : S.ulist[ch.u];
+        int ra, rb;
+        const void* map;
+        if (ch.phase == 1) {
+          ra = e * 2 * a.I + 64 * ch.T;
+          rb = ra + a.I;
+          map = &a.map13;
+        } else {
+          ra = e * a.H + 128 * ch.T;
+          rb = ra + 64;
+          map = &a.map2;
+        }
+        for (int j = 0; j < ch.kc; ++j, ++k) {
+          const int s = k % kTcStages;
+          if (k >= kTcStages && !mbar_wait(&S.empty[s], ((k / kTcStages) - 1) & 1, a.timeout_ns, &S.abort)) {
+            if (!S.abort) tc_error(a, S, kErrRingWait);
+            ok = false;
             break;
           }
-          __nanosleep(64);
+          mbar_arrive_expect_tx(&S.full[s], kAStageBytes);
+          const int xk = (ch.kb0 + j) * 128;
+          tma_load_2d(S.A[s], map, xk, ra, &S.full[s], pol);
+          tma_load_2d(S.A[s] + kAStageBytes / 2, map, xk, rb, &S.full[s], pol);
         }
       }
-      compute_bar();
-      if (S.abort) {
-        drain(a, S, P, it);
-        return;
+      // Every load issued must land before the CTA may exit.
+      for (int kk = max(0, k - kTcStages); kk < k; ++kk)
+        if (!mbar_wait(&S.full[kk % kTcStages], (kk / kTcStages) & 1, a.timeout_ns, nullptr))
+          atomicOr(a.err, kErrDrain);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = f8_idesc(128, P.N);
+      Cursor cur{P.p[0].lo, 1};
+      Chunk ch;
+      int k = 0, ci = 0;
+      bool ok = true;
+      while (ok && cur.next(P, ch)) {
+        const int b = ci & 1;
+        if (!mbar_wait(&S.bfull[b], (ci >> 1) & 1, a.timeout_ns, &S.abort) ||
+            (ci >= 2 && !mbar_wait(&S.tmemfree[b], ((ci >> 1) - 1) & 1, a.timeout_ns, &S.abort))) {
+          if (!S.abort) tc_error(a, S, kErrRingWait);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t bbase = smem_u32(S.B[b]);
+        for (int j = 0; j < ch.kc; ++j, ++k) {
+          const int s = k % kTcStages;
+          if (!mbar_wait(&S.full[s], (k / kTcStages) & 1, a.timeout_ns, &S.abort)) {
+            if (!S.abort) tc_error(a, S, kErrRingWait);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t abase = smem_u32(S.A[s]);
+          const uint32_t d = tmem + b * kTmemBuf + j * P.N;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_f8(d, sw128_desc(abase + 32 * kk), sw128_desc(bbase + j * P.N * 128 + 32 * kk), idesc,
+                      kk > 0 ? 1u : 0u);
+          tc_commit(&S.empty[s]);
+        }
+        if (!ok) break;
+        tc_commit(&S.accfull[b]);
+        ++ci;
       }
-      cur_u = u;
-      fresh = true;
+      // Every MMA issued must complete before TMEM is released.
+      tc_commit(&S.final_bar);
+      if (!mbar_wait(&S.final_bar, 0, a.timeout_ns, nullptr)) atomicOr(a.err, kErrDrain);
     }
-    if (!wait_stage(a, S, it)) {
-      drain(a, S, P, it);
-      return;
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int etid = tid - 64;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;  // TMEM lane = tile row
+    Cursor cur{P.p[0].lo, 1}, ahead{P.p[0].lo, 1};
+    Chunk ch, nx;
+    int ci = 0;
+    bool have_next = ahead.next(P, nx);
+    bool ok = true;
+    if (have_next) {  // B of the first chunk
+      fill_context(a, S, nx.u, 0, etid);
+      if (nx.phase == 2) ok = wait_hidden(a, S, P, nx.u, etid);
+      if (ok) fill_b(a, S, P, nx, 0, etid);
     }
-    const int nt = S.ctx_n;
-    const bool single = nt <= kTokChunk;
-    const uint8_t* stage = S.ring[it % kStages];
-    for (int c0 = 0; c0 < nt; c0 += kTokChunk) {
-      const int rt = min(kTokChunk, nt - c0);
-      const bool requant = fresh || !single;
-      // 8 rows x 1, 2 or 4 token slots per lane keep the warp reduction a power of two.
-      switch (rt) {
-        case 1: gemm2_chunk<1>(a, S, stage, e, m0, c0, rt, requant, ctid, warp, lane, xa, xs); break;
-        case 2: gemm2_chunk<2>(a, S, stage, e, m0, c0, rt, requant, ctid, warp, lane, xa, xs); break;
-        default: gemm2_chunk<4>(a, S, stage, e, m0, c0, rt, requant, ctid, warp, lane, xa, xs); break;
+    int ctx_u = have_next ? nx.u : -1, ctx_phase = have_next ? nx.phase : 0;
+    float y[kMaxTokens];
+#pragma unroll
+    for (int t = 0; t < kMaxTokens; ++t) y[t] = 0.0f;
+    while (ok && cur.next(P, ch)) {
+      const int b = ci & 1;
+      have_next = ahead.next(P, nx);  // the chunk after `ch`
+      // Prefill the next chunk's B now unless it needs the cross-CTA wait.
+      const bool next_new_ctx = have_next && (nx.u != ctx_u || nx.phase != ctx_phase);
+      const bool early = have_next && !(next_new_ctx && nx.phase == 2);
+      if (early) {
+        fill_context(a, S, nx.u, b ^ 1, etid);
+        fill_b(a, S, P, nx, b ^ 1, etid);
       }
-    }
-    if (ctid == 0) {
-      // The last GEMM2 item of this expert re-arms its counters for the next call.
-      const uint32_t old = atomicAdd(a.consumed + e, 1u);
-      if (old + 1u == static_cast<uint32_t>(P.per_u2)) {
-        atomicExch(a.done + e, 0u);
-        atomicExch(a.consumed + e, 0u);
+      // Block scales of this chunk's K blocks for this thread's row.
+      const int e = a.mode == kModeShared ? 0 : S.ulist[ch.u];
+      float ws[kMaxKc];
+      {
+        const float* sp;
+        if (ch.phase == 1) {
+          const int rb = (row < 64 ? 0 : a.I / 128) + ch.T / 2;
+          sp = a.s13 + (static_cast<size_t>(e) * (2 * a.I / 128) + rb) * P.p[0].nb;
+        } else {
+          sp = a.s2 + (static_cast<size_t>(e) * (a.H / 128) + ch.T) * P.p[1].nb;
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxKc; ++j) ws[j] = j < ch.kc ? __ldg(sp + ch.kb0 + j) : 0.0f;
       }
+      if (!mbar_wait(&S.accfull[b], (ci >> 1) & 1, a.timeout_ns, &S.abort)) {
+        if (!S.abort) tc_error(a, S, kErrRingWait);
+      }
+      epi_bar();
+      if (S.abort) break;
+      tc_fence_after();
+      const int r = S.ctx_n[b];
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16) + b * kTmemBuf;
+#pragma unroll
+      for (int j = 0; j < kMaxKc; ++j) {
+        if (j < ch.kc) {
+#pragma unroll
+          for (int g = 0; g < kTokGroups; ++g) {
+            if (g * 16 < r) {
+              uint32_t v[16];
+              tmem_ld<16>(tbase + j * P.N + g * 16, v);
+              tc_wait_ld();
+#pragma unroll
+              for (int t = 0; t < 16; ++t) {
+                if (g * 16 + t < r) {
+                  const float c = __fmul_rn(ws[j], S.xs[b][g * 16 + t][j]);
+                  y[g * 16 + t] = fmaf(__uint_as_float(v[t]), c, y[g * 16 + t]);
+                }
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.tmemfree[b]);
+      if (ch.last_of_seg) {
+        end_segment(a, S, P, ch, b, y, row, etid);
+#pragma unroll
+        for (int t = 0; t < kMaxTokens; ++t) y[t] = 0.0f;
+      }
+      if (have_next && !early) {
+        fill_context(a, S, nx.u, b ^ 1, etid);
+        if (nx.phase == 2 && next_new_ctx) ok = wait_hidden(a, S, P, nx.u, etid);
+        if (ok) fill_b(a, S, P, nx, b ^ 1, etid);
+      }
+      if (have_next) {
+        ctx_u = nx.u;
+        ctx_phase = nx.phase;
+      }
+      ++ci;
     }
-    refill(a, S, P, it, pol);
   }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ---------------------------------------------------------------- host side
-static PhaseGeom make_geom(int K) {
-  PhaseGeom g;
-  g.ns = K / 16;
-  int tpr = 32;
-  while (tpr < g.ns && tpr < kComputeThreads) tpr *= 2;
-  g.tpr = tpr;
-  g.rg = kComputeThreads / tpr;
-  g.nspt = (g.ns + tpr - 1) / tpr;
-  return g;
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
 }
 
-struct Fp8Workspace {
-  uint32_t* err;
-  uint32_t* done;
-  uint32_t* consumed;
-  float* hbuf;
+// 2-D byte tensor [rows, cols] (row-major), box 64 rows x 128 bytes, 128-byte swizzle.
+static bool make_map(CUtensorMap* map, const void* base, unsigned long long rows, unsigned long long cols) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {128, 64};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct TcWorkspace {
+  uint32_t *err, *done, *passed, *cnt1, *cnt2;
+  float *hbuf, *part;
+  int ptok;
+  size_t zero_bytes;  // error word and counters: must be zero when a call starts
   size_t bytes;
 };
 
 static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-static Fp8Workspace fp8_workspace_layout(void* base, int routes, int I, int E) {
-  Fp8Workspace w;
+static TcWorkspace tc_layout(void* base, int M, int routes, int H, int I, int E) {
+  TcWorkspace w;
   uint8_t* p = static_cast<uint8_t*>(base);
   size_t off = 0;
   w.err = reinterpret_cast<uint32_t*>(p + off);
   off += 256;
   w.done = reinterpret_cast<uint32_t*>(p + off);
-  off += align256(sizeof(uint32_t) * E);
-  w.consumed = reinterpret_cast<uint32_t*>(p + off);
-  off += align256(sizeof(uint32_t) * E);
+  off += align256(4 * static_cast<size_t>(E));
+  w.passed = reinterpret_cast<uint32_t*>(p + off);
+  off += align256(4 * static_cast<size_t>(E));
+  // Counters first, sized by the expert count only: the zeroed prefix is the
+  // same for every M, so one workspace serves calls with any M up to its size.
+  w.cnt1 = reinterpret_cast<uint32_t*>(p + off);
+  off += align256(4 * static_cast<size_t>(E) * (I / 64));
+  w.cnt2 = reinterpret_cast<uint32_t*>(p + off);
+  off += align256(4 * static_cast<size_t>(E) * (H / 128));
+  w.zero_bytes = off;
   w.hbuf = reinterpret_cast<float*>(p + off);
-  off += align256(sizeof(float) * static_cast<size_t>(routes) * I);
+  off += align256(4 * static_cast<size_t>(routes) * I);
+  w.ptok = M < kMaxTokens ? M : kMaxTokens;
+  w.part = reinterpret_cast<float*>(p + off);
+  off += align256(4 * static_cast<size_t>(2) * kFp8MaxCtas * 2 * w.ptok * 128);
   w.bytes = off;
   return w;
 }
 
-size_t fp8_workspace_bytes(int routes, int I, int E) {
-  return fp8_workspace_layout(nullptr, routes, I, E).bytes;
+size_t fp8_workspace_bytes(int M, int routes, int H, int I, int E) {
+  return tc_layout(nullptr, M, routes, H, I, E).bytes;
 }
 
-static int launch_fp8(Fp8Args& a, void* workspace, size_t workspace_bytes, int routes, cudaStream_t st) {
-  const Fp8Workspace w = fp8_workspace_layout(workspace, routes, a.I, a.mode == kModeShared ? 1 : a.E);
+size_t fp8_workspace_zero_bytes(int M, int routes, int H, int I, int E) {
+  return tc_layout(nullptr, M, routes, H, I, E).zero_bytes;
+}
+
+static int launch_tc(TcArgs& a, const uint8_t* w13, const uint8_t* w2, void* workspace, size_t workspace_bytes,
+                     int routes, cudaStream_t st) {
+  const int E = a.mode == kModeShared ? 1 : a.E;
+  const TcWorkspace w = tc_layout(workspace, a.M, routes, a.H, a.I, E);
   if (workspace == nullptr || workspace_bytes < w.bytes)
     return set_last_error(FME_EWORKSPACE, "workspace of %zu bytes needed, %zu given", w.bytes, workspace_bytes);
   a.err = w.err;
   a.done = w.done;
-  a.consumed = w.consumed;
+  a.passed = w.passed;
+  a.cnt1 = w.cnt1;
+  a.cnt2 = w.cnt2;
   a.hbuf = w.hbuf;
-  a.g1 = make_geom(a.H);
-  a.g2 = make_geom(a.I);
-  a.gp = kRowsPerGroup * a.g1.rg / 2;
-  a.r2 = kRowsPerGroup * a.g2.rg;
+  a.part = w.part;
+  a.ptok = w.ptok;
   a.timeout_ns = wait_timeout_ns();
+  if (!make_map(&a.map13, w13, static_cast<unsigned long long>(E) * 2 * a.I, a.H) ||
+      !make_map(&a.map2, w2, static_cast<unsigned long long>(E) * a.H, a.I))
+    return set_last_error(FME_ECUDA, "cuTensorMapEncodeTiled failed or unavailable");
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return set_last_error(FME_ECUDA, "cudaGetDevice failed");
   const int sms = device_sm_count(dev);
   if (sms <= 0) return set_last_error(FME_ECUDA, "cannot query the SM count");
-  if (!ensure_smem_attr(dev, reinterpret_cast<const void*>(fp8_moe_kernel), kFp8SmemBytes))
+  if (!ensure_smem_attr(dev, reinterpret_cast<const void*>(fp8_moe_tc_kernel), kTcSmemBytes))
     return set_last_error(FME_ECUDA, "cudaFuncSetAttribute(max dynamic smem) failed");
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(sms);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kFp8SmemBytes;
+  cfg.gridDim = dim3(sms < kFp8MaxCtas ? sms : kFp8MaxCtas);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = kTcSmemBytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t err = cudaLaunchKernelEx(&cfg, fp8_moe_kernel, a);
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, fp8_moe_tc_kernel, a);
   if (err != cudaSuccess) return set_last_error(FME_ECUDA, "fp8 kernel launch: %s", cudaGetErrorString(err));
   return FME_OK;
 }
@@ -751,18 +851,16 @@ int routed_fp8(const void* x, const void* logits, int logits_dtype, const float*
                const float* s13, const uint8_t* w2, const float* s2, int M, int H, int I, int E, int top_k,
                float limit, float scale, int ue8m0, void* out, int32_t* ids, float* weights, void* workspace,
                size_t workspace_bytes, cudaStream_t st) {
-  Fp8Args a = {};
+  TcArgs a;
+  memset(&a, 0, sizeof(a));
   a.x = static_cast<const __nv_bfloat16*>(x);
   a.logits = logits;
   a.bias = bias;
-  a.w13 = w13;
   a.s13 = s13;
-  a.w2 = w2;
   a.s2 = s2;
   a.out = static_cast<__nv_bfloat16*>(out);
   a.ids = ids;
   a.weights = weights;
-  a.gate_up = nullptr;
   a.M = M;
   a.H = H;
   a.I = I;
@@ -773,17 +871,16 @@ int routed_fp8(const void* x, const void* logits, int logits_dtype, const float*
   a.ue8m0 = ue8m0 ? 1 : 0;
   a.logits_f32 = logits_dtype == FME_F32 ? 1 : 0;
   a.mode = kModeRouted;
-  return launch_fp8(a, workspace, workspace_bytes, M * top_k, st);
+  return launch_tc(a, w13, w2, workspace, workspace_bytes, M * top_k, st);
 }
 
 int shared_fp8(const void* x, const uint8_t* w13, const float* s13, const uint8_t* w2, const float* s2, int M,
                int H, int I, float limit, int ue8m0, void* gate_up, void* out, void* workspace,
                size_t workspace_bytes, cudaStream_t st) {
-  Fp8Args a = {};
+  TcArgs a;
+  memset(&a, 0, sizeof(a));
   a.x = static_cast<const __nv_bfloat16*>(x);
-  a.w13 = w13;
   a.s13 = s13;
-  a.w2 = w2;
   a.s2 = s2;
   a.out = static_cast<__nv_bfloat16*>(out);
   a.gate_up = static_cast<__nv_bfloat16*>(gate_up);
@@ -796,7 +893,7 @@ int shared_fp8(const void* x, const uint8_t* w13, const float* s13, const uint8_
   a.scale = 1.0f;
   a.ue8m0 = ue8m0 ? 1 : 0;
   a.mode = kModeShared;
-  return launch_fp8(a, workspace, workspace_bytes, M, st);
+  return launch_tc(a, w13, w2, workspace, workspace_bytes, M, st);
 }
 
 }  // namespace fme

@@ -20,8 +20,9 @@
  *   *_workspace() function returns. It must be zero-filled before its first
  *   use (fme_workspace_clear). Every successful call leaves its counters at
  *   zero again, so one workspace serves any number of calls issued in stream
- *   order. Two calls that overlap on the GPU need two workspaces. After a
- *   device-side error, clear it again before reuse.
+ *   order, including calls with fewer tokens M than it was sized for (same
+ *   other sizes). Two calls that overlap on the GPU need two workspaces.
+ *   After a device-side error, clear it again before reuse.
  * - BF16 is IEEE bfloat16 (uint16 bit patterns). FP8 is E4M3 ("e4m3fn": no
  *   infinities, 0x7F/0xFF are NaN). FP4 is E2M1, sign in bit 3.
  */
@@ -103,14 +104,15 @@ size_t fme_moe_routed_fp8_workspace(int M, int H, int I, int E, int top_k);
  * cannot call cudaMalloc (code running inside another owner's memory pool, a
  * plug-in whose host forbids device allocations after start-up, paths that
  * run while a graph is being captured), so they cannot hand over a workspace.
- * This variant takes the same arguments minus the workspace and uses a
- * 1 MiB scratch array compiled into libfme.so instead; every GPU that loads
+ * This variant takes the same arguments minus the workspace and uses an
+ * 8 MiB scratch array compiled into libfme.so instead; every GPU that loads
  * the library holds that array until the process exits. It allocates
  * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
  *
- * - Size limit: the call must need at most 1 MiB of workspace
- *   (fme_moe_routed_fp8_workspace <= 1048576; e.g. I = 2048 with up to 64
- *   routes M * top_k). Larger requests return FME_EUNSUPPORTED.
+ * - Size limit: the call must need at most 8 MiB of workspace
+ *   (fme_moe_routed_fp8_workspace <= 8388608; e.g. the DeepSeek-V3 shape
+ *   H = 7168, I = 2048, top_k = 8 up to M = 16 tokens). Larger requests
+ *   return FME_EUNSUPPORTED.
  * - First call per device: it looks up the array's device address with that
  *   device current. Make that first call before any stream capture.
  * - Every call shares the one array and zeroes its counters first, so calls

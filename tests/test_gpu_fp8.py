@@ -105,6 +105,28 @@ def test_routed_workspace_stays_clean(fme):
     assert int(counters.abs().sum().item()) == 0
 
 
+def test_routed_one_workspace_serves_every_token_count(fme):
+    """A workspace sized for the largest M is reused by calls with fewer tokens."""
+    cfg = W.RAGGED
+    w13h, w2h = W.fp8_weights_host(cfg, 8)
+    s13, s2 = W.fp8_weight_scales(cfg, 8)
+    w13 = torch.from_numpy(w13h.full()).to(DEV)
+    w2 = torch.from_numpy(w2h.full()).to(DEV)
+    ws = fme.Workspace(fme.moe_routed_fp8_workspace(8, cfg.H, cfg.I, cfg.E, cfg.top_k), DEV)
+    for step, M in enumerate((8, 1, 5, 2, 8)):
+        x, logits, bias = W.fp8_activations(cfg, M, 8, step)
+        xd, ld, bd = _to_dev(cfg, x, logits, bias)
+        out, ids, wts = fme.moe_routed_fp8(xd, ld, bd, w13, torch.from_numpy(s13).to(DEV), w2,
+                                           torch.from_numpy(s2).to(DEV), cfg.top_k, cfg.limit, cfg.scale,
+                                           cfg.ue8m0, workspace=ws)
+        torch.cuda.synchronize()
+        assert ws.error() == 0, (step, M)
+        ref, rids, rw, keys = moe_fp8.routed_fp8(x, logits, bias, w13h, s13, w2h, s2, cfg.top_k, cfg.limit,
+                                                 cfg.scale, cfg.ue8m0)
+        assert_routing(ids.cpu().numpy(), wts.cpu().numpy(), rids, rw, routing.selection_gap(keys, rids))
+        assert_outputs(out.float().cpu().numpy(), ref)
+
+
 def _full_size(fme, cfg, M, seed, routes, rows):
     w13, s13, w2, s2 = W.fp8_weights_device(cfg, seed, DEV)
     s13h, s2h = s13.cpu().numpy(), s2.cpu().numpy()
