@@ -479,6 +479,41 @@ __device__ bool wait_hidden(const TcArgs& a, TcSmem& S, const Plan& P, int u, in
   return !S.abort;
 }
 
+// Scaled sum of one chunk's per-K-block partials: y[t] += D[j][t] *
+// (w_scale[j] * x_scale[t][j]) for this thread's row. Loads LD columns per
+// tcgen05.ld, GROUPS groups of them per K block, KB K blocks per wait.
+template <int LD, int GROUPS, int KB>
+__device__ __forceinline__ void accumulate(uint32_t tbase, int N, int kc, int r, const float (&ws)[kMaxKc],
+                                           const float (&xs)[kMaxTokens][kMaxKc], float (&y)[kMaxTokens]) {
+#pragma unroll
+  for (int j0 = 0; j0 < kMaxKc; j0 += KB) {
+    if (j0 < kc) {
+#pragma unroll
+      for (int g = 0; g < GROUPS; ++g) {
+        if (g * LD < r) {
+          uint32_t v[KB][LD];
+#pragma unroll
+          for (int jb = 0; jb < KB; ++jb)
+            if (j0 + jb < kc) tmem_ld<LD>(tbase + (j0 + jb) * N + g * LD, v[jb]);
+          tc_wait_ld();
+#pragma unroll
+          for (int jb = 0; jb < KB; ++jb) {
+            if (j0 + jb < kc) {
+#pragma unroll
+              for (int t = 0; t < LD; ++t) {
+                if (g * LD + t < r) {
+                  const float c = __fmul_rn(ws[j0 + jb], xs[g * LD + t][j0 + jb]);
+                  y[g * LD + t] = fmaf(__uint_as_float(v[jb][t]), c, y[g * LD + t]);
+                }
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- kernel
 __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_constant__ TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -689,25 +724,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
       const int r = S.ctx_n[b];
       const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16) + b * kTmemBuf;
 #pragma unroll
-      for (int j = 0; j < kMaxKc; ++j) {
-        if (j < ch.kc) {
-#pragma unroll
-          for (int g = 0; g < kTokGroups; ++g) {
-            if (g * 16 < r) {
-              uint32_t v[16];
-              tmem_ld<16>(tbase + j * P.N + g * 16, v);
-              tc_wait_ld();
-#pragma unroll
-              for (int t = 0; t < 16; ++t) {
-                if (g * 16 + t < r) {
-                  const float c = __fmul_rn(ws[j], S.xs[b][g * 16 + t][j]);
-                  y[g * 16 + t] = fmaf(__uint_as_float(v[t]), c, y[g * 16 + t]);
-                }
-              }
-            }
-          }
-        }
-      }
+      if (r == 1)
+        accumulate<1, 1, 16>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
+      else if (r <= 4)
+        accumulate<4, 1, 8>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
+      else if (r <= 16)
+        accumulate<16, 1, 2>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
+      else
+        accumulate<16, kTokGroups, 1>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.tmemfree[b]);
