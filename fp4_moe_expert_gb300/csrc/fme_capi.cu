@@ -38,9 +38,12 @@ bool ensure_smem_attr(int dev, const void* kernel, size_t bytes) {
   static std::set<std::pair<int, const void*>> done;
   std::lock_guard<std::mutex> lock(mu);
   if (done.count({dev, kernel})) return true;
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) !=
-      cudaSuccess)
+  const cudaError_t err =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (err != cudaSuccess) {
+    set_last_error(FME_ECUDA, "cudaFuncSetAttribute(max dynamic smem = %zu): %s", bytes, cudaGetErrorString(err));
     return false;
+  }
   done.insert({dev, kernel});
   return true;
 }

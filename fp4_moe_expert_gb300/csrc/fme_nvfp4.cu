@@ -624,8 +624,7 @@ int routed_nvfp4(const void* x, const int32_t* ids, const float* weights, const 
   if (cudaGetDevice(&dev) != cudaSuccess) return set_last_error(FME_ECUDA, "cudaGetDevice failed");
   const int sms = device_sm_count(dev);
   if (sms <= 0) return set_last_error(FME_ECUDA, "cannot query the SM count");
-  if (!ensure_smem_attr(dev, reinterpret_cast<const void*>(nvfp4_moe_kernel), kFp4SmemBytes))
-    return set_last_error(FME_ECUDA, "cudaFuncSetAttribute(max dynamic smem) failed");
+  if (!ensure_smem_attr(dev, reinterpret_cast<const void*>(nvfp4_moe_kernel), kFp4SmemBytes)) return FME_ECUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sms);
   cfg.blockDim = dim3(kThreads);

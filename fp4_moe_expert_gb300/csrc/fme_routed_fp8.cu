@@ -38,7 +38,8 @@ namespace fme {
 
 enum : int { kModeRouted = 0, kModeShared = 1 };
 
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 256;  // TMA, MMA, 4 accumulate, 2 fill warps
+constexpr int kFillThreads = 64;
 constexpr int kTcStages = 8;
 constexpr int kAStageBytes = 128 * 128;  // one 128-row x 128-byte K block of weights
 constexpr int kBBufBytes = 256 * 128;    // K blocks x N token rows x 128 bytes <= 256 rows
@@ -77,9 +78,10 @@ struct TcSmem {
   uint8_t A[kTcStages][kAStageBytes];
   uint8_t B[2][kBBufBytes];
   float xs[2][kMaxTokens][kMaxKc];  // activation block scales per B buffer
+  float wsc[2][2][kMaxKc];          // weight block scales per B buffer: [row half][K block]
   float ysm[16][64];                // SwiGLU exchange (16 tokens x 64 rows)
   uint64_t full[kTcStages], empty[kTcStages];
-  uint64_t bfull[2], accfull[2], tmemfree[2], final_bar;
+  uint64_t bfull[2], accfull[2], tmemfree[2], mfree[2], final_bar;
   unsigned long long tokmask[kMaxExperts];
   int16_t rid[kMaxTokens * kMaxTopK];
   int16_t ulist[kMaxExperts];
@@ -99,7 +101,9 @@ __device__ __forceinline__ void tc_error(const TcArgs& a, TcSmem& S, uint32_t bi
   S.abort = 1;
 }
 
+// The four accumulate warps and the two fill warps each sync among themselves.
 __device__ __forceinline__ void epi_bar() { named_bar_sync(1, 128); }
+__device__ __forceinline__ void fill_bar() { named_bar_sync(2, kFillThreads); }
 
 // ---------------------------------------------------------------- routing
 // One warp routes token t ("mega_moe" _MegaKernel.top_k_pick): sigmoid scores
@@ -217,10 +221,10 @@ struct Cursor {
 };
 
 // ---------------------------------------------------------------- B operand fill
-// Routes of expert u (token order) into ctx_route[b].
-__device__ void fill_context(const TcArgs& a, TcSmem& S, int u, int b, int etid) {
-  if (etid < 32) {
-    const int lane = etid;
+// Routes of expert u (token order) into ctx_route[b] (fill warps).
+__device__ void fill_context(const TcArgs& a, TcSmem& S, int u, int b, int fid) {
+  if (fid < 32) {
+    const int lane = fid;
     if (a.mode == kModeShared) {
       for (int t = lane; t < a.M; t += 32) S.ctx_route[b][t] = static_cast<int16_t>(t);
       if (lane == 0) S.ctx_n[b] = a.M;
@@ -243,7 +247,7 @@ __device__ void fill_context(const TcArgs& a, TcSmem& S, int u, int b, int etid)
       if (lane == 0) S.ctx_n[b] = base;
     }
   }
-  epi_bar();
+  fill_bar();
 }
 
 // Quantise the activations of chunk `ch` into B buffer b: for each token row
@@ -253,14 +257,14 @@ __device__ void fill_context(const TcArgs& a, TcSmem& S, int u, int b, int etid)
 // ("mega_moe" hidden_block), shared q = e4m3(h * (1/sh)) ("shared_expert" _DownKernel).
 // Row t of K block j sits at j*N*128 + t*128, its 16-byte chunk c at c ^ (t % 8)
 // (the 128-byte swizzle the MMA descriptor names).
-__device__ void fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& ch, int b, int etid) {
+__device__ void fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& ch, int b, int fid) {
   const int r = S.ctx_n[b];
   const int N = P.N;
   uint8_t* B = S.B[b];
   const int items = ch.kc * r * 8;
   const int K = ch.phase == 1 ? a.H : a.I;
-  for (int base = 0; base < items; base += 128) {
-    const int w = base + etid;
+  for (int base = 0; base < items; base += kFillThreads) {
+    const int w = base + fid;
     const bool valid = w < items;
     const int p = w >> 3, sub = w & 7;
     const int t = valid ? p % r : 0, j = valid ? p / r : 0;
@@ -321,15 +325,31 @@ __device__ void fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
   const int dirty = S.dirty[b];
   if (dirty > r) {
     const int zr = dirty - r;
-    for (int w = etid; w < ch.kc * zr * 8; w += 128) {
+    for (int w = fid; w < ch.kc * zr * 8; w += kFillThreads) {
       const int j = w / (zr * 8), rem = w % (zr * 8);
       const int t = r + rem / 8, c16 = rem % 8;
       *reinterpret_cast<uint4*>(B + j * N * 128 + t * 128 + c16 * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
   }
+  // Weight block scales of the chunk's K blocks: [first/second row half][j]
+  // for GEMM1 (row blocks T/2 and I/128 + T/2), [0][j] for GEMM2 (row block T).
+  if (fid < 2 * kMaxKc) {
+    const int half = fid / kMaxKc, j = fid % kMaxKc;
+    const int e = a.mode == kModeShared ? 0 : S.ulist[ch.u];
+    float w = 0.0f;
+    if (j < ch.kc) {
+      if (ch.phase == 1) {
+        const int rb = (half == 0 ? 0 : a.I / 128) + ch.T / 2;
+        w = __ldg(a.s13 + (static_cast<size_t>(e) * (2 * a.I / 128) + rb) * (a.H / 128) + ch.kb0 + j);
+      } else if (half == 0) {
+        w = __ldg(a.s2 + (static_cast<size_t>(e) * (a.H / 128) + ch.T) * (a.I / 128) + ch.kb0 + j);
+      }
+    }
+    S.wsc[b][half][j] = w;
+  }
   fence_proxy_async_smem();
-  epi_bar();
-  if (etid == 0) {
+  fill_bar();
+  if (fid == 0) {
     S.dirty[b] = max(dirty, r);
     mbar_arrive(&S.bfull[b]);
   }
@@ -448,8 +468,8 @@ __device__ void end_segment(const TcArgs& a, TcSmem& S, const Plan& P, const Chu
 
 // Wait until every GEMM1 tile of expert u is finished, then count this CTA in;
 // the last CTA with GEMM2 work on it re-arms the counters for the next call.
-__device__ bool wait_hidden(const TcArgs& a, TcSmem& S, const Plan& P, int u, int etid) {
-  if (etid == 0) {
+__device__ bool wait_hidden(const TcArgs& a, TcSmem& S, const Plan& P, int u, int fid) {
+  if (fid == 0) {
     const int e = a.mode == kModeShared ? 0 : S.ulist[u];
     const uint32_t target = static_cast<uint32_t>(P.p[0].tiles);
     const uint64_t t0 = globaltimer_ns();
@@ -475,7 +495,7 @@ __device__ bool wait_hidden(const TcArgs& a, TcSmem& S, const Plan& P, int u, in
       }
     }
   }
-  epi_bar();
+  fill_bar();
   return !S.abort;
 }
 
@@ -529,6 +549,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
       mbar_init(&S.bfull[b], 1);
       mbar_init(&S.accfull[b], 1);
       mbar_init(&S.tmemfree[b], 4);
+      mbar_init(&S.mfree[b], 4);
       S.dirty[b] = 0;
     }
     mbar_init(&S.final_bar, 1);
@@ -672,49 +693,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
       tc_commit(&S.final_bar);
       if (!mbar_wait(&S.final_bar, 0, a.timeout_ns, nullptr)) atomicOr(a.err, kErrDrain);
     }
-  } else {
-    // ------------------------------------------------------------ epilogue
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ accumulate
     const int etid = tid - 64;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;  // TMEM lane = tile row
-    Cursor cur{P.p[0].lo, 1}, ahead{P.p[0].lo, 1};
-    Chunk ch, nx;
+    const int half = row < 64 ? 0 : 1;
+    Cursor cur{P.p[0].lo, 1};
+    Chunk ch;
     int ci = 0;
-    bool have_next = ahead.next(P, nx);
-    bool ok = true;
-    if (have_next) {  // B of the first chunk
-      fill_context(a, S, nx.u, 0, etid);
-      if (nx.phase == 2) ok = wait_hidden(a, S, P, nx.u, etid);
-      if (ok) fill_b(a, S, P, nx, 0, etid);
-    }
-    int ctx_u = have_next ? nx.u : -1, ctx_phase = have_next ? nx.phase : 0;
     float y[kMaxTokens];
 #pragma unroll
     for (int t = 0; t < kMaxTokens; ++t) y[t] = 0.0f;
-    while (ok && cur.next(P, ch)) {
+    while (cur.next(P, ch)) {
       const int b = ci & 1;
-      have_next = ahead.next(P, nx);  // the chunk after `ch`
-      // Prefill the next chunk's B now unless it needs the cross-CTA wait.
-      const bool next_new_ctx = have_next && (nx.u != ctx_u || nx.phase != ctx_phase);
-      const bool early = have_next && !(next_new_ctx && nx.phase == 2);
-      if (early) {
-        fill_context(a, S, nx.u, b ^ 1, etid);
-        fill_b(a, S, P, nx, b ^ 1, etid);
-      }
-      // Block scales of this chunk's K blocks for this thread's row.
-      const int e = a.mode == kModeShared ? 0 : S.ulist[ch.u];
-      float ws[kMaxKc];
-      {
-        const float* sp;
-        if (ch.phase == 1) {
-          const int rb = (row < 64 ? 0 : a.I / 128) + ch.T / 2;
-          sp = a.s13 + (static_cast<size_t>(e) * (2 * a.I / 128) + rb) * P.p[0].nb;
-        } else {
-          sp = a.s2 + (static_cast<size_t>(e) * (a.H / 128) + ch.T) * P.p[1].nb;
-        }
-#pragma unroll
-        for (int j = 0; j < kMaxKc; ++j) ws[j] = j < ch.kc ? __ldg(sp + ch.kb0 + j) : 0.0f;
-      }
       if (!mbar_wait(&S.accfull[b], (ci >> 1) & 1, a.timeout_ns, &S.abort)) {
         if (!S.abort) tc_error(a, S, kErrRingWait);
       }
@@ -722,8 +714,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
       if (S.abort) break;
       tc_fence_after();
       const int r = S.ctx_n[b];
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16) + b * kTmemBuf;
+      float ws[kMaxKc];
 #pragma unroll
+      for (int j = 0; j < kMaxKc; ++j) ws[j] = S.wsc[b][ch.phase == 1 ? half : 0][j];
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16) + b * kTmemBuf;
       if (r == 1)
         accumulate<1, 1, 16>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
       else if (r <= 4)
@@ -740,15 +734,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
 #pragma unroll
         for (int t = 0; t < kMaxTokens; ++t) y[t] = 0.0f;
       }
-      if (have_next && !early) {
-        fill_context(a, S, nx.u, b ^ 1, etid);
-        if (nx.phase == 2 && next_new_ctx) ok = wait_hidden(a, S, P, nx.u, etid);
-        if (ok) fill_b(a, S, P, nx, b ^ 1, etid);
+      // Buffer b's B tile, scales and routes may now be refilled.
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.mfree[b]);
+      ++ci;
+    }
+  } else {
+    // ------------------------------------------------------------ fill
+    // Quantise each chunk's activations into the B operand and stage its
+    // scales, up to two chunks ahead of the accumulate warps.
+    const int fid = tid - 192;
+    Cursor cur{P.p[0].lo, 1};
+    Chunk ch;
+    int ci = 0, ctx_u = -1, ctx_phase = 0;
+    while (cur.next(P, ch)) {
+      const int b = ci & 1;
+      if (ci >= 2) {
+        if (!mbar_wait(&S.mfree[b], ((ci >> 1) - 1) & 1, a.timeout_ns, &S.abort)) {
+          if (!S.abort) tc_error(a, S, kErrRingWait);
+        }
+        fill_bar();
+        if (S.abort) break;
       }
-      if (have_next) {
-        ctx_u = nx.u;
-        ctx_phase = nx.phase;
+      fill_context(a, S, ch.u, b, fid);
+      if (ch.phase == 2 && (ch.u != ctx_u || ctx_phase != 2)) {
+        if (!wait_hidden(a, S, P, ch.u, fid)) break;
       }
+      ctx_u = ch.u;
+      ctx_phase = ch.phase;
+      fill_b(a, S, P, ch, b, fid);
       ++ci;
     }
   }
@@ -854,8 +868,7 @@ static int launch_tc(TcArgs& a, const uint8_t* w13, const uint8_t* w2, void* wor
   if (cudaGetDevice(&dev) != cudaSuccess) return set_last_error(FME_ECUDA, "cudaGetDevice failed");
   const int sms = device_sm_count(dev);
   if (sms <= 0) return set_last_error(FME_ECUDA, "cannot query the SM count");
-  if (!ensure_smem_attr(dev, reinterpret_cast<const void*>(fp8_moe_tc_kernel), kTcSmemBytes))
-    return set_last_error(FME_ECUDA, "cudaFuncSetAttribute(max dynamic smem) failed");
+  if (!ensure_smem_attr(dev, reinterpret_cast<const void*>(fp8_moe_tc_kernel), kTcSmemBytes)) return FME_ECUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sms < kFp8MaxCtas ? sms : kFp8MaxCtas);
   cfg.blockDim = dim3(kTcThreads);
