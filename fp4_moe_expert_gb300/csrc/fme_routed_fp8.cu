@@ -87,6 +87,8 @@ struct TcSmem {
   int16_t ulist[kMaxExperts];
   int16_t ctx_route[2][kMaxTokens];  // routes of each B buffer's expert, in token order
   int ctx_n[2];
+  int16_t seg_route[kMaxTokens];     // the accumulate warps' copy for the current segment
+  int seg_n;
   int dirty[2];  // B rows >= dirty[b] are zero in every K block of buffer b
   uint32_t tmem_base;
   int U, rmax;
@@ -109,42 +111,57 @@ __device__ __forceinline__ void fill_bar() { named_bar_sync(2, kFillThreads); }
 // One warp routes token t ("mega_moe" _MegaKernel.top_k_pick): sigmoid scores
 // (accurate expf, IEEE divide), keys score + bias as monotone uint32, top_k
 // rounds of warp max key then lowest expert among equals, weights
-// score / (float sum in pick order) * scale.
-__device__ void route_token(const TcArgs& a, TcSmem& S, int t, float* sc, uint32_t* ky, int lane, bool write_out) {
+// score / (float sum in pick order) * scale. Lane l holds experts l + 32 j in
+// registers; every load is issued before any sigmoid.
+template <int J>
+__device__ void route_token(const TcArgs& a, TcSmem& S, int t, int lane, bool write_out) {
   const int E = a.E;
-  for (int e = lane; e < E; e += 32) {
-    float l;
-    if (a.logits_f32)
-      l = __ldg(static_cast<const float*>(a.logits) + static_cast<size_t>(t) * E + e);
-    else
-      l = __bfloat162float(static_cast<const __nv_bfloat16*>(a.logits)[static_cast<size_t>(t) * E + e]);
-    const float s = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l)));
-    sc[e] = s;
-    ky[e] = ordered_key(__fadd_rn(s, __ldg(a.bias + e)));
+  float lg[J], bs[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int e = lane + 32 * j;
+    lg[j] = 0.0f;
+    bs[j] = 0.0f;
+    if (e < E) {
+      if (a.logits_f32)
+        lg[j] = __ldg(static_cast<const float*>(a.logits) + static_cast<size_t>(t) * E + e);
+      else
+        lg[j] = __bfloat162float(static_cast<const __nv_bfloat16*>(a.logits)[static_cast<size_t>(t) * E + e]);
+      bs[j] = __ldg(a.bias + e);
+    }
   }
-  __syncwarp();
+  uint32_t ky[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const float sgm = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-lg[j])));
+    lg[j] = sgm;  // score
+    ky[j] = (lane + 32 * j < E) ? ordered_key(__fadd_rn(sgm, bs[j])) : 0u;
+  }
   float total = 0.0f, mine = 0.0f;
   int mine_e = 0;
   for (int r = 0; r < a.top_k; ++r) {
     uint32_t best = 0u;
-    for (int e = lane; e < E; e += 32) best = max(best, ky[e]);
+#pragma unroll
+    for (int j = 0; j < J; ++j) best = max(best, ky[j]);
     const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, best);
     uint32_t cand = 0xFFFFFFFFu;
-    for (int e = lane; e < E; e += 32)
-      if (ky[e] == top) {
-        cand = static_cast<uint32_t>(e);
-        break;
-      }
+#pragma unroll
+    for (int j = J - 1; j >= 0; --j)
+      if (ky[j] == top) cand = static_cast<uint32_t>(lane + 32 * j);
     const int win = static_cast<int>(__reduce_min_sync(0xFFFFFFFFu, cand));
-    const float s = sc[win];
+    float sv = 0.0f;
+#pragma unroll
+    for (int j = 0; j < J; ++j)
+      if (lane + 32 * j == win) {
+        sv = lg[j];
+        ky[j] = 0u;
+      }
+    const float s = __shfl_sync(0xFFFFFFFFu, sv, win & 31);
     total = __fadd_rn(total, s);
     if (lane == r) {
       mine = s;
       mine_e = win;
     }
-    __syncwarp();
-    if (lane == 0) ky[win] = 0u;
-    __syncwarp();
   }
   if (lane < a.top_k) {
     const int route = t * a.top_k + lane;
@@ -261,64 +278,96 @@ __device__ void fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
   const int r = S.ctx_n[b];
   const int N = P.N;
   uint8_t* B = S.B[b];
+  // Weight block scales of the chunk's K blocks ([first/second row half][j]
+  // for GEMM1: row blocks T/2 and I/128 + T/2; [0][j] for GEMM2: row block T),
+  // loaded together with the first activations.
+  float wsv = 0.0f;
+  if (fid < 2 * kMaxKc) {
+    const int half = fid / kMaxKc, j = fid % kMaxKc;
+    const int e = a.mode == kModeShared ? 0 : S.ulist[ch.u];
+    if (j < ch.kc) {
+      if (ch.phase == 1) {
+        const int rb = (half == 0 ? 0 : a.I / 128) + ch.T / 2;
+        wsv = __ldg(a.s13 + (static_cast<size_t>(e) * (2 * a.I / 128) + rb) * (a.H / 128) + ch.kb0 + j);
+      } else if (half == 0) {
+        wsv = __ldg(a.s2 + (static_cast<size_t>(e) * (a.H / 128) + ch.T) * (a.I / 128) + ch.kb0 + j);
+      }
+    }
+  }
   const int items = ch.kc * r * 8;
   const int K = ch.phase == 1 ? a.H : a.I;
-  for (int base = 0; base < items; base += kFillThreads) {
-    const int w = base + fid;
-    const bool valid = w < items;
-    const int p = w >> 3, sub = w & 7;
-    const int t = valid ? p % r : 0, j = valid ? p / r : 0;
-    float v[16];
-    float amax = 0.0f;
-    if (valid) {
-      const int route = S.ctx_route[b][t];
-      const int col = (ch.kb0 + j) * 128 + sub * 16;
-      if (ch.phase == 1) {
-        const int tok = a.mode == kModeShared ? route : route / a.top_k;
-        const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(tok) * K + col);
-        const uint4 q0 = __ldg(src), q1 = __ldg(src + 1);
-        const uint32_t wd[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+  constexpr int IPT = 4;  // items per thread per round: all loads first, then quantise
+  for (int base = 0; base < items; base += kFillThreads * IPT) {
+    float v[IPT][16];
+    int tt[IPT], jj[IPT];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          v[2 * k] = __uint_as_float(wd[k] << 16);
-          v[2 * k + 1] = __uint_as_float(wd[k] & 0xFFFF0000u);
+    for (int q = 0; q < IPT; ++q) {
+      const int w = base + q * kFillThreads + fid;
+      const int p = w >> 3, sub = w & 7;
+      tt[q] = -1;
+      jj[q] = 0;
+      if (w < items) {
+        tt[q] = p % r;
+        jj[q] = p / r;
+        const int route = S.ctx_route[b][tt[q]];
+        const int col = (ch.kb0 + jj[q]) * 128 + sub * 16;
+        if (ch.phase == 1) {
+          const int tok = a.mode == kModeShared ? route : route / a.top_k;
+          const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(tok) * K + col);
+          const uint4 q0 = __ldg(src), q1 = __ldg(src + 1);
+          const uint32_t wd[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            v[q][2 * k] = __uint_as_float(wd[k] << 16);
+            v[q][2 * k + 1] = __uint_as_float(wd[k] & 0xFFFF0000u);
+          }
+        } else {
+          const float4* src = reinterpret_cast<const float4*>(a.hbuf + static_cast<size_t>(route) * K + col);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float4 f = __ldcg(src + k);
+            v[q][4 * k] = f.x;
+            v[q][4 * k + 1] = f.y;
+            v[q][4 * k + 2] = f.z;
+            v[q][4 * k + 3] = f.w;
+          }
         }
       } else {
-        const float4* src = reinterpret_cast<const float4*>(a.hbuf + static_cast<size_t>(route) * K + col);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float4 f = __ldcg(src + k);
-          v[4 * k] = f.x;
-          v[4 * k + 1] = f.y;
-          v[4 * k + 2] = f.z;
-          v[4 * k + 3] = f.w;
-        }
+        for (int k = 0; k < 16; ++k) v[q][k] = 0.0f;
       }
-#pragma unroll
-      for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(v[k]));
     }
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
-    if (valid) {
-      float scale = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
-      if (a.ue8m0) scale = ue8m0_ceil(scale);
-      float q[16];
-      if (ch.phase == 2 && a.mode == kModeRouted) {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) q[k] = __fdiv_rn(v[k], scale);
-      } else {
-        const float inv = __fdiv_rn(1.0f, scale);
+    for (int q = 0; q < IPT; ++q) {
+      if (base + q * kFillThreads >= items) break;  // uniform over the fill warps
+      const int sub = (base + q * kFillThreads + fid) & 7;
+      float amax = 0.0f;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) q[k] = __fmul_rn(v[k], inv);
+      for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(v[q][k]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+      if (tt[q] >= 0) {
+        const int t = tt[q], j = jj[q];
+        float scale = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+        if (a.ue8m0) scale = ue8m0_ceil(scale);
+        float qv[16];
+        if (ch.phase == 2 && a.mode == kModeRouted) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) qv[k] = __fdiv_rn(v[q][k], scale);
+        } else {
+          const float inv = __fdiv_rn(1.0f, scale);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) qv[k] = __fmul_rn(v[q][k], inv);
+        }
+        uint32_t wq[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          wq[k] = f32x2_to_e4m3x2(qv[4 * k], qv[4 * k + 1]) | (f32x2_to_e4m3x2(qv[4 * k + 2], qv[4 * k + 3]) << 16);
+        uint8_t* dst = B + j * N * 128 + t * 128 + ((sub ^ (t & 7)) << 4);
+        *reinterpret_cast<uint4*>(dst) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+        if (sub == 0) S.xs[b][t][j] = scale;
       }
-      uint32_t wq[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        wq[k] = f32x2_to_e4m3x2(q[4 * k], q[4 * k + 1]) | (f32x2_to_e4m3x2(q[4 * k + 2], q[4 * k + 3]) << 16);
-      uint8_t* dst = B + j * N * 128 + t * 128 + ((sub ^ (t & 7)) << 4);
-      *reinterpret_cast<uint4*>(dst) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
-      if (sub == 0) S.xs[b][t][j] = scale;
     }
   }
   // Rows [r, dirty) of the chunk's K blocks may hold an earlier expert's tokens.
@@ -331,22 +380,7 @@ __device__ void fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
       *reinterpret_cast<uint4*>(B + j * N * 128 + t * 128 + c16 * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
   }
-  // Weight block scales of the chunk's K blocks: [first/second row half][j]
-  // for GEMM1 (row blocks T/2 and I/128 + T/2), [0][j] for GEMM2 (row block T).
-  if (fid < 2 * kMaxKc) {
-    const int half = fid / kMaxKc, j = fid % kMaxKc;
-    const int e = a.mode == kModeShared ? 0 : S.ulist[ch.u];
-    float w = 0.0f;
-    if (j < ch.kc) {
-      if (ch.phase == 1) {
-        const int rb = (half == 0 ? 0 : a.I / 128) + ch.T / 2;
-        w = __ldg(a.s13 + (static_cast<size_t>(e) * (2 * a.I / 128) + rb) * (a.H / 128) + ch.kb0 + j);
-      } else if (half == 0) {
-        w = __ldg(a.s2 + (static_cast<size_t>(e) * (a.H / 128) + ch.T) * (a.I / 128) + ch.kb0 + j);
-      }
-    }
-    S.wsc[b][half][j] = w;
-  }
+  if (fid < 2 * kMaxKc) S.wsc[b][fid / kMaxKc][fid % kMaxKc] = wsv;
   fence_proxy_async_smem();
   fill_bar();
   if (fid == 0) {
@@ -361,7 +395,7 @@ __device__ void fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
 // the expert counter.
 __device__ void finish_gemm1(const TcArgs& a, TcSmem& S, const Chunk& ch, int b, const float (&y)[kMaxTokens],
                              int row, int etid) {
-  const int r = S.ctx_n[b];
+  const int r = S.seg_n;
   const bool second = row >= 64;
   const int q = row & 63;
   const float L = a.limit;
@@ -377,7 +411,7 @@ __device__ void finish_gemm1(const TcArgs& a, TcSmem& S, const Chunk& ch, int b,
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
           if (g * 16 + t < r) {
-            const int route = S.ctx_route[b][g * 16 + t];
+            const int route = S.seg_route[g * 16 + t];
             const float first = y[g * 16 + t], sec = S.ysm[t][q];
             float h;
             if (a.mode == kModeRouted) {
@@ -413,11 +447,11 @@ __device__ void finish_gemm1(const TcArgs& a, TcSmem& S, const Chunk& ch, int b,
 
 __device__ void finish_gemm2(const TcArgs& a, TcSmem& S, const Chunk& ch, int b, const float (&y)[kMaxTokens],
                              int row) {
-  const int r = S.ctx_n[b];
+  const int r = S.seg_n;
   const int m = 128 * ch.T + row;
 #pragma unroll
   for (int t = 0; t < kMaxTokens; ++t)
-    if (t < r) a.out[static_cast<size_t>(S.ctx_route[b][t]) * a.H + m] = __float2bfloat16_rn(y[t]);
+    if (t < r) a.out[static_cast<size_t>(S.seg_route[t]) * a.H + m] = __float2bfloat16_rn(y[t]);
 }
 
 __device__ __forceinline__ float* part_slot(const TcArgs& a, int phase, int c, int slot) {
@@ -431,7 +465,7 @@ __device__ void end_segment(const TcArgs& a, TcSmem& S, const Plan& P, const Chu
                             int row, int etid) {
   const PhasePlan& pp = P.p[ch.phase - 1];
   const int cf = pp.cta_of(ch.t0), cl = pp.cta_of(ch.t0 + pp.nb - 1);
-  const int r = S.ctx_n[b];
+  const int r = S.seg_n;
   if (cf != cl) {
     float* mine = part_slot(a, ch.phase, P.c, pp.lo >= ch.t0 ? 0 : 1);
 #pragma unroll
@@ -572,11 +606,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
 
-  // ---- routing and the unique-expert list (scratch overlays the A ring)
+  // ---- routing and the unique-expert list
   if (a.mode == kModeRouted) {
-    float* sc = reinterpret_cast<float*>(&S.A[0][0]) + warp * 2 * kMaxExperts;
-    uint32_t* ky = reinterpret_cast<uint32_t*>(sc + kMaxExperts);
-    for (int t = warp; t < a.M; t += kTcThreads / 32) route_token(a, S, t, sc, ky, lane, blockIdx.x == 0);
+    for (int t = warp; t < a.M; t += kTcThreads / 32) {
+      // Lane l holds experts l + 32 j, j < J: loops sized to the expert count.
+      if (a.E <= 64)
+        route_token<2>(a, S, t, lane, blockIdx.x == 0);
+      else if (a.E <= 256)
+        route_token<8>(a, S, t, lane, blockIdx.x == 0);
+      else if (a.E <= 512)
+        route_token<16>(a, S, t, lane, blockIdx.x == 0);
+      else
+        route_token<kMaxExperts / 32>(a, S, t, lane, blockIdx.x == 0);
+    }
     __syncthreads();
     if (warp == 0) {
       int U = 0, rmax = 0;
@@ -616,7 +658,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
-      fence_proxy_async_smem();  // routing scratch overlaid the ring
       Cursor cur{P.p[0].lo, 1};
       Chunk ch;
       int k = 0;
@@ -702,6 +743,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
     Cursor cur{P.p[0].lo, 1};
     Chunk ch;
     int ci = 0;
+    bool seg_first = true;
     float y[kMaxTokens];
 #pragma unroll
     for (int t = 0; t < kMaxTokens; ++t) y[t] = 0.0f;
@@ -727,16 +769,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
       else
         accumulate<16, kTokGroups, 1>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
       tc_fence_before();
+      if (seg_first) {
+        // First chunk of a segment: keep its routes for the segment's end.
+        for (int t = etid; t < r; t += 128) S.seg_route[t] = S.ctx_route[b][t];
+        if (etid == 0) S.seg_n = r;
+      }
+      epi_bar();
+      // TMEM buffer b and B buffer b (tile, scales, routes) may now be reused.
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.tmemfree[b]);
+      if (lane == 0) {
+        mbar_arrive(&S.tmemfree[b]);
+        mbar_arrive(&S.mfree[b]);
+      }
+      seg_first = ch.last_of_seg;
       if (ch.last_of_seg) {
         end_segment(a, S, P, ch, b, y, row, etid);
 #pragma unroll
         for (int t = 0; t < kMaxTokens; ++t) y[t] = 0.0f;
       }
-      // Buffer b's B tile, scales and routes may now be refilled.
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.mfree[b]);
       ++ci;
     }
   } else {
