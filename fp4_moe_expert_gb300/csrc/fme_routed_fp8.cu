@@ -175,14 +175,19 @@ __device__ void route_token(const TcArgs& a, TcSmem& S, int t, int lane, bool wr
 }
 
 // ---------------------------------------------------------------- work plan
-// Each phase's slots are split over Ge = min(G, n) CTAs: CTA c < Ge owns
-// [n*c/Ge, n*(c+1)/Ge), never empty; CTAs c >= Ge own nothing.
+// Each phase's slots (at most 1024 experts x 128 tiles x 64 K blocks, so
+// 32-bit arithmetic suffices) are split over Ge = min(G, n) CTAs: CTA c < Ge
+// owns [n*c/Ge, n*(c+1)/Ge), never empty; CTAs c >= Ge own nothing.
 struct PhasePlan {
-  long long n, lo, hi;
+  int n, lo, hi;
   int Ge, tiles, nb;
-  __device__ long long lo_of(int c) const { return c >= Ge ? n : n * c / Ge; }
+  __device__ int lo_of(int c) const {
+    return c >= Ge ? n : static_cast<int>(static_cast<long long>(n) * c / Ge);
+  }
   // The CTA whose slice holds slot x.
-  __device__ int cta_of(long long x) const { return static_cast<int>(((x + 1) * Ge + n - 1) / n) - 1; }
+  __device__ int cta_of(int x) const {
+    return static_cast<int>((static_cast<long long>(x + 1) * Ge + n - 1) / n) - 1;
+  }
 };
 
 struct Plan {
@@ -190,11 +195,11 @@ struct Plan {
   PhasePlan p[2];
 };
 
-__device__ void make_phase(PhasePlan& pp, long long n, int tiles, int nb, int G, int c) {
+__device__ void make_phase(PhasePlan& pp, int n, int tiles, int nb, int G, int c) {
   pp.n = n;
   pp.tiles = tiles;
   pp.nb = nb;
-  pp.Ge = static_cast<int>(min(static_cast<long long>(G), n));
+  pp.Ge = min(G, n);
   pp.lo = pp.lo_of(c);
   pp.hi = pp.lo_of(c + 1 > pp.Ge ? pp.Ge : c + 1);
   if (c >= pp.Ge) pp.lo = pp.hi = n;
@@ -202,30 +207,30 @@ __device__ void make_phase(PhasePlan& pp, long long n, int tiles, int nb, int G,
 
 struct Chunk {
   int phase, u, T, kb0, kc;
-  long long tile, t0;  // global tile index and its first slot
+  int tile, t0;  // global tile index and its first slot
   bool last_of_seg;
 };
 
 // Walks this CTA's slots of both phases in chunks of at most kcmax K blocks
 // that never cross a tile.
 struct Cursor {
-  long long pos;
+  int pos;
   int phase;
   __device__ bool next(const Plan& P, Chunk& ch) {
     while (true) {
       const PhasePlan& pp = P.p[phase - 1];
       if (pos < pp.lo) pos = pp.lo;
       if (pos < pp.hi) {
-        const long long tile = pos / pp.nb;
-        const long long t0 = tile * pp.nb;
-        const long long seg1 = min(pp.hi, t0 + pp.nb);
+        const int tile = pos / pp.nb;
+        const int t0 = tile * pp.nb;
+        const int seg1 = min(pp.hi, t0 + pp.nb);
         ch.phase = phase;
-        ch.u = static_cast<int>(tile / pp.tiles);
-        ch.T = static_cast<int>(tile % pp.tiles);
+        ch.u = tile / pp.tiles;
+        ch.T = tile - ch.u * pp.tiles;
         ch.tile = tile;
         ch.t0 = t0;
-        ch.kb0 = static_cast<int>(pos - t0);
-        ch.kc = static_cast<int>(min(static_cast<long long>(P.kcmax), seg1 - pos));
+        ch.kb0 = pos - t0;
+        ch.kc = min(P.kcmax, seg1 - pos);
         ch.last_of_seg = pos + ch.kc == seg1;
         pos += ch.kc;
         return true;
@@ -519,8 +524,8 @@ __device__ bool wait_hidden(const TcArgs& a, TcSmem& S, const Plan& P, int u, in
       if (!S.abort) tc_error(a, S, kErrCrossWait);
     } else {
       const PhasePlan& p2 = P.p[1];
-      const long long s0 = static_cast<long long>(u) * p2.tiles * p2.nb;
-      const long long s1 = s0 + static_cast<long long>(p2.tiles) * p2.nb - 1;
+      const int s0 = u * p2.tiles * p2.nb;
+      const int s1 = s0 + p2.tiles * p2.nb - 1;
       const uint32_t ctas = static_cast<uint32_t>(p2.cta_of(s1) - p2.cta_of(s0) + 1);
       const uint32_t old = atomicAdd(a.passed + e, 1u);
       if (old + 1u == ctas) {
@@ -648,39 +653,50 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
   P.N = 16 * ((S.rmax + 15) / 16);
   P.kcmax = min(kMaxKc, kTmemBuf / P.N);
   P.c = blockIdx.x;
-  make_phase(P.p[0], static_cast<long long>(P.U) * (a.I / 64) * (a.H / 128), a.I / 64, a.H / 128, gridDim.x,
-             blockIdx.x);
-  make_phase(P.p[1], static_cast<long long>(P.U) * (a.H / 128) * (a.I / 128), a.H / 128, a.I / 128, gridDim.x,
-             blockIdx.x);
+  make_phase(P.p[0], P.U * (a.I / 64) * (a.H / 128), a.I / 64, a.H / 128, gridDim.x, blockIdx.x);
+  make_phase(P.p[1], P.U * (a.H / 128) * (a.I / 128), a.H / 128, a.I / 128, gridDim.x, blockIdx.x);
   const uint32_t tmem = S.tmem_base;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
+      // Rows (two 64-row boxes) and tensor map of K block j of a chunk.
+      auto coords = [&](const Chunk& c, int& ra, int& rb, const void*& map) {
+        const int e = a.mode == kModeShared ? 0 : S.ulist[c.u];
+        if (c.phase == 1) {
+          ra = e * 2 * a.I + 64 * c.T;
+          rb = ra + a.I;
+          map = &a.map13;
+        } else {
+          ra = e * a.H + 128 * c.T;
+          rb = ra + 64;
+          map = &a.map2;
+        }
+      };
       Cursor cur{P.p[0].lo, 1};
       Chunk ch;
       int k = 0;
       bool ok = true;
       while (ok && cur.next(P, ch)) {
-        const int e = a.mode == kModeShared ? 0 : S.ulist[ch.u];
         int ra, rb;
         const void* map;
-        if (ch.phase == 1) {
-          ra = e * 2 * a.I + 64 * ch.T;
-          rb = ra + a.I;
-          map = &a.map13;
-        } else {
-          ra = e * a.H + 128 * ch.T;
-          rb = ra + 64;
-          map = &a.map2;
-        }
+        coords(ch, ra, rb, map);
         for (int j = 0; j < ch.kc; ++j, ++k) {
           const int s = k % kTcStages;
-          if (k >= kTcStages && !mbar_wait(&S.empty[s], ((k / kTcStages) - 1) & 1, a.timeout_ns, &S.abort)) {
-            if (!S.abort) tc_error(a, S, kErrRingWait);
-            ok = false;
-            break;
+          if (k >= kTcStages) {
+            const uint32_t parity = ((k / kTcStages) - 1) & 1;
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(&S.empty[s], parity)) {
+              if (S.abort || globaltimer_ns() - t0 > a.timeout_ns) {
+                ok = false;
+                break;
+              }
+            }
+            if (!ok) {
+              if (!S.abort) tc_error(a, S, kErrRingWait);
+              break;
+            }
           }
           mbar_arrive_expect_tx(&S.full[s], kAStageBytes);
           const int xk = (ch.kb0 + j) * 128;
