@@ -307,12 +307,19 @@ def gpu_arm(args, rank, world, local_rank):
 
 
 def load_traffic():
-    """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary (profiles/fp8_moe_kernel_dsv3.md), if it matches this kernel."""
+    """Mean DRAM bytes (read + write) per launch of the dominant kernel from the
+    committed ncu launch list (profiles/traffic.json); None when the kernel
+    source has changed since those counters were taken."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "fp4_moe_expert_gb300", "csrc", "fme_routed_fp8.cu")
     try:
         with open(path) as f:
-            return json.load(f).get("fp8_moe_kernel_dsv3_bytes_per_launch")
+            d = json.load(f)
+        with open(src, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != d.get("kernel_source_sha256"):
+                return None
+        return d.get("fp8_moe_kernel_dsv3_bytes_per_launch")
     except Exception:
         return None
 
