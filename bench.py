@@ -119,6 +119,22 @@ def reference_arm(args, rank):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------- replicas
+def aggregate(total_bytes, elapsed_ms, dist=None, device="cpu"):
+    """Whole-job weight-stream GB/s of N independent replicas: the bytes every
+    rank streamed, summed, over the slowest rank's time (the only collective
+    is this end-of-run reduction of two scalars)."""
+    import torch
+
+    if dist is not None and dist.is_initialized() and dist.get_world_size() > 1:
+        t = torch.tensor([float(elapsed_ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        b = torch.tensor([float(total_bytes)], dtype=torch.float64, device=device)
+        dist.all_reduce(b)
+        elapsed_ms, total_bytes = float(t.item()), float(b.item())
+    return total_bytes, elapsed_ms, total_bytes / (elapsed_ms * 1e-3) / 1e9
+
+
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -248,14 +264,7 @@ def gpu_arm(args, rank, world, local_rank):
     uniq = np.array([len(set(r[r >= 0].tolist())) for r in ids_np])
     bytes_call = uniq * EXPERT_BYTES
     total_bytes = float(bytes_call.sum())
-    if dist:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-        b = torch.tensor([total_bytes], device=dev, dtype=torch.float64)
-        dist.all_reduce(b)
-        total_bytes = float(b.item())
-    value = total_bytes / (elapsed_ms * 1e-3) / 1e9
+    total_bytes, elapsed_ms, value = aggregate(total_bytes, elapsed_ms, dist, dev)
     per_m = {}
     for i, M in enumerate(MS):
         sel = slice(i, None, len(MS))
@@ -398,6 +407,31 @@ def side_measurements(fme, dev, args):
         us = float(np.median(ts))
         res[f"shared_expert_fp8_M{M}"] = {"us_median": round(us, 2),
                                          "GBps": round(shared_bytes / (us * 1e-6) / 1e9, 1)}
+    # NVFP4 slot MoE: 48 local experts of a 384-expert router (bytes = unique
+    # local experts x 37,158,912 B of packed E2M1 weights + UE4M3 scales).
+    from oracle import routing
+    ncfg = W.NVFP4
+    nw = W.nvfp4_weights_device(ncfg, args.seed, dev)
+    per_expert = 6144 * 3584 + 7168 * 1536 + 6144 * 448 + 7168 * 192
+    for M in ncfg.Ms:
+        x, logits, rbias = W.nvfp4_activations(ncfg, M, args.seed, 5)
+        ids, wts, _ = routing.route(logits, rbias, ncfg.top_k, 1.0)
+        uniq = len({int(e) for e in ids.reshape(-1) if ncfg.e0 <= e < ncfg.e0 + ncfg.L})
+        xd = torch.from_numpy(x).to(dev).to(torch.bfloat16)
+        idd, wd = torch.from_numpy(ids).to(dev), torch.from_numpy(wts).to(dev)
+        ts = []
+        for i in range(25):
+            flush.add_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fme.moe_routed_nvfp4(xd, idd, wd, *nw, ncfg.e0, ncfg.limit)
+            b.record()
+            torch.cuda.synchronize()
+            if i >= 5:
+                ts.append(a.elapsed_time(b) * 1e3)
+        us = float(np.median(ts))
+        res[f"nvfp4_slot_moe_M{M}"] = {"us_median": round(us, 2), "unique_local_experts": uniq,
+                                       "GBps": round(uniq * per_expert / (us * 1e-6) / 1e9, 1) if uniq else 0.0}
     del flush
     return res
 

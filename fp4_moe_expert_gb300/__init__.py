@@ -37,6 +37,7 @@ SIGNATURES = {
                                       _c_int, _c_float, _vp, _vp, _c_size, _vp]),
     "fme_moe_routed_nvfp4_workspace": (_c_size, [_c_int] * 5),
     "fme_workspace_clear": (_c_int, [_vp, _c_size, _vp]),
+    "fme_selftest_wait_timeout": (_c_int, [_vp, _c_size, _c_int, _vp]),
     "fme_workspace_error": (_c_int, [_vp, ctypes.POINTER(_c_int), _vp]),
     "fme_sm_count": (_c_int, []),
 }

@@ -91,6 +91,26 @@ int ue8m0_unpack(const int32_t* packed, int n, int k, float* dst, int check, int
   return FME_OK;
 }
 
+// Bounded-wait self-test: waits, each with the kernels' own primitives and a
+// time limit, on a global flag nothing sets and on an mbarrier nothing
+// arrives at; both must give up, set their error bits and return.
+__global__ void selftest_wait_kernel(uint32_t* word, const uint32_t* flag, unsigned long long timeout_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire_gpu(flag) == 0u) {
+      if (globaltimer_ns() - t0 > timeout_ns) {
+        atomicOr(word, kErrCrossWait);
+        break;
+      }
+      __nanosleep(256);
+    }
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait(&bar, 0, timeout_ns, nullptr)) atomicOr(word, kErrRingWait);
+  }
+}
+
 }  // namespace fme
 
 using namespace fme;
@@ -201,6 +221,19 @@ int fme_moe_routed_nvfp4(const void* x, const int32_t* topk_ids, const float* to
               FME_EALIGN, "every pointer must be 16-byte aligned");
   return routed_nvfp4(x, topk_ids, topk_weights, w13, s13, w2, s2, M, H, N, L, e0, top_k, limit, y, workspace,
                       workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int fme_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int timeout_ms, void* stream) {
+  FME_REQUIRE(workspace != nullptr && workspace_bytes >= 512, FME_EWORKSPACE, "workspace of 512 bytes needed");
+  FME_REQUIRE(timeout_ms > 0 && timeout_ms <= 10000, FME_EINVAL, "timeout_ms=%d outside [1, 10000]", timeout_ms);
+  FME_REQUIRE(!misaligned(workspace), FME_EALIGN, "workspace must be 16-byte aligned");
+  uint32_t* word = static_cast<uint32_t*>(workspace);
+  const uint32_t* flag = reinterpret_cast<const uint32_t*>(static_cast<uint8_t*>(workspace) + 256);
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      word, flag, static_cast<unsigned long long>(timeout_ms) * 1000000ull);
+  const cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return set_last_error(FME_ECUDA, "selftest launch: %s", cudaGetErrorString(err));
+  return FME_OK;
 }
 
 int fme_workspace_clear(void* workspace, size_t workspace_bytes, void* stream) {

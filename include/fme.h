@@ -207,6 +207,17 @@ int fme_workspace_clear(void* workspace, size_t workspace_bytes, void* stream);
  */
 int fme_workspace_error(void* workspace, int* code, void* stream);
 
+/*
+ * Self-test of the device-side bounded waits (no counterpart in the pages,
+ * whose flag waits poll without a limit). Launches one small kernel that
+ * waits, with the same primitives and a timeout_ms limit as the layer kernels,
+ * on a flag nobody sets (workspace byte 256, which must be zero) and on an
+ * mbarrier nobody arrives at. Both waits give up and set error bits 2 and 1
+ * of the workspace error word; the GPU context stays usable. Read the result
+ * with fme_workspace_error. workspace_bytes >= 512, timeout_ms in [1, 10000].
+ */
+int fme_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int timeout_ms, void* stream);
+
 /* Number of streaming multiprocessors the kernels size their grids to. */
 int fme_sm_count(void);
 
