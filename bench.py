@@ -381,6 +381,76 @@ def e2e_leg(fme, cfg, w13, s13, w2, s2, bias, dev, args):
             "ms_per_step": round(ms / steps, 4)}
 
 
+def _event_us(fn, flush, reps=25, skip=5):
+    """Median device time of fn() in microseconds, L2 flushed before each call."""
+    import torch
+    ts = []
+    for i in range(reps):
+        flush.add_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        if i >= skip:
+            ts.append(a.elapsed_time(b) * 1e3)
+    return float(np.median(ts))
+
+
+def layer_measurements(fme, dev, args, shared_w, shared_bytes, flush):
+    """DSv3 ue8m0 routed experts plus the shared expert, M = 1, 2, 4, 8: the
+    shared-expert call then the routed call on one stream, against the
+    one-launch layer (fme_moe_layer_fp8). Bytes = unique routed experts x
+    expert bytes + the shared expert's bytes."""
+    import torch
+    from synth import workloads as W
+
+    import dataclasses
+    cfg = dataclasses.replace(W.DSV3_UE8M0, E=args.experts)
+    w13, s13, w2, s2 = W.fp8_weights_device(cfg, args.seed, dev)
+    sw13, ss13, sw2, ss2 = shared_w
+    res = {}
+    for M in MS:
+        x, logits, bias = W.fp8_activations(cfg, M, args.seed, 7)
+        xd = torch.from_numpy(x).to(dev).to(torch.bfloat16)
+        ld = torch.from_numpy(logits).to(dev).to(torch.bfloat16)
+        bd = torch.from_numpy(bias).to(dev)
+        routed = (xd, ld, bd, w13, s13, w2, s2, cfg.top_k, cfg.limit, cfg.scale, cfg.ue8m0)
+        shared = (sw13, ss13, sw2, ss2, W.SHARED.limit, W.SHARED.ue8m0)
+        ws_r = fme.Workspace(fme.moe_routed_fp8_workspace(M, cfg.H, cfg.I, cfg.E, cfg.top_k), dev)
+        ws_s = fme.Workspace(fme.shared_expert_fp8_workspace(M, cfg.H, cfg.I), dev)
+        ws_l = fme.Workspace(fme.moe_layer_fp8_workspace(M, cfg.H, cfg.I, cfg.E, cfg.top_k), dev)
+        outs = {}
+
+        def separate():
+            outs["s"] = fme.shared_expert_fp8(xd, *shared, workspace=ws_s)
+            outs["r"] = fme.moe_routed_fp8(*routed, workspace=ws_r)
+
+        def fused():
+            outs["l"] = fme.moe_layer_fp8(*routed, *shared, workspace=ws_l)
+
+        us_sep = _event_us(separate, flush)
+        us_fused = _event_us(fused, flush)
+        us_shared = _event_us(lambda: fme.shared_expert_fp8(xd, *shared, workspace=ws_s), flush)
+        for w in (ws_r, ws_s, ws_l):
+            if w.error() != 0:
+                raise RuntimeError("device wait timed out in the layer measurement")
+        if not torch.equal(outs["l"][1], outs["r"][1]):
+            raise RuntimeError("one-launch layer routed differently from the separate call")
+        uniq = len(set(outs["l"][1].reshape(-1).tolist()))
+        nbytes = uniq * EXPERT_BYTES + shared_bytes
+        res[f"dsv3_ue8m0_plus_shared_M{M}"] = {
+            "unique_experts": uniq,
+            "shared_only_us": round(us_shared, 2),
+            "shared_then_routed_us": round(us_sep, 2),
+            "one_launch_layer_us": round(us_fused, 2),
+            "one_launch_layer_GBps": round(nbytes / (us_fused * 1e-6) / 1e9, 1),
+            "shared_then_routed_GBps": round(nbytes / (us_sep * 1e-6) / 1e9, 1),
+        }
+    del w13, w2
+    return res
+
+
 def side_measurements(fme, dev, args):
     """Shared expert (UE8M0, H 7168 / I 2048) and NVFP4 slot MoE latencies."""
     import torch
@@ -392,6 +462,7 @@ def side_measurements(fme, dev, args):
     w13, s13, w2, s2 = (torch.from_numpy(v).to(dev) for v in (w13, s13, w2, s2))
     shared_bytes = w13.numel() + w2.numel() + 4 * (s13.numel() + s2.numel())
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    res.update(layer_measurements(fme, dev, args, (w13, s13, w2, s2), shared_bytes, flush))
     for M in (1, 8):
         x = torch.from_numpy(W.fp8_activations(W.DSV3, M, args.seed, 3)[0]).to(dev).to(torch.bfloat16)
         ts = []

@@ -32,6 +32,10 @@ SIGNATURES = {
     "fme_shared_expert_fp8": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_float, _c_int, _vp,
                                        _vp, _vp, _c_size, _vp]),
     "fme_shared_expert_fp8_workspace": (_c_size, [_c_int] * 3),
+    "fme_moe_layer_fp8": (_c_int, [_vp, _vp, _c_int, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                   _c_int, _c_float, _c_float, _c_int, _vp, _vp, _vp, _vp, _c_float, _c_int,
+                                   _vp, _vp, _vp, _vp, _vp, _c_size, _vp]),
+    "fme_moe_layer_fp8_workspace": (_c_size, [_c_int] * 5),
     "fme_ue8m0_unpack": (_c_int, [_vp, _c_int, _c_int, _vp, _c_int, _vp, _vp]),
     "fme_moe_routed_nvfp4": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                       _c_int, _c_float, _vp, _vp, _c_size, _vp]),
@@ -161,6 +165,10 @@ def moe_routed_fp8(x, logits, bias, w13, s13, w2, s2, top_k, limit, scale, ue8m0
     return out, ids, weights
 
 
+def shared_expert_fp8_workspace(M, H, I):
+    return lib.fme_shared_expert_fp8_workspace(M, H, I)
+
+
 def shared_expert_fp8(x, w13, s13, w2, s2, limit, ue8m0, out=None, gate_up=None, want_gate_up=False,
                       workspace=None):
     """FP8 shared expert (fme_shared_expert_fp8). w13 [2I, H] (gate rows first),
@@ -179,12 +187,60 @@ def shared_expert_fp8(x, w13, s13, w2, s2, limit, ue8m0, out=None, gate_up=None,
         out = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
     if want_gate_up and gate_up is None:
         gate_up = torch.empty(M, 2 * I, dtype=torch.bfloat16, device=dev)
-    need = lib.fme_shared_expert_fp8_workspace(M, H, I)
+    need = shared_expert_fp8_workspace(M, H, I)
     ws = _workspace(need, dev, workspace)
     _check(lib.fme_shared_expert_fp8(_ptr(x), _ptr(w13), _ptr(s13), _ptr(w2), _ptr(s2), M, H, I, float(limit),
                                      int(bool(ue8m0)), _ptr(gate_up), _ptr(out), ws.ptr(), ws.nbytes,
                                      _stream(dev)))
     return (out, gate_up) if want_gate_up else out
+
+
+def moe_layer_fp8_workspace(M, H, I, E, top_k):
+    return lib.fme_moe_layer_fp8_workspace(M, H, I, E, top_k)
+
+
+def moe_layer_fp8(x, logits, bias, w13, s13, w2, s2, top_k, limit, scale, ue8m0,
+                  shared_w13, shared_s13, shared_w2, shared_s2, shared_limit, shared_ue8m0,
+                  out=None, ids=None, weights=None, shared_out=None, workspace=None):
+    """Routed experts and shared expert in one launch (fme_moe_layer_fp8).
+
+    Routed arguments as moe_routed_fp8; shared_* as shared_expert_fp8 (same H, I).
+    Returns (out [M*top_k, H], ids, weights, shared_out [M, H]).
+    """
+    M, H = x.shape
+    E, n2, _ = w13.shape
+    I = n2 // 2
+    dev = x.device
+    _need(x, torch.bfloat16, (M, H), "x")
+    if logits.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("logits must be float32 or bfloat16")
+    _need(logits, logits.dtype, (M, E), "logits")
+    _need(bias, torch.float32, (E,), "bias")
+    _need(w13, torch.uint8, (E, 2 * I, H), "w13")
+    _need(s13, torch.float32, (E, 2 * I // 128, H // 128), "s13")
+    _need(w2, torch.uint8, (E, H, I), "w2")
+    _need(s2, torch.float32, (E, H // 128, I // 128), "s2")
+    _need(shared_w13, torch.uint8, (2 * I, H), "shared_w13")
+    _need(shared_s13, torch.float32, (2 * I // 128, H // 128), "shared_s13")
+    _need(shared_w2, torch.uint8, (H, I), "shared_w2")
+    _need(shared_s2, torch.float32, (H // 128, I // 128), "shared_s2")
+    if out is None:
+        out = torch.empty(M * top_k, H, dtype=torch.bfloat16, device=dev)
+    if ids is None:
+        ids = torch.empty(M, top_k, dtype=torch.int32, device=dev)
+    if weights is None:
+        weights = torch.empty(M, top_k, dtype=torch.float32, device=dev)
+    if shared_out is None:
+        shared_out = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    need = moe_layer_fp8_workspace(M, H, I, E, top_k)
+    ws = _workspace(need, dev, workspace)
+    ldt = FME_F32 if logits.dtype == torch.float32 else FME_BF16
+    _check(lib.fme_moe_layer_fp8(_ptr(x), _ptr(logits), ldt, _ptr(bias), _ptr(w13), _ptr(s13), _ptr(w2),
+                                 _ptr(s2), M, H, I, E, top_k, float(limit), float(scale), int(bool(ue8m0)),
+                                 _ptr(shared_w13), _ptr(shared_s13), _ptr(shared_w2), _ptr(shared_s2),
+                                 float(shared_limit), int(bool(shared_ue8m0)), _ptr(out), _ptr(ids),
+                                 _ptr(weights), _ptr(shared_out), ws.ptr(), ws.nbytes, _stream(dev)))
+    return out, ids, weights, shared_out
 
 
 def ue8m0_unpack(packed, n, k, check=True):

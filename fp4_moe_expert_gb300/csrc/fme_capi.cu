@@ -149,7 +149,7 @@ static int check_fp8_shapes(int M, int H, int I, int E, int top_k, float limit) 
 
 size_t fme_moe_routed_fp8_workspace(int M, int H, int I, int E, int top_k) {
   if (check_fp8_shapes(M, H, I, E, top_k, 1.0f) != FME_OK) return 0;
-  return fp8_workspace_bytes(M, M * top_k, H, I, E);
+  return layer_fp8_workspace_bytes(M, H, I, E, top_k, false);
 }
 
 int fme_moe_routed_fp8(const void* x, const void* logits, int logits_dtype, const float* bias, const uint8_t* w13,
@@ -166,13 +166,29 @@ int fme_moe_routed_fp8(const void* x, const void* logits, int logits_dtype, cons
                   !misaligned(w2) && !misaligned(s2) && !misaligned(out) && !misaligned(ids) &&
                   !misaligned(weights) && !misaligned(workspace),
               FME_EALIGN, "every pointer must be 16-byte aligned");
-  return routed_fp8(x, logits, logits_dtype, bias, w13, s13, w2, s2, M, H, I, E, top_k, limit, scale, ue8m0, out,
-                    ids, weights, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+  RoutedFp8 r;
+  r.x = x;
+  r.logits = logits;
+  r.logits_dtype = logits_dtype;
+  r.bias = bias;
+  r.w13 = w13;
+  r.s13 = s13;
+  r.w2 = w2;
+  r.s2 = s2;
+  r.E = E;
+  r.top_k = top_k;
+  r.limit = limit;
+  r.scale = scale;
+  r.ue8m0 = ue8m0;
+  r.out = out;
+  r.ids = ids;
+  r.weights = weights;
+  return layer_fp8(r, SharedFp8(), M, H, I, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 size_t fme_shared_expert_fp8_workspace(int M, int H, int I) {
   if (check_fp8_shapes(M, H, I, 1, 1, 1.0f) != FME_OK) return 0;
-  return fp8_workspace_bytes(M, M, H, I, 1);
+  return layer_fp8_workspace_bytes(M, H, I, 0, 0, true);
 }
 
 int fme_shared_expert_fp8(const void* x, const uint8_t* w13, const float* s13, const uint8_t* w2, const float* s2,
@@ -184,8 +200,71 @@ int fme_shared_expert_fp8(const void* x, const uint8_t* w13, const float* s13, c
   FME_REQUIRE(!misaligned(x) && !misaligned(w13) && !misaligned(s13) && !misaligned(w2) && !misaligned(s2) &&
                   !misaligned(out) && !misaligned(gate_up) && !misaligned(workspace),
               FME_EALIGN, "every pointer must be 16-byte aligned");
-  return shared_fp8(x, w13, s13, w2, s2, M, H, I, limit, ue8m0, gate_up, out, workspace, workspace_bytes,
-                    static_cast<cudaStream_t>(stream));
+  SharedFp8 sh;
+  sh.x = x;
+  sh.w13 = w13;
+  sh.s13 = s13;
+  sh.w2 = w2;
+  sh.s2 = s2;
+  sh.limit = limit;
+  sh.ue8m0 = ue8m0;
+  sh.gate_up = gate_up;
+  sh.out = out;
+  return layer_fp8(RoutedFp8(), sh, M, H, I, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+size_t fme_moe_layer_fp8_workspace(int M, int H, int I, int E, int top_k) {
+  if (check_fp8_shapes(M, H, I, E, top_k, 1.0f) != FME_OK) return 0;
+  return layer_fp8_workspace_bytes(M, H, I, E, top_k, true);
+}
+
+int fme_moe_layer_fp8(const void* x, const void* logits, int logits_dtype, const float* bias, const uint8_t* w13,
+                      const float* s13, const uint8_t* w2, const float* s2, int M, int H, int I, int E, int top_k,
+                      float limit, float scale, int ue8m0, const uint8_t* shared_w13, const float* shared_s13,
+                      const uint8_t* shared_w2, const float* shared_s2, float shared_limit, int shared_ue8m0,
+                      void* out, int32_t* ids, float* weights, void* shared_out, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  FME_REQUIRE(x && logits && bias && w13 && s13 && w2 && s2 && out && ids && weights && shared_w13 && shared_s13 &&
+                  shared_w2 && shared_s2 && shared_out,
+              FME_EINVAL, "null pointer argument");
+  int st = check_fp8_shapes(M, H, I, E, top_k, limit);
+  if (st != FME_OK) return st;
+  FME_REQUIRE(shared_limit > 0.0f, FME_EINVAL, "shared_limit must be > 0 (got %g)", static_cast<double>(shared_limit));
+  FME_REQUIRE(logits_dtype == FME_F32 || logits_dtype == FME_BF16, FME_EINVAL, "logits_dtype=%d", logits_dtype);
+  FME_REQUIRE(std::isfinite(scale), FME_EINVAL, "scale must be finite");
+  FME_REQUIRE(!misaligned(x) && !misaligned(logits) && !misaligned(bias) && !misaligned(w13) && !misaligned(s13) &&
+                  !misaligned(w2) && !misaligned(s2) && !misaligned(out) && !misaligned(ids) &&
+                  !misaligned(weights) && !misaligned(shared_w13) && !misaligned(shared_s13) &&
+                  !misaligned(shared_w2) && !misaligned(shared_s2) && !misaligned(shared_out) &&
+                  !misaligned(workspace),
+              FME_EALIGN, "every pointer must be 16-byte aligned");
+  RoutedFp8 r;
+  r.x = x;
+  r.logits = logits;
+  r.logits_dtype = logits_dtype;
+  r.bias = bias;
+  r.w13 = w13;
+  r.s13 = s13;
+  r.w2 = w2;
+  r.s2 = s2;
+  r.E = E;
+  r.top_k = top_k;
+  r.limit = limit;
+  r.scale = scale;
+  r.ue8m0 = ue8m0;
+  r.out = out;
+  r.ids = ids;
+  r.weights = weights;
+  SharedFp8 sh;
+  sh.x = x;
+  sh.w13 = shared_w13;
+  sh.s13 = shared_s13;
+  sh.w2 = shared_w2;
+  sh.s2 = shared_s2;
+  sh.limit = shared_limit;
+  sh.ue8m0 = shared_ue8m0;
+  sh.out = shared_out;
+  return layer_fp8(r, sh, M, H, I, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 int fme_ue8m0_unpack(const int32_t* packed, int n, int k, float* dst, int check, int* mismatch, void* stream) {

@@ -26,6 +26,7 @@ constexpr int kFp8MaxCtas = 160;                 // grid cap of the FP8 kernel (
 constexpr uint32_t kErrRingWait = 1u;  // a ring stage never landed
 constexpr uint32_t kErrCrossWait = 2u;
 constexpr uint32_t kErrDrain = 4u;
+constexpr uint32_t kErrRoute = 8u;  // an output row outside its tensor (write skipped)
 
 // Thread layout of one GEMM phase: `rg` groups of `tpr` threads; a thread owns
 // K slices s = t + tpr * i (16 bytes each) and the group owns 8 rows of an item.

@@ -22,19 +22,48 @@ bool ensure_smem_attr(int dev, const void* kernel, size_t bytes);
 // override, default 1000 ms).
 unsigned long long wait_timeout_ns();
 
-size_t fp8_workspace_bytes(int M, int routes, int H, int I, int E);
-// Leading workspace bytes (error word and counters) that must be zero when a call starts.
-size_t fp8_workspace_zero_bytes(int M, int routes, int H, int I, int E);
 size_t nvfp4_workspace_bytes(int M, int H, int N, int L, int top_k);
 
-int routed_fp8(const void* x, const void* logits, int logits_dtype, const float* bias, const uint8_t* w13,
-               const float* s13, const uint8_t* w2, const float* s2, int M, int H, int I, int E, int top_k,
-               float limit, float scale, int ue8m0, void* out, int32_t* ids, float* weights, void* workspace,
-               size_t workspace_bytes, cudaStream_t st);
+// The routed experts of one FP8 layer call (E == 0: none).
+struct RoutedFp8 {
+  const void* x = nullptr;
+  const void* logits = nullptr;
+  int logits_dtype = 0;
+  const float* bias = nullptr;
+  const uint8_t* w13 = nullptr;
+  const float* s13 = nullptr;
+  const uint8_t* w2 = nullptr;
+  const float* s2 = nullptr;
+  int E = 0, top_k = 0;
+  float limit = 0.0f, scale = 1.0f;
+  int ue8m0 = 0;
+  void* out = nullptr;
+  int32_t* ids = nullptr;
+  float* weights = nullptr;
+};
 
-int shared_fp8(const void* x, const uint8_t* w13, const float* s13, const uint8_t* w2, const float* s2, int M,
-               int H, int I, float limit, int ue8m0, void* gate_up, void* out, void* workspace,
-               size_t workspace_bytes, cudaStream_t st);
+// The shared expert of one FP8 layer call (w13 == nullptr: none).
+struct SharedFp8 {
+  const void* x = nullptr;
+  const uint8_t* w13 = nullptr;
+  const float* s13 = nullptr;
+  const uint8_t* w2 = nullptr;
+  const float* s2 = nullptr;
+  float limit = 0.0f;
+  int ue8m0 = 0;
+  void* gate_up = nullptr;
+  void* out = nullptr;
+};
+
+// One launch of the tcgen05 kernel over the routed experts and/or the shared
+// expert of M tokens (arguments already validated).
+int layer_fp8(const RoutedFp8& r, const SharedFp8& sh, int M, int H, int I, void* workspace, size_t workspace_bytes,
+              cudaStream_t st);
+// Workspace bytes of a layer_fp8 call (E routed experts, 0 for the shared
+// expert alone with top_k 0), and its leading bytes (error word and counters)
+// that must be zero when a call starts.
+size_t layer_fp8_workspace_bytes(int M, int H, int I, int E, int top_k, bool shared);
+size_t layer_fp8_zero_bytes(int M, int H, int I, int E, int top_k, bool shared);
 
 int routed_nvfp4(const void* x, const int32_t* ids, const float* weights, const uint8_t* w13, const uint8_t* s13,
                  const uint8_t* w2, const uint8_t* s2, int M, int H, int N, int L, int e0, int top_k, float limit,

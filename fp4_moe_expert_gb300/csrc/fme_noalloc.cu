@@ -69,7 +69,7 @@ extern "C" int fme_moe_routed_fp8_noalloc(const void* x, const void* logits, int
   // The array keeps whatever the previous call left; start from a zeroed
   // error word and zeroed counters (the rest is written before it is read).
   const cudaError_t err =
-      cudaMemsetAsync(scratch, 0, fme::fp8_workspace_zero_bytes(M, M * top_k, H, I, E),
+      cudaMemsetAsync(scratch, 0, fme::layer_fp8_zero_bytes(M, H, I, E, top_k, false),
                       static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return fme::set_last_error(FME_ECUDA, "cudaMemsetAsync: %s", cudaGetErrorString(err));
   return fme_moe_routed_fp8(x, logits, logits_dtype, bias, w13, s13, w2, s2, M, H, I, E, top_k, limit, scale,

@@ -36,8 +36,6 @@
 
 namespace fme {
 
-enum : int { kModeRouted = 0, kModeShared = 1 };
-
 constexpr int kTcThreads = 256;  // TMA, MMA, 4 accumulate, 2 fill warps
 constexpr int kFillThreads = 64;
 constexpr int kTcStages = 8;
@@ -49,28 +47,35 @@ constexpr int kMaxKc = 16;
 constexpr int kTokGroups = kMaxTokens / 16;
 
 struct TcArgs {
-  CUtensorMap map13;  // W13 as [E * 2I rows, H bytes], box 64 rows x 128 bytes
-  CUtensorMap map2;   // W2 as [E * H rows, I bytes]
+  CUtensorMap map13;   // routed W13 as [E * 2I rows, H bytes], box 64 rows x 128 bytes
+  CUtensorMap map2;    // routed W2 as [E * H rows, I bytes]
+  CUtensorMap smap13;  // shared-expert gate_up as [2I rows, H bytes]
+  CUtensorMap smap2;   // shared-expert down as [H rows, I bytes]
   const __nv_bfloat16* x;
   const void* logits;
   const float* bias;
   const float* s13;
   const float* s2;
-  __nv_bfloat16* out;
+  const float* ss13;   // shared-expert block scales
+  const float* ss2;
+  __nv_bfloat16* out;   // routed rows [M * top_k, H]
+  __nv_bfloat16* sout;  // shared-expert rows [M, H]
   int32_t* ids;
   float* weights;
   __nv_bfloat16* gate_up;
   uint32_t* err;
-  uint32_t* done;    // [E] GEMM1 tiles finished per expert
-  uint32_t* passed;  // [E] CTAs whose GEMM2 work passed the wait
-  uint32_t* cnt1;    // [E * I/64] contributors arrived per GEMM1 tile (expert id, tile)
-  uint32_t* cnt2;    // [E * H/128] per GEMM2 tile
-  float* hbuf;       // [routes, I] SwiGLU output
+  uint32_t* done;    // [E + 1] GEMM1 tiles finished per expert (id E: the shared expert)
+  uint32_t* passed;  // [E + 1] CTAs whose GEMM2 work passed the wait
+  uint32_t* cnt1;    // [(E + 1) * I/64] contributors arrived per GEMM1 tile (expert id, tile)
+  uint32_t* cnt2;    // [(E + 1) * H/128] per GEMM2 tile
+  float* hbuf;       // [M * top_k + M, I] SwiGLU output (routed routes, then shared tokens)
   float* part;       // [2 phases][kFp8MaxCtas][2 slots][tokens][128 rows] split-tile partials
-  int M, H, I, E, top_k;
+  int M, H, I, E, top_k;  // E routed experts (0: shared expert only)
   int ptok;          // token rows of one partial slot (min(M, 64))
   float limit, scale;
-  int ue8m0, logits_f32, mode;
+  float slimit;      // shared-expert SwiGLU clamp
+  int ue8m0, logits_f32, has_shared;
+  int sue8m0;        // shared-expert activation scales rounded up to powers of two
   unsigned long long timeout_ns;
 };
 
@@ -101,6 +106,48 @@ constexpr size_t kTcSmemBytes = sizeof(TcSmem) + 1024;
 __device__ __forceinline__ void tc_error(const TcArgs& a, TcSmem& S, uint32_t bit) {
   atomicOr(a.err, bit);
   S.abort = 1;
+}
+
+// What differs per work expert: the routed experts of the unique list, then
+// (when present) the shared expert as the last unit, routed to every token.
+// The shared expert follows "shared_expert" (gate rows first, BF16 gate_up and
+// h, re-quant by multiplying with the inverse); routed experts follow
+// "mega_moe" (up rows first, FP32 h, re-quant by dividing).
+struct XInfo {
+  bool shared;
+  int id;     // counter index: routed expert id, or E for the shared expert
+  int row_e;  // expert index within its tensor maps
+  const CUtensorMap* m13;
+  const CUtensorMap* m2;
+  const float* s13;
+  const float* s2;
+  float limit;
+  bool ue8m0;
+};
+
+__device__ __forceinline__ XInfo xinfo(const TcArgs& a, const TcSmem& S, int u) {
+  XInfo x;
+  x.shared = a.has_shared && u == S.U - 1;
+  if (x.shared) {
+    x.id = a.E;
+    x.row_e = 0;
+    x.m13 = &a.smap13;
+    x.m2 = &a.smap2;
+    x.s13 = a.ss13;
+    x.s2 = a.ss2;
+    x.limit = a.slimit;
+    x.ue8m0 = a.sue8m0 != 0;
+  } else {
+    x.id = S.ulist[u];
+    x.row_e = x.id;
+    x.m13 = &a.map13;
+    x.m2 = &a.map2;
+    x.s13 = a.s13;
+    x.s2 = a.s2;
+    x.limit = a.limit;
+    x.ue8m0 = a.ue8m0 != 0;
+  }
+  return x;
 }
 
 // The four accumulate warps and the two fill warps each sync among themselves.
@@ -247,8 +294,9 @@ struct Cursor {
 __device__ void fill_context(const TcArgs& a, TcSmem& S, int u, int b, int fid) {
   if (fid < 32) {
     const int lane = fid;
-    if (a.mode == kModeShared) {
-      for (int t = lane; t < a.M; t += 32) S.ctx_route[b][t] = static_cast<int16_t>(t);
+    if (a.has_shared && u == S.U - 1) {
+      // The shared expert's rows follow the routed ones in hbuf: M*top_k + t.
+      for (int t = lane; t < a.M; t += 32) S.ctx_route[b][t] = static_cast<int16_t>(a.M * a.top_k + t);
       if (lane == 0) S.ctx_n[b] = a.M;
     } else {
       const int e = S.ulist[u];
@@ -283,19 +331,20 @@ __device__ void fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
   const int r = S.ctx_n[b];
   const int N = P.N;
   uint8_t* B = S.B[b];
+  const XInfo xi = xinfo(a, S, ch.u);
   // Weight block scales of the chunk's K blocks ([first/second row half][j]
   // for GEMM1: row blocks T/2 and I/128 + T/2; [0][j] for GEMM2: row block T),
   // loaded together with the first activations.
   float wsv = 0.0f;
   if (fid < 2 * kMaxKc) {
     const int half = fid / kMaxKc, j = fid % kMaxKc;
-    const int e = a.mode == kModeShared ? 0 : S.ulist[ch.u];
+    const int e = xi.row_e;
     if (j < ch.kc) {
       if (ch.phase == 1) {
         const int rb = (half == 0 ? 0 : a.I / 128) + ch.T / 2;
-        wsv = __ldg(a.s13 + (static_cast<size_t>(e) * (2 * a.I / 128) + rb) * (a.H / 128) + ch.kb0 + j);
+        wsv = __ldg(xi.s13 + (static_cast<size_t>(e) * (2 * a.I / 128) + rb) * (a.H / 128) + ch.kb0 + j);
       } else if (half == 0) {
-        wsv = __ldg(a.s2 + (static_cast<size_t>(e) * (a.H / 128) + ch.T) * (a.I / 128) + ch.kb0 + j);
+        wsv = __ldg(xi.s2 + (static_cast<size_t>(e) * (a.H / 128) + ch.T) * (a.I / 128) + ch.kb0 + j);
       }
     }
   }
@@ -317,7 +366,7 @@ __device__ void fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
         const int route = S.ctx_route[b][tt[q]];
         const int col = (ch.kb0 + jj[q]) * 128 + sub * 16;
         if (ch.phase == 1) {
-          const int tok = a.mode == kModeShared ? route : route / a.top_k;
+          const int tok = xi.shared ? route - a.M * a.top_k : route / a.top_k;
           const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(tok) * K + col);
           const uint4 q0 = __ldg(src), q1 = __ldg(src + 1);
           const uint32_t wd[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
@@ -355,9 +404,9 @@ __device__ void fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
       if (tt[q] >= 0) {
         const int t = tt[q], j = jj[q];
         float scale = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
-        if (a.ue8m0) scale = ue8m0_ceil(scale);
+        if (xi.ue8m0) scale = ue8m0_ceil(scale);
         float qv[16];
-        if (ch.phase == 2 && a.mode == kModeRouted) {
+        if (ch.phase == 2 && !xi.shared) {
 #pragma unroll
           for (int k = 0; k < 16; ++k) qv[k] = __fdiv_rn(v[q][k], scale);
         } else {
@@ -401,9 +450,11 @@ __device__ void fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
 __device__ void finish_gemm1(const TcArgs& a, TcSmem& S, const Chunk& ch, int b, const float (&y)[kMaxTokens],
                              int row, int etid) {
   const int r = S.seg_n;
+  const XInfo xi = xinfo(a, S, ch.u);
+  const bool shared = xi.shared;
   const bool second = row >= 64;
   const int q = row & 63;
-  const float L = a.limit;
+  const float L = xi.limit;
 #pragma unroll
   for (int g = 0; g < kTokGroups; ++g) {
     if (g * 16 < r) {
@@ -419,7 +470,7 @@ __device__ void finish_gemm1(const TcArgs& a, TcSmem& S, const Chunk& ch, int b,
             const int route = S.seg_route[g * 16 + t];
             const float first = y[g * 16 + t], sec = S.ysm[t][q];
             float h;
-            if (a.mode == kModeRouted) {
+            if (!shared) {
               // W31: up rows first, then gate rows ("mega_moe" module docstring).
               const float gate = fminf(sec, L);
               const float up = fmaxf(fminf(first, L), -L);
@@ -429,8 +480,9 @@ __device__ void finish_gemm1(const TcArgs& a, TcSmem& S, const Chunk& ch, int b,
               const __nv_bfloat16 gb = __float2bfloat16_rn(first);
               const __nv_bfloat16 ub = __float2bfloat16_rn(sec);
               if (a.gate_up != nullptr) {
-                a.gate_up[static_cast<size_t>(route) * 2 * a.I + 64 * ch.T + q] = gb;
-                a.gate_up[static_cast<size_t>(route) * 2 * a.I + a.I + 64 * ch.T + q] = ub;
+                const size_t tok = static_cast<size_t>(route - a.M * a.top_k);
+                a.gate_up[tok * 2 * a.I + 64 * ch.T + q] = gb;
+                a.gate_up[tok * 2 * a.I + a.I + 64 * ch.T + q] = ub;
               }
               const float gate = fminf(__bfloat162float(gb), L);
               const float up = fmaxf(fminf(__bfloat162float(ub), L), -L);
@@ -446,7 +498,7 @@ __device__ void finish_gemm1(const TcArgs& a, TcSmem& S, const Chunk& ch, int b,
   }
   if (etid == 0) {
     __threadfence();
-    red_release_gpu_add(a.done + (a.mode == kModeShared ? 0 : S.ulist[ch.u]), 1u);
+    red_release_gpu_add(a.done + xi.id, 1u);
   }
 }
 
@@ -454,9 +506,21 @@ __device__ void finish_gemm2(const TcArgs& a, TcSmem& S, const Chunk& ch, int b,
                              int row) {
   const int r = S.seg_n;
   const int m = 128 * ch.T + row;
+  const bool shared = a.has_shared && ch.u == S.U - 1;
+  // Routed rows go to out[route]; the shared expert's (routes M*top_k + t) to sout[t].
+  __nv_bfloat16* dst = shared ? a.sout : a.out;
+  const int row0 = shared ? a.M * a.top_k : 0;
+  const int rows = shared ? a.M : a.M * a.top_k;
 #pragma unroll
-  for (int t = 0; t < kMaxTokens; ++t)
-    if (t < r) a.out[static_cast<size_t>(S.seg_route[t]) * a.H + m] = __float2bfloat16_rn(y[t]);
+  for (int t = 0; t < kMaxTokens; ++t) {
+    const int o = S.seg_route[t] - row0;
+    if (t < r) {
+      if (o >= 0 && o < rows)
+        dst[static_cast<size_t>(o) * a.H + m] = __float2bfloat16_rn(y[t]);
+      else
+        atomicOr(a.err, kErrRoute);
+    }
+  }
 }
 
 __device__ __forceinline__ float* part_slot(const TcArgs& a, int phase, int c, int slot) {
@@ -479,7 +543,7 @@ __device__ void end_segment(const TcArgs& a, TcSmem& S, const Plan& P, const Chu
     __threadfence();
     epi_bar();
     if (etid == 0) {
-      const int e = a.mode == kModeShared ? 0 : S.ulist[ch.u];
+      const int e = xinfo(a, S, ch.u).id;
       uint32_t* cnt = ch.phase == 1 ? a.cnt1 + static_cast<size_t>(e) * pp.tiles + ch.T
                                     : a.cnt2 + static_cast<size_t>(e) * pp.tiles + ch.T;
       const uint32_t old = atomicAdd(cnt, 1u);
@@ -509,7 +573,7 @@ __device__ void end_segment(const TcArgs& a, TcSmem& S, const Plan& P, const Chu
 // the last CTA with GEMM2 work on it re-arms the counters for the next call.
 __device__ bool wait_hidden(const TcArgs& a, TcSmem& S, const Plan& P, int u, int fid) {
   if (fid == 0) {
-    const int e = a.mode == kModeShared ? 0 : S.ulist[u];
+    const int e = xinfo(a, S, u).id;
     const uint32_t target = static_cast<uint32_t>(P.p[0].tiles);
     const uint64_t t0 = globaltimer_ns();
     bool ok = true;
@@ -594,25 +658,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
     mbar_init(&S.final_bar, 1);
     fence_mbar_init();
     S.abort = 0;
-    prefetch_tmap(&a.map13);
-    prefetch_tmap(&a.map2);
+    if (a.E > 0) {
+      prefetch_tmap(&a.map13);
+      prefetch_tmap(&a.map2);
+    }
+    if (a.has_shared) {
+      prefetch_tmap(&a.smap13);
+      prefetch_tmap(&a.smap2);
+    }
   }
   if (warp == 1) {
     tmem_alloc(&S.tmem_base, kTmemCols);
     tmem_relinquish();
   }
   for (int e = tid; e < a.E; e += kTcThreads) S.tokmask[e] = 0ull;
-  {  // B buffers start zero
+  {  // B buffers start zero (read by the tensor cores through the async proxy)
     uint4* z = reinterpret_cast<uint4*>(&S.B[0][0]);
     for (int i = tid; i < 2 * kBBufBytes / 16; i += kTcThreads) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
   }
   griddep_wait();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
 
-  // ---- routing and the unique-expert list
-  if (a.mode == kModeRouted) {
+  // ---- routing and the unique-expert list (routed experts first, then the shared one)
+  if (a.E > 0) {
     for (int t = warp; t < a.M; t += kTcThreads / 32) {
       // Lane l holds experts l + 32 j, j < J: loops sized to the expert count.
       if (a.E <= 64)
@@ -637,13 +708,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
         rmax = max(rmax, static_cast<int>(__reduce_max_sync(0xFFFFFFFFu, static_cast<uint32_t>(__popcll(m)))));
       }
       if (lane == 0) {
-        S.U = U;
-        S.rmax = rmax;
+        S.U = U + a.has_shared;
+        S.rmax = a.has_shared ? max(rmax, a.M) : rmax;
       }
     }
   } else if (tid == 0) {
-    S.U = 1;
-    S.ulist[0] = 0;
+    S.U = 1;  // shared expert only
     S.rmax = a.M;
   }
   __syncthreads();
@@ -663,15 +733,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
       const uint64_t pol = l2_evict_first_policy();
       // Rows (two 64-row boxes) and tensor map of K block j of a chunk.
       auto coords = [&](const Chunk& c, int& ra, int& rb, const void*& map) {
-        const int e = a.mode == kModeShared ? 0 : S.ulist[c.u];
+        const XInfo xi = xinfo(a, S, c.u);
+        const int e = xi.row_e;
         if (c.phase == 1) {
           ra = e * 2 * a.I + 64 * c.T;
           rb = ra + a.I;
-          map = &a.map13;
+          map = xi.m13;
         } else {
           ra = e * a.H + 128 * c.T;
           rb = ra + 64;
-          map = &a.map2;
+          map = xi.m2;
         }
       };
       Cursor cur{P.p[0].lo, 1};
@@ -904,18 +975,10 @@ static TcWorkspace tc_layout(void* base, int M, int routes, int H, int I, int E)
   return w;
 }
 
-size_t fp8_workspace_bytes(int M, int routes, int H, int I, int E) {
-  return tc_layout(nullptr, M, routes, H, I, E).bytes;
-}
-
-size_t fp8_workspace_zero_bytes(int M, int routes, int H, int I, int E) {
-  return tc_layout(nullptr, M, routes, H, I, E).zero_bytes;
-}
-
-static int launch_tc(TcArgs& a, const uint8_t* w13, const uint8_t* w2, void* workspace, size_t workspace_bytes,
-                     int routes, cudaStream_t st) {
-  const int E = a.mode == kModeShared ? 1 : a.E;
-  const TcWorkspace w = tc_layout(workspace, a.M, routes, a.H, a.I, E);
+static int launch_tc(TcArgs& a, const uint8_t* w13, const uint8_t* w2, const uint8_t* sw13, const uint8_t* sw2,
+                     void* workspace, size_t workspace_bytes, cudaStream_t st) {
+  const int routes = a.M * a.top_k + (a.has_shared ? a.M : 0);
+  const TcWorkspace w = tc_layout(workspace, a.M, routes, a.H, a.I, a.E + 1);
   if (workspace == nullptr || workspace_bytes < w.bytes)
     return set_last_error(FME_EWORKSPACE, "workspace of %zu bytes needed, %zu given", w.bytes, workspace_bytes);
   a.err = w.err;
@@ -927,8 +990,11 @@ static int launch_tc(TcArgs& a, const uint8_t* w13, const uint8_t* w2, void* wor
   a.part = w.part;
   a.ptok = w.ptok;
   a.timeout_ns = wait_timeout_ns();
-  if (!make_map(&a.map13, w13, static_cast<unsigned long long>(E) * 2 * a.I, a.H) ||
-      !make_map(&a.map2, w2, static_cast<unsigned long long>(E) * a.H, a.I))
+  if (a.E > 0 && (!make_map(&a.map13, w13, static_cast<unsigned long long>(a.E) * 2 * a.I, a.H) ||
+                  !make_map(&a.map2, w2, static_cast<unsigned long long>(a.E) * a.H, a.I)))
+    return set_last_error(FME_ECUDA, "cuTensorMapEncodeTiled failed or unavailable");
+  if (a.has_shared && (!make_map(&a.smap13, sw13, static_cast<unsigned long long>(2) * a.I, a.H) ||
+                       !make_map(&a.smap2, sw2, static_cast<unsigned long long>(a.H), a.I)))
     return set_last_error(FME_ECUDA, "cuTensorMapEncodeTiled failed or unavailable");
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return set_last_error(FME_ECUDA, "cudaGetDevice failed");
@@ -950,53 +1016,52 @@ static int launch_tc(TcArgs& a, const uint8_t* w13, const uint8_t* w2, void* wor
   return FME_OK;
 }
 
-int routed_fp8(const void* x, const void* logits, int logits_dtype, const float* bias, const uint8_t* w13,
-               const float* s13, const uint8_t* w2, const float* s2, int M, int H, int I, int E, int top_k,
-               float limit, float scale, int ue8m0, void* out, int32_t* ids, float* weights, void* workspace,
-               size_t workspace_bytes, cudaStream_t st) {
+int layer_fp8(const RoutedFp8& r, const SharedFp8& sh, int M, int H, int I, void* workspace, size_t workspace_bytes,
+              cudaStream_t st) {
   TcArgs a;
   memset(&a, 0, sizeof(a));
-  a.x = static_cast<const __nv_bfloat16*>(x);
-  a.logits = logits;
-  a.bias = bias;
-  a.s13 = s13;
-  a.s2 = s2;
-  a.out = static_cast<__nv_bfloat16*>(out);
-  a.ids = ids;
-  a.weights = weights;
   a.M = M;
   a.H = H;
   a.I = I;
-  a.E = E;
-  a.top_k = top_k;
-  a.limit = limit;
-  a.scale = scale;
-  a.ue8m0 = ue8m0 ? 1 : 0;
-  a.logits_f32 = logits_dtype == FME_F32 ? 1 : 0;
-  a.mode = kModeRouted;
-  return launch_tc(a, w13, w2, workspace, workspace_bytes, M * top_k, st);
+  a.scale = 1.0f;
+  if (r.E > 0) {
+    a.x = static_cast<const __nv_bfloat16*>(r.x);
+    a.logits = r.logits;
+    a.bias = r.bias;
+    a.s13 = r.s13;
+    a.s2 = r.s2;
+    a.out = static_cast<__nv_bfloat16*>(r.out);
+    a.ids = r.ids;
+    a.weights = r.weights;
+    a.E = r.E;
+    a.top_k = r.top_k;
+    a.limit = r.limit;
+    a.scale = r.scale;
+    a.ue8m0 = r.ue8m0 ? 1 : 0;
+    a.logits_f32 = r.logits_dtype == FME_F32 ? 1 : 0;
+  }
+  if (sh.w13 != nullptr) {
+    a.x = static_cast<const __nv_bfloat16*>(sh.x);
+    a.has_shared = 1;
+    a.ss13 = sh.s13;
+    a.ss2 = sh.s2;
+    a.sout = static_cast<__nv_bfloat16*>(sh.out);
+    a.gate_up = static_cast<__nv_bfloat16*>(sh.gate_up);
+    a.slimit = sh.limit;
+    a.sue8m0 = sh.ue8m0 ? 1 : 0;
+  }
+  return launch_tc(a, r.w13, r.w2, sh.w13, sh.w2, workspace, workspace_bytes, st);
 }
 
-int shared_fp8(const void* x, const uint8_t* w13, const float* s13, const uint8_t* w2, const float* s2, int M,
-               int H, int I, float limit, int ue8m0, void* gate_up, void* out, void* workspace,
-               size_t workspace_bytes, cudaStream_t st) {
-  TcArgs a;
-  memset(&a, 0, sizeof(a));
-  a.x = static_cast<const __nv_bfloat16*>(x);
-  a.s13 = s13;
-  a.s2 = s2;
-  a.out = static_cast<__nv_bfloat16*>(out);
-  a.gate_up = static_cast<__nv_bfloat16*>(gate_up);
-  a.M = M;
-  a.H = H;
-  a.I = I;
-  a.E = 1;
-  a.top_k = 1;
-  a.limit = limit;
-  a.scale = 1.0f;
-  a.ue8m0 = ue8m0 ? 1 : 0;
-  a.mode = kModeShared;
-  return launch_tc(a, w13, w2, workspace, workspace_bytes, M, st);
+// Counter slots are sized for the routed experts plus the shared expert
+// whether or not a call has it, so routed-only and one-launch calls with the
+// same sizes lay out their counters alike and can share one workspace.
+size_t layer_fp8_workspace_bytes(int M, int H, int I, int E, int top_k, bool shared) {
+  return tc_layout(nullptr, M, M * top_k + (shared ? M : 0), H, I, E + 1).bytes;
+}
+
+size_t layer_fp8_zero_bytes(int M, int H, int I, int E, int top_k, bool shared) {
+  return tc_layout(nullptr, M, M * top_k + (shared ? M : 0), H, I, E + 1).zero_bytes;
 }
 
 }  // namespace fme

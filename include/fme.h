@@ -21,8 +21,11 @@
  *   use (fme_workspace_clear). Every successful call leaves its counters at
  *   zero again, so one workspace serves any number of calls issued in stream
  *   order, including calls with fewer tokens M than it was sized for (same
- *   other sizes). Two calls that overlap on the GPU need two workspaces.
- *   After a device-side error, clear it again before reuse.
+ *   other sizes). fme_moe_routed_fp8 and fme_moe_layer_fp8 calls with the same
+ *   H, I, E and top_k may share one workspace (sized for the larger need);
+ *   the shared-expert and NVFP4 calls each need their own. Two calls that
+ *   overlap on the GPU need two workspaces. After a device-side error, clear
+ *   it again before reuse.
  * - BF16 is IEEE bfloat16 (uint16 bit patterns). FP8 is E4M3 ("e4m3fn": no
  *   infinities, 0x7F/0xFF are NaN). FP4 is E2M1, sign in bit 3.
  */
@@ -152,6 +155,42 @@ int fme_shared_expert_fp8(const void* x, const uint8_t* w13, const float* s13, c
 size_t fme_shared_expert_fp8_workspace(int M, int H, int I);
 
 /*
+ * Routed experts and shared expert of one FP8 decode layer in one launch.
+ *
+ * Sources: the routed part is fme_moe_routed_fp8 ("mega_moe"), the shared
+ * part fme_shared_expert_fp8 ("shared_expert"), each with its own rounding
+ * rules, weight layout (routed: up rows first; shared: gate rows first) and
+ * clamp. The "shared_expert" page runs its two GEMVs as separate small kernels
+ * beside the mega MoE kernel, sharing its SMs; here the shared expert is one
+ * more unit of work in the routed kernel's schedule, so its 44 MB of weights
+ * stream in the same pass as the routed experts' and no second launch or
+ * GEMM1 -> GEMM2 drain is paid for it. Every token routes to it.
+ *
+ * Arguments: those of fme_moe_routed_fp8 (x, logits, bias, routed weights,
+ * M, H, I, E, top_k, limit, scale, ue8m0, out, ids, weights), plus the shared
+ * expert's shared_w13 [2I, H] E4M3, shared_s13 [2I/128, H/128] FP32,
+ * shared_w2 [H, I] E4M3, shared_s2 [H/128, I/128] FP32, its clamp
+ * shared_limit (> 0, +inf allowed) and scale flag shared_ue8m0, and its
+ * output shared_out [M, H] BF16. The shared expert has the routed experts'
+ * H and I. ids and weights equal those of fme_moe_routed_fp8 bit for bit;
+ * out and shared_out meet the same tolerances. They can differ from the
+ * separate calls in the last bit of a few elements: the K blocks of a tile are
+ * split over CTAs by the total work, which the extra unit changes, and that
+ * changes the FP32 summation order.
+ * workspace / workspace_bytes: see fme_moe_layer_fp8_workspace.
+ */
+int fme_moe_layer_fp8(const void* x, const void* logits, int logits_dtype, const float* bias,
+                      const uint8_t* w13, const float* s13, const uint8_t* w2, const float* s2,
+                      int M, int H, int I, int E, int top_k, float limit, float scale, int ue8m0,
+                      const uint8_t* shared_w13, const float* shared_s13, const uint8_t* shared_w2,
+                      const float* shared_s2, float shared_limit, int shared_ue8m0, void* out,
+                      int32_t* ids, float* weights, void* shared_out, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* Workspace bytes fme_moe_layer_fp8 needs for these sizes (0 on bad sizes). */
+size_t fme_moe_layer_fp8_workspace(int M, int H, int I, int E, int top_k);
+
+/*
  * Packed UE8M0 block scales -> FP32 block scales.
  *
  * Source: "vllm.models.glm5next.nvidia.specialized_decode.shared_expert",
@@ -202,7 +241,8 @@ int fme_workspace_clear(void* workspace, size_t workspace_bytes, void* stream);
 /*
  * Read and clear the device error word of a workspace (synchronises stream).
  * *code receives 0 or a bit set: 1 = a ring wait timed out, 2 = a cross-CTA
- * wait timed out, 4 = the producer could not drain its copies. Returns
+ * wait timed out, 4 = the producer could not drain its copies, 8 = an output
+ * row index fell outside its tensor (the write was skipped). Returns
  * FME_ETIMEOUT when *code != 0, FME_OK otherwise.
  */
 int fme_workspace_error(void* workspace, int* code, void* stream);

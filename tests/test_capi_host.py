@@ -77,3 +77,36 @@ def test_nvfp4_and_unpack_validation(fme):
     assert rc == -1
     assert fme.lib.fme_ue8m0_unpack(vp(16), 100, 512, vp(16), 0, None, None) == -1
     assert fme.lib.fme_ue8m0_unpack(None, 128, 512, vp(16), 0, None, None) == -1
+
+
+def test_binding_exposes_a_wrapper_per_entry_point(fme):
+    for name in ("moe_routed_fp8", "moe_routed_fp8_workspace", "moe_layer_fp8", "moe_layer_fp8_workspace",
+                 "shared_expert_fp8", "shared_expert_fp8_workspace", "moe_routed_nvfp4",
+                 "moe_routed_nvfp4_workspace", "ue8m0_unpack"):
+        assert callable(getattr(fme, name)), name
+
+
+def _layer(fme, **kw):
+    vp = ctypes.c_void_p
+    args = dict(x=vp(16), logits=vp(16), dt=0, bias=vp(16), w13=vp(16), s13=vp(16), w2=vp(16), s2=vp(16),
+                M=1, H=512, I=256, E=8, k=2, limit=7.0, scale=1.0, ue=0, sw13=vp(16), ss13=vp(16), sw2=vp(16),
+                ss2=vp(16), slimit=7.0, sue=1, out=vp(16), ids=vp(16), weights=vp(16), sout=vp(16), ws=vp(16),
+                wsb=1 << 20, st=None)
+    args.update(kw)
+    return fme.lib.fme_moe_layer_fp8(*args.values())
+
+
+def test_layer_validation_and_workspace(fme):
+    assert _layer(fme, sw13=None) == -1               # the shared expert is required
+    assert _layer(fme, sout=None) == -1
+    assert _layer(fme, slimit=0.0) == -1
+    assert _layer(fme, M=65) == -2
+    assert _layer(fme, k=9) == -1
+    assert _layer(fme, ss2=ctypes.c_void_p(20)) == -3
+    # the one-launch layer needs the routed call's bytes plus M hidden rows
+    routed = fme.moe_routed_fp8_workspace(8, 7168, 2048, 256, 8)
+    layer = fme.moe_layer_fp8_workspace(8, 7168, 2048, 256, 8)
+    assert layer >= routed + 8 * 2048 * 4 - 256
+    assert fme.moe_layer_fp8_workspace(0, 7168, 2048, 256, 8) == 0
+    # a workspace too small for the call is refused before any launch
+    assert _layer(fme, wsb=64) in (-6, -4)
