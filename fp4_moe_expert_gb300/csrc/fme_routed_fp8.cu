@@ -44,7 +44,13 @@ constexpr int kBBufBytes = 256 * 128;    // K blocks x N token rows x 128 bytes 
 constexpr int kTmemCols = 512;
 constexpr int kTmemBuf = 256;            // two accumulator buffers
 constexpr int kMaxKc = 16;
-constexpr int kTokGroups = kMaxTokens / 16;
+// GEMM2 K blocks per CTA prefetched into L2 once every CTA has issued all its
+// GEMM1 loads. The GEMM1 -> GEMM2 hand-over of an expert (its last tiles
+// finishing, the hidden rows being re-quantised) otherwise leaves HBM idle;
+// waiting for the whole grid's GEMM1 loads first keeps the prefetch from
+// delaying any GEMM1 stream. 40 slots = 640 KB per CTA, about 97 MB over
+// 152 CTAs, within the 129 MB L2.
+constexpr int kL2PrefetchSlots = 40;
 
 struct TcArgs {
   CUtensorMap map13;   // routed W13 as [E * 2I rows, H bytes], box 64 rows x 128 bytes
@@ -63,7 +69,8 @@ struct TcArgs {
   int32_t* ids;
   float* weights;
   __nv_bfloat16* gate_up;
-  uint32_t* err;
+  uint32_t* err;     // device error word
+  uint32_t* sync;    // [2]: CTAs whose GEMM1 loads are all issued; CTAs done reading [0]
   uint32_t* done;    // [E + 1] GEMM1 tiles finished per expert (id E: the shared expert)
   uint32_t* passed;  // [E + 1] CTAs whose GEMM2 work passed the wait
   uint32_t* cnt1;    // [(E + 1) * I/64] contributors arrived per GEMM1 tile (expert id, tile)
@@ -90,11 +97,10 @@ struct TcSmem {
   unsigned long long tokmask[kMaxExperts];
   int16_t rid[kMaxTokens * kMaxTopK];
   int16_t ulist[kMaxExperts];
-  int16_t ctx_route[2][kMaxTokens];  // routes of each B buffer's expert, in token order
-  int ctx_n[2];
+  int16_t ctx_route[3][kMaxTokens];  // routes of each B buffer's expert, in token order; [2]: the fill's next
+  int ctx_n[3];
   int16_t seg_route[kMaxTokens];     // the accumulate warps' copy for the current segment
   int seg_n;
-  int dirty[2];  // B rows >= dirty[b] are zero in every K block of buffer b
   uint32_t tmem_base;
   int U, rmax;
   int flag;
@@ -290,8 +296,9 @@ struct Cursor {
 };
 
 // ---------------------------------------------------------------- B operand fill
-// Routes of expert u (token order) into ctx_route[b] (fill warps).
-__device__ void fill_context(const TcArgs& a, TcSmem& S, int u, int b, int fid) {
+// Routes of expert u (token order) into the fill warps' staging slot ctx_route[2].
+__device__ void fill_context(const TcArgs& a, TcSmem& S, int u, int fid) {
+  constexpr int b = 2;
   if (fid < 32) {
     const int lane = fid;
     if (a.has_shared && u == S.U - 1) {
@@ -326,15 +333,18 @@ __device__ void fill_context(const TcArgs& a, TcSmem& S, int u, int b, int fid) 
 // Phase 2 reads the SwiGLU output: sh likewise; routed q = e4m3(h / sh)
 // ("mega_moe" hidden_block), shared q = e4m3(h * (1/sh)) ("shared_expert" _DownKernel).
 // Row t of K block j sits at j*N*128 + t*128, its 16-byte chunk c at c ^ (t % 8)
-// (the 128-byte swizzle the MMA descriptor names).
-__device__ void fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& ch, int b, int fid) {
-  const int r = S.ctx_n[b];
+// (the 128-byte swizzle the MMA descriptor names). Rows r..N-1 are left as
+// they are: they only feed accumulator columns nobody reads.
+// The scales and the first batch of activations are loaded before waiting
+// for buffer b (chunk ci - 2's accumulators read), hiding their latency.
+// Returns false when the wait gave up.
+__device__ bool fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& ch, int b, int ci, int fid) {
+  const int r = S.ctx_n[2];
   const int N = P.N;
   uint8_t* B = S.B[b];
   const XInfo xi = xinfo(a, S, ch.u);
   // Weight block scales of the chunk's K blocks ([first/second row half][j]
-  // for GEMM1: row blocks T/2 and I/128 + T/2; [0][j] for GEMM2: row block T),
-  // loaded together with the first activations.
+  // for GEMM1: row blocks T/2 and I/128 + T/2; [0][j] for GEMM2: row block T).
   float wsv = 0.0f;
   if (fid < 2 * kMaxKc) {
     const int half = fid / kMaxKc, j = fid % kMaxKc;
@@ -351,9 +361,9 @@ __device__ void fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
   const int items = ch.kc * r * 8;
   const int K = ch.phase == 1 ? a.H : a.I;
   constexpr int IPT = 4;  // items per thread per round: all loads first, then quantise
-  for (int base = 0; base < items; base += kFillThreads * IPT) {
-    float v[IPT][16];
-    int tt[IPT], jj[IPT];
+  float v[IPT][16];
+  int tt[IPT], jj[IPT];
+  auto load_batch = [&](int base) {
 #pragma unroll
     for (int q = 0; q < IPT; ++q) {
       const int w = base + q * kFillThreads + fid;
@@ -363,7 +373,7 @@ __device__ void fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
       if (w < items) {
         tt[q] = p % r;
         jj[q] = p / r;
-        const int route = S.ctx_route[b][tt[q]];
+        const int route = S.ctx_route[2][tt[q]];
         const int col = (ch.kb0 + jj[q]) * 128 + sub * 16;
         if (ch.phase == 1) {
           const int tok = xi.shared ? route - a.M * a.top_k : route / a.top_k;
@@ -391,6 +401,8 @@ __device__ void fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
         for (int k = 0; k < 16; ++k) v[q][k] = 0.0f;
       }
     }
+  };
+  auto store_batch = [&](int base) {
 #pragma unroll
     for (int q = 0; q < IPT; ++q) {
       if (base + q * kFillThreads >= items) break;  // uniform over the fill warps
@@ -423,31 +435,36 @@ __device__ void fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
         if (sub == 0) S.xs[b][t][j] = scale;
       }
     }
-  }
-  // Rows [r, dirty) of the chunk's K blocks may hold an earlier expert's tokens.
-  const int dirty = S.dirty[b];
-  if (dirty > r) {
-    const int zr = dirty - r;
-    for (int w = fid; w < ch.kc * zr * 8; w += kFillThreads) {
-      const int j = w / (zr * 8), rem = w % (zr * 8);
-      const int t = r + rem / 8, c16 = rem % 8;
-      *reinterpret_cast<uint4*>(B + j * N * 128 + t * 128 + c16 * 16) = make_uint4(0u, 0u, 0u, 0u);
+  };
+  load_batch(0);
+  if (ci >= 2) {
+    if (!mbar_wait(&S.mfree[b], ((ci >> 1) - 1) & 1, a.timeout_ns, &S.abort)) {
+      if (!S.abort) tc_error(a, S, kErrRingWait);
     }
+    fill_bar();
+    if (S.abort) return false;
+  }
+  // Buffer b is free: publish the chunk's routes, then quantise.
+  for (int t = fid; t < r; t += kFillThreads) S.ctx_route[b][t] = S.ctx_route[2][t];
+  if (fid == 0) S.ctx_n[b] = r;
+  store_batch(0);
+  for (int base = kFillThreads * IPT; base < items; base += kFillThreads * IPT) {
+    load_batch(base);
+    store_batch(base);
   }
   if (fid < 2 * kMaxKc) S.wsc[b][fid / kMaxKc][fid % kMaxKc] = wsv;
   fence_proxy_async_smem();
   fill_bar();
-  if (fid == 0) {
-    S.dirty[b] = max(dirty, r);
-    mbar_arrive(&S.bfull[b]);
-  }
+  if (fid == 0) mbar_arrive(&S.bfull[b]);
+  return true;
 }
 
 // ---------------------------------------------------------------- epilogue pieces
 // Finish one GEMM1 tile: y of a first-half row (threads 0..63) or a
 // second-half row (64..127) -> SwiGLU of hidden 64T + q -> hbuf, then release
 // the expert counter.
-__device__ void finish_gemm1(const TcArgs& a, TcSmem& S, const Chunk& ch, int b, const float (&y)[kMaxTokens],
+template <int TOK>
+__device__ void finish_gemm1(const TcArgs& a, TcSmem& S, const Chunk& ch, int b, const float (&y)[TOK],
                              int row, int etid) {
   const int r = S.seg_n;
   const XInfo xi = xinfo(a, S, ch.u);
@@ -456,7 +473,7 @@ __device__ void finish_gemm1(const TcArgs& a, TcSmem& S, const Chunk& ch, int b,
   const int q = row & 63;
   const float L = xi.limit;
 #pragma unroll
-  for (int g = 0; g < kTokGroups; ++g) {
+  for (int g = 0; g < TOK / 16; ++g) {
     if (g * 16 < r) {
       if (second) {
 #pragma unroll
@@ -502,7 +519,8 @@ __device__ void finish_gemm1(const TcArgs& a, TcSmem& S, const Chunk& ch, int b,
   }
 }
 
-__device__ void finish_gemm2(const TcArgs& a, TcSmem& S, const Chunk& ch, int b, const float (&y)[kMaxTokens],
+template <int TOK>
+__device__ void finish_gemm2(const TcArgs& a, TcSmem& S, const Chunk& ch, int b, const float (&y)[TOK],
                              int row) {
   const int r = S.seg_n;
   const int m = 128 * ch.T + row;
@@ -512,7 +530,7 @@ __device__ void finish_gemm2(const TcArgs& a, TcSmem& S, const Chunk& ch, int b,
   const int row0 = shared ? a.M * a.top_k : 0;
   const int rows = shared ? a.M : a.M * a.top_k;
 #pragma unroll
-  for (int t = 0; t < kMaxTokens; ++t) {
+  for (int t = 0; t < TOK; ++t) {
     const int o = S.seg_route[t] - row0;
     if (t < r) {
       if (o >= 0 && o < rows)
@@ -527,46 +545,78 @@ __device__ __forceinline__ float* part_slot(const TcArgs& a, int phase, int c, i
   return a.part + ((static_cast<size_t>(phase - 1) * kFp8MaxCtas + c) * 2 + slot) * a.ptok * 128;
 }
 
-// End of a segment: finish the tile directly when this CTA owns all of it,
-// else publish the partial; the last contributor sums all partials in CTA
-// order and finishes the tile.
-__device__ void end_segment(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& ch, int b, float (&y)[kMaxTokens],
+// End of a segment: finish the tile directly when this CTA owns all of it.
+// A split tile is finished by its first contributor cf, which holds the
+// tile's first K blocks at the END of its slice: the others (holding later K
+// blocks at the START of theirs, or whole slices inside the tile) publish
+// their partials and move on without waiting, and cf, usually the last to get
+// there, adds them to its own in CTA order.
+template <int TOK>
+__device__ void end_segment(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& ch, int b, float (&y)[TOK],
                             int row, int etid) {
   const PhasePlan& pp = P.p[ch.phase - 1];
   const int cf = pp.cta_of(ch.t0), cl = pp.cta_of(ch.t0 + pp.nb - 1);
   const int r = S.seg_n;
   if (cf != cl) {
-    float* mine = part_slot(a, ch.phase, P.c, pp.lo >= ch.t0 ? 0 : 1);
+    const int e = xinfo(a, S, ch.u).id;
+    uint32_t* cnt = ch.phase == 1 ? a.cnt1 + static_cast<size_t>(e) * pp.tiles + ch.T
+                                  : a.cnt2 + static_cast<size_t>(e) * pp.tiles + ch.T;
+    if (P.c != cf) {
+      float* mine = part_slot(a, ch.phase, P.c, pp.lo >= ch.t0 ? 0 : 1);
 #pragma unroll
-    for (int t = 0; t < kMaxTokens; ++t)
-      if (t < r) mine[t * 128 + row] = y[t];
-    __threadfence();
-    epi_bar();
+      for (int t = 0; t < TOK; ++t)
+        if (t < r) __stcg(mine + t * 128 + row, y[t]);
+      // The barrier orders every thread's partial before one release.
+      epi_bar();
+      if (etid == 0) red_release_gpu_add(cnt, 1u);
+      return;
+    }
     if (etid == 0) {
-      const int e = xinfo(a, S, ch.u).id;
-      uint32_t* cnt = ch.phase == 1 ? a.cnt1 + static_cast<size_t>(e) * pp.tiles + ch.T
-                                    : a.cnt2 + static_cast<size_t>(e) * pp.tiles + ch.T;
-      const uint32_t old = atomicAdd(cnt, 1u);
-      const bool last = old + 1u == static_cast<uint32_t>(cl - cf + 1);
-      if (last) atomicExch(cnt, 0u);
-      S.flag = last ? 1 : 0;
+      const uint32_t want = static_cast<uint32_t>(cl - cf);
+      const uint64_t t0 = globaltimer_ns();
+      bool ok = true;
+      while (ld_acquire_gpu(cnt) < want) {
+        if (S.abort || globaltimer_ns() - t0 > a.timeout_ns) {
+          ok = false;
+          break;
+        }
+        __nanosleep(32);
+      }
+      if (ok) {
+        atomicExch(cnt, 0u);  // every contributor has arrived: re-arm for the next call
+      } else if (!S.abort) {
+        tc_error(a, S, kErrCrossWait);
+      }
     }
     epi_bar();
-    if (!S.flag) return;
-    __threadfence();
+    if (S.abort) return;
+    // Add the other contributors' partials, four at a time (all loads in
+    // flight), in CTA order after this CTA's own.
+    for (int c0 = cf + 1; c0 <= cl; c0 += 4) {
+      const float* src[4];
 #pragma unroll
-    for (int t = 0; t < kMaxTokens; ++t) y[t] = 0.0f;
-    for (int cc = cf; cc <= cl; ++cc) {
-      const float* src = part_slot(a, ch.phase, cc, pp.lo_of(cc) >= ch.t0 ? 0 : 1);
+      for (int q = 0; q < 4; ++q) {
+        const int cc = min(c0 + q, cl);
+        src[q] = part_slot(a, ch.phase, cc, pp.lo_of(cc) >= ch.t0 ? 0 : 1) + row;
+      }
+      const int nq = min(4, cl - c0 + 1);
 #pragma unroll
-      for (int t = 0; t < kMaxTokens; ++t)
-        if (t < r) y[t] += __ldcg(src + t * 128 + row);
+      for (int t = 0; t < TOK; ++t) {
+        if (t < r) {
+          float v[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) v[q] = __ldcg(src[q] + t * 128);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (q < nq) y[t] += v[q];
+        }
+      }
     }
   }
   if (ch.phase == 1)
-    finish_gemm1(a, S, ch, b, y, row, etid);
+    finish_gemm1<TOK>(a, S, ch, b, y, row, etid);
   else
-    finish_gemm2(a, S, ch, b, y, row);
+    finish_gemm2<TOK>(a, S, ch, b, y, row);
 }
 
 // Wait until every GEMM1 tile of expert u is finished, then count this CTA in;
@@ -605,9 +655,9 @@ __device__ bool wait_hidden(const TcArgs& a, TcSmem& S, const Plan& P, int u, in
 // Scaled sum of one chunk's per-K-block partials: y[t] += D[j][t] *
 // (w_scale[j] * x_scale[t][j]) for this thread's row. Loads LD columns per
 // tcgen05.ld, GROUPS groups of them per K block, KB K blocks per wait.
-template <int LD, int GROUPS, int KB>
+template <int LD, int GROUPS, int KB, int TOK>
 __device__ __forceinline__ void accumulate(uint32_t tbase, int N, int kc, int r, const float (&ws)[kMaxKc],
-                                           const float (&xs)[kMaxTokens][kMaxKc], float (&y)[kMaxTokens]) {
+                                           const float (&xs)[kMaxTokens][kMaxKc], float (&y)[TOK]) {
 #pragma unroll
   for (int j0 = 0; j0 < kMaxKc; j0 += KB) {
     if (j0 < kc) {
@@ -638,6 +688,10 @@ __device__ __forceinline__ void accumulate(uint32_t tbase, int N, int kc, int r,
 }
 
 // ---------------------------------------------------------------- kernel
+// TOK: token capacity of the accumulators (16 when M <= 16, else 64): the
+// per-token loops are unrolled to it, so the small case keeps its code small
+// enough to stay in the instruction caches.
+template <int TOK>
 __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_constant__ TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   TcSmem& S = *reinterpret_cast<TcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -653,7 +707,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
       mbar_init(&S.accfull[b], 1);
       mbar_init(&S.tmemfree[b], 4);
       mbar_init(&S.mfree[b], 4);
-      S.dirty[b] = 0;
     }
     mbar_init(&S.final_bar, 1);
     fence_mbar_init();
@@ -745,11 +798,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
           map = xi.m2;
         }
       };
+      // L2 prefetch of this CTA's GEMM2 slots [from, to) (two boxes each).
+      auto prefetch_gemm2 = [&](int from, int to) {
+        const PhasePlan& p2 = P.p[1];
+        for (int sl = from; sl < to; ++sl) {
+          const int tile = sl / p2.nb;
+          const int u = tile / p2.tiles;
+          const XInfo xi = xinfo(a, S, u);
+          const int ra = xi.row_e * a.H + 128 * (tile - u * p2.tiles);
+          const int xk = (sl - tile * p2.nb) * 128;
+          tma_prefetch_l2_2d(xi.m2, xk, ra);
+          tma_prefetch_l2_2d(xi.m2, xk, ra + 64);
+        }
+      };
       Cursor cur{P.p[0].lo, 1};
       Chunk ch;
       int k = 0;
-      bool ok = true;
+      bool ok = true, issued1 = false, prefetched = false;
       while (ok && cur.next(P, ch)) {
+        if (ch.phase == 2 && !issued1) {
+          issued1 = true;  // every GEMM1 load of this CTA is issued
+          red_release_gpu_add(a.sync, 1u);
+        }
         int ra, rb;
         const void* map;
         coords(ch, ra, rb, map);
@@ -759,6 +829,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
             const uint32_t parity = ((k / kTcStages) - 1) & 1;
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait(&S.empty[s], parity)) {
+              // Blocked on the ring in GEMM2: once the whole grid's GEMM1
+              // loads are out, stream the next GEMM2 slots into L2.
+              if (ch.phase == 2 && !prefetched && ld_acquire_gpu(a.sync) >= gridDim.x) {
+                prefetched = true;
+                const int sl = ch.t0 + ch.kb0 + j;
+                prefetch_gemm2(sl, min(P.p[1].hi, sl + kL2PrefetchSlots));
+              }
               if (S.abort || globaltimer_ns() - t0 > a.timeout_ns) {
                 ok = false;
                 break;
@@ -774,6 +851,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
           tma_load_2d(S.A[s], map, xk, ra, &S.full[s], pol);
           tma_load_2d(S.A[s] + kAStageBytes / 2, map, xk, rb, &S.full[s], pol);
         }
+      }
+      if (!issued1) red_release_gpu_add(a.sync, 1u);
+      // The last CTA past this point re-arms both sync counters (no CTA reads
+      // sync[0] after its own sync[1] increment).
+      if (atomicAdd(a.sync + 1, 1u) + 1u == gridDim.x) {
+        atomicExch(a.sync, 0u);
+        atomicExch(a.sync + 1, 0u);
       }
       // Every load issued must land before the CTA may exit.
       for (int kk = max(0, k - kTcStages); kk < k; ++kk)
@@ -831,9 +915,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
     Chunk ch;
     int ci = 0;
     bool seg_first = true;
-    float y[kMaxTokens];
+    float y[TOK];
 #pragma unroll
-    for (int t = 0; t < kMaxTokens; ++t) y[t] = 0.0f;
+    for (int t = 0; t < TOK; ++t) y[t] = 0.0f;
     while (cur.next(P, ch)) {
       const int b = ci & 1;
       if (!mbar_wait(&S.accfull[b], (ci >> 1) & 1, a.timeout_ns, &S.abort)) {
@@ -851,10 +935,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
         accumulate<1, 1, 16>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
       else if (r <= 4)
         accumulate<4, 1, 8>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
-      else if (r <= 16)
+      else if (TOK == 16 || r <= 16)
         accumulate<16, 1, 2>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
-      else
-        accumulate<16, kTokGroups, 1>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
+      else if constexpr (TOK > 16)
+        accumulate<16, TOK / 16, 1>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
       tc_fence_before();
       if (seg_first) {
         // First chunk of a segment: keep its routes for the segment's end.
@@ -870,9 +954,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
       }
       seg_first = ch.last_of_seg;
       if (ch.last_of_seg) {
-        end_segment(a, S, P, ch, b, y, row, etid);
+        end_segment<TOK>(a, S, P, ch, b, y, row, etid);
 #pragma unroll
-        for (int t = 0; t < kMaxTokens; ++t) y[t] = 0.0f;
+        for (int t = 0; t < TOK; ++t) y[t] = 0.0f;
       }
       ++ci;
     }
@@ -886,20 +970,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
     int ci = 0, ctx_u = -1, ctx_phase = 0;
     while (cur.next(P, ch)) {
       const int b = ci & 1;
-      if (ci >= 2) {
-        if (!mbar_wait(&S.mfree[b], ((ci >> 1) - 1) & 1, a.timeout_ns, &S.abort)) {
-          if (!S.abort) tc_error(a, S, kErrRingWait);
-        }
-        fill_bar();
-        if (S.abort) break;
-      }
-      fill_context(a, S, ch.u, b, fid);
+      if (ch.u != ctx_u) fill_context(a, S, ch.u, fid);
       if (ch.phase == 2 && (ch.u != ctx_u || ctx_phase != 2)) {
         if (!wait_hidden(a, S, P, ch.u, fid)) break;
       }
       ctx_u = ch.u;
       ctx_phase = ch.phase;
-      fill_b(a, S, P, ch, b, fid);
+      if (!fill_b(a, S, P, ch, b, ci, fid)) break;
       ++ci;
     }
   }
@@ -982,6 +1059,7 @@ static int launch_tc(TcArgs& a, const uint8_t* w13, const uint8_t* w2, const uin
   if (workspace == nullptr || workspace_bytes < w.bytes)
     return set_last_error(FME_EWORKSPACE, "workspace of %zu bytes needed, %zu given", w.bytes, workspace_bytes);
   a.err = w.err;
+  a.sync = w.err + 1;
   a.done = w.done;
   a.passed = w.passed;
   a.cnt1 = w.cnt1;
@@ -1000,7 +1078,9 @@ static int launch_tc(TcArgs& a, const uint8_t* w13, const uint8_t* w2, const uin
   if (cudaGetDevice(&dev) != cudaSuccess) return set_last_error(FME_ECUDA, "cudaGetDevice failed");
   const int sms = device_sm_count(dev);
   if (sms <= 0) return set_last_error(FME_ECUDA, "cannot query the SM count");
-  if (!ensure_smem_attr(dev, reinterpret_cast<const void*>(fp8_moe_tc_kernel), kTcSmemBytes)) return FME_ECUDA;
+  // M <= 16 tokens: the 16-token variant (every expert then has <= 16 rows).
+  auto kernel = a.M <= 16 ? fp8_moe_tc_kernel<16> : fp8_moe_tc_kernel<kMaxTokens>;
+  if (!ensure_smem_attr(dev, reinterpret_cast<const void*>(kernel), kTcSmemBytes)) return FME_ECUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sms < kFp8MaxCtas ? sms : kFp8MaxCtas);
   cfg.blockDim = dim3(kTcThreads);
@@ -1011,7 +1091,7 @@ static int launch_tc(TcArgs& a, const uint8_t* w13, const uint8_t* w2, const uin
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t err = cudaLaunchKernelEx(&cfg, fp8_moe_tc_kernel, a);
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, a);
   if (err != cudaSuccess) return set_last_error(FME_ECUDA, "fp8 kernel launch: %s", cudaGetErrorString(err));
   return FME_OK;
 }
