@@ -91,7 +91,7 @@ struct TcSmem {
   uint8_t B[2][kBBufBytes];
   float xs[2][kMaxTokens][kMaxKc];  // activation block scales per B buffer
   float wsc[2][2][kMaxKc];          // weight block scales per B buffer: [row half][K block]
-  float ysm[16][64];                // SwiGLU exchange (16 tokens x 64 rows)
+  float ysm[16][128];               // GEMM1 epilogue exchange (16 tokens x 128 tile rows)
   uint64_t full[kTcStages], empty[kTcStages];
   uint64_t bfull[2], accfull[2], tmemfree[2], mfree[2], final_bar;
   unsigned long long tokmask[kMaxExperts];
@@ -360,7 +360,7 @@ __device__ bool fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
   }
   const int items = ch.kc * r * 8;
   const int K = ch.phase == 1 ? a.H : a.I;
-  constexpr int IPT = 4;  // items per thread per round: all loads first, then quantise
+  constexpr int IPT = 2;  // items per thread per round: all loads first, then quantise
   float v[IPT][16];
   int tt[IPT], jj[IPT];
   auto load_batch = [&](int base) {
@@ -462,56 +462,56 @@ __device__ bool fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
 // ---------------------------------------------------------------- epilogue pieces
 // Finish one GEMM1 tile: y of a first-half row (threads 0..63) or a
 // second-half row (64..127) -> SwiGLU of hidden 64T + q -> hbuf, then release
-// the expert counter.
+// the expert counter. Tokens go 16 at a time through shared memory, and the
+// SwiGLU loop is not unrolled: this code runs once per tile, and keeping it
+// small keeps it in the instruction cache.
 template <int TOK>
 __device__ void finish_gemm1(const TcArgs& a, TcSmem& S, const Chunk& ch, int b, const float (&y)[TOK],
                              int row, int etid) {
   const int r = S.seg_n;
   const XInfo xi = xinfo(a, S, ch.u);
   const bool shared = xi.shared;
-  const bool second = row >= 64;
   const int q = row & 63;
   const float L = xi.limit;
+  for (int g = 0; g * 16 < r; ++g) {
 #pragma unroll
-  for (int g = 0; g < TOK / 16; ++g) {
-    if (g * 16 < r) {
-      if (second) {
+    for (int gg = 0; gg < TOK / 16; ++gg) {
+      if (gg == g) {
 #pragma unroll
-        for (int t = 0; t < 16; ++t) S.ysm[t][q] = y[g * 16 + t];
+        for (int t = 0; t < 16; ++t) S.ysm[t][row] = y[gg * 16 + t];
       }
-      epi_bar();
-      if (!second) {
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          if (g * 16 + t < r) {
-            const int route = S.seg_route[g * 16 + t];
-            const float first = y[g * 16 + t], sec = S.ysm[t][q];
-            float h;
-            if (!shared) {
-              // W31: up rows first, then gate rows ("mega_moe" module docstring).
-              const float gate = fminf(sec, L);
-              const float up = fmaxf(fminf(first, L), -L);
-              h = __fmul_rn(__fdiv_rn(gate, __fadd_rn(1.0f, expf(-gate))), up);
-            } else {
-              // Shared gate_up: gate rows first; BF16 gate_up and BF16 h.
-              const __nv_bfloat16 gb = __float2bfloat16_rn(first);
-              const __nv_bfloat16 ub = __float2bfloat16_rn(sec);
-              if (a.gate_up != nullptr) {
-                const size_t tok = static_cast<size_t>(route - a.M * a.top_k);
-                a.gate_up[tok * 2 * a.I + 64 * ch.T + q] = gb;
-                a.gate_up[tok * 2 * a.I + a.I + 64 * ch.T + q] = ub;
-              }
-              const float gate = fminf(__bfloat162float(gb), L);
-              const float up = fmaxf(fminf(__bfloat162float(ub), L), -L);
-              const float silu = __fdiv_rn(gate, __fadd_rn(1.0f, expf(-gate)));
-              h = __bfloat162float(__float2bfloat16_rn(__fmul_rn(silu, up)));
-            }
-            a.hbuf[static_cast<size_t>(route) * a.I + 64 * ch.T + q] = h;
-          }
-        }
-      }
-      epi_bar();
     }
+    epi_bar();
+    if (row < 64) {
+      const int n = min(16, r - g * 16);
+#pragma unroll 1
+      for (int t = 0; t < n; ++t) {
+        const int route = S.seg_route[g * 16 + t];
+        const float first = S.ysm[t][q], sec = S.ysm[t][q + 64];
+        float h;
+        if (!shared) {
+          // W31: up rows first, then gate rows ("mega_moe" module docstring).
+          const float gate = fminf(sec, L);
+          const float up = fmaxf(fminf(first, L), -L);
+          h = __fmul_rn(__fdiv_rn(gate, __fadd_rn(1.0f, expf(-gate))), up);
+        } else {
+          // Shared gate_up: gate rows first; BF16 gate_up and BF16 h.
+          const __nv_bfloat16 gb = __float2bfloat16_rn(first);
+          const __nv_bfloat16 ub = __float2bfloat16_rn(sec);
+          if (a.gate_up != nullptr) {
+            const size_t tok = static_cast<size_t>(route - a.M * a.top_k);
+            a.gate_up[tok * 2 * a.I + 64 * ch.T + q] = gb;
+            a.gate_up[tok * 2 * a.I + a.I + 64 * ch.T + q] = ub;
+          }
+          const float gate = fminf(__bfloat162float(gb), L);
+          const float up = fmaxf(fminf(__bfloat162float(ub), L), -L);
+          const float silu = __fdiv_rn(gate, __fadd_rn(1.0f, expf(-gate)));
+          h = __bfloat162float(__float2bfloat16_rn(__fmul_rn(silu, up)));
+        }
+        a.hbuf[static_cast<size_t>(route) * a.I + 64 * ch.T + q] = h;
+      }
+    }
+    epi_bar();
   }
   if (etid == 0) {
     __threadfence();
