@@ -513,10 +513,9 @@ __device__ void finish_gemm1(const TcArgs& a, TcSmem& S, const Chunk& ch, int b,
     }
     epi_bar();
   }
-  if (etid == 0) {
-    __threadfence();
-    red_release_gpu_add(a.done + xi.id, 1u);
-  }
+  // The barrier above orders every thread's hidden values before this
+  // release (the same pattern publishes the partials).
+  if (etid == 0) red_release_gpu_add(a.done + xi.id, 1u);
 }
 
 template <int TOK>
