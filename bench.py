@@ -302,7 +302,7 @@ def gpu_arm(args, rank, world, local_rank):
                    "per_m": per_m, "unique_experts_per_step": round(float(uniq.sum() / args.steps), 2)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "fp8_moe_kernel", "bytes_per_launch": "unique experts x 44,050,944 B"},
+                     "kernel": "fp8_moe_tc_kernel", "bytes_per_launch": "unique experts x 44,050,944 B"},
         "clocks": clocks.summary(),
         "e2e": e2e,
         "gpu_launches": args.steps * len(MS),
