@@ -18,10 +18,10 @@
 
 namespace {
 
-// Largest workspace the variant can serve: 8 MiB. That covers, e.g., the
-// DeepSeek-V3 shape (H = 7168, I = 2048, 256 experts, top_k 8) up to M = 16
+// Largest workspace the variant can serve: 16 MiB. That covers, e.g., the
+// DeepSeek-V3 shape (H = 7168, I = 2048, 256 experts, top_k 8) up to M = 32
 // tokens. Larger requests are rejected with FME_EUNSUPPORTED.
-constexpr size_t kScratchBytes = size_t(8) << 20;
+constexpr size_t kScratchBytes = size_t(16) << 20;
 
 // The scratch itself. In host code `g_scratch` only names a host-side
 // stand-in, never the device memory: host code must take the device address
@@ -61,7 +61,7 @@ extern "C" int fme_moe_routed_fp8_noalloc(const void* x, const void* logits, int
     return fme::set_last_error(FME_EINVAL, "bad sizes M=%d H=%d I=%d E=%d top_k=%d", M, H, I, E, top_k);
   if (need > kScratchBytes)
     return fme::set_last_error(FME_EUNSUPPORTED,
-                               "needs %zu bytes of scratch; the no-allocation variant holds %zu (8 MiB): "
+                               "needs %zu bytes of scratch; the no-allocation variant holds %zu (16 MiB): "
                                "use fme_moe_routed_fp8 with a caller workspace",
                                need, kScratchBytes);
   void* scratch = scratch_address(dev);

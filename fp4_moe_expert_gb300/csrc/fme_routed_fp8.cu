@@ -44,13 +44,15 @@ constexpr int kBBufBytes = 256 * 128;    // K blocks x N token rows x 128 bytes 
 constexpr int kTmemCols = 512;
 constexpr int kTmemBuf = 256;            // two accumulator buffers
 constexpr int kMaxKc = 16;
-// GEMM2 K blocks per CTA prefetched into L2 once every CTA has issued all its
-// GEMM1 loads. The GEMM1 -> GEMM2 hand-over of an expert (its last tiles
-// finishing, the hidden rows being re-quantised) otherwise leaves HBM idle;
-// waiting for the whole grid's GEMM1 loads first keeps the prefetch from
-// delaying any GEMM1 stream. 40 slots = 640 KB per CTA, about 97 MB over
-// 152 CTAs, within the 129 MB L2.
-constexpr int kL2PrefetchSlots = 40;
+// Waves: the unit list is cut into W consecutive groups; every CTA takes a
+// share of every wave and runs GEMM1 of wave w + 1 before GEMM2 of wave w, so
+// one wave's GEMM1 -> GEMM2 hand-over (last tiles finishing, hidden rows
+// re-quantised) overlaps the next wave's weight stream, and each CTA's work
+// mixes experts hit by different token counts. Every wave adds split tiles,
+// each with a partial round trip. Measured on the DeepSeek-V3 shape: three
+// waves pay off at 5-8 tokens (M = 8: 414 -> 389 us); at 1-4 tokens two
+// waves were slower than one.
+__host__ __device__ constexpr int max_waves(int ptok) { return ptok > 4 && ptok <= 8 ? 3 : 1; }
 
 struct TcArgs {
   CUtensorMap map13;   // routed W13 as [E * 2I rows, H bytes], box 64 rows x 128 bytes
@@ -70,7 +72,6 @@ struct TcArgs {
   float* weights;
   __nv_bfloat16* gate_up;
   uint32_t* err;     // device error word
-  uint32_t* sync;    // [2]: CTAs whose GEMM1 loads are all issued; CTAs done reading [0]
   uint32_t* done;    // [E + 1] GEMM1 tiles finished per expert (id E: the shared expert)
   uint32_t* passed;  // [E + 1] CTAs whose GEMM2 work passed the wait
   uint32_t* cnt1;    // [(E + 1) * I/64] contributors arrived per GEMM1 tile (expert id, tile)
@@ -228,12 +229,14 @@ __device__ void route_token(const TcArgs& a, TcSmem& S, int t, int lane, bool wr
 }
 
 // ---------------------------------------------------------------- work plan
-// Each phase's slots (at most 1024 experts x 128 tiles x 64 K blocks, so
-// 32-bit arithmetic suffices) are split over Ge = min(G, n) CTAs: CTA c < Ge
-// owns [n*c/Ge, n*(c+1)/Ge), never empty; CTAs c >= Ge own nothing.
+// The units are cut into W waves of consecutive units. The slots of one
+// (wave, phase) -- units x tiles x K blocks, at most 1024 x 128 x 64, so 32-bit
+// arithmetic suffices -- are split over Ge = min(G, n) CTAs: CTA c < Ge owns
+// [n*c/Ge, n*(c+1)/Ge), never empty; CTAs c >= Ge own nothing.
 struct PhasePlan {
   int n, lo, hi;
   int Ge, tiles, nb;
+  int w, u0;  // wave and its first unit
   __device__ int lo_of(int c) const {
     return c >= Ge ? n : static_cast<int>(static_cast<long long>(n) * c / Ge);
   }
@@ -244,53 +247,78 @@ struct PhasePlan {
 };
 
 struct Plan {
-  int U, N, kcmax, c;
-  PhasePlan p[2];
+  int U, N, kcmax, c, G, W;
+  int tiles[2], nb[2];  // per unit: GEMM1 64-row tiles x H/128 K blocks; GEMM2 128-row tiles x I/128
+  __device__ int wave_lo(int w) const { return static_cast<int>(static_cast<long long>(U) * w / W); }
+  // Stage q of 2W: GEMM1 of wave 0, then GEMM1(w + 1) / GEMM2(w) pairs, then
+  // the last GEMM2.
+  __device__ void stage(int q, int& w, int& phase) const {
+    if (q == 0) {
+      w = 0;
+      phase = 1;
+    } else if (q < 2 * W - 1) {
+      w = (q & 1) ? (q + 1) / 2 : q / 2 - 1;
+      phase = (q & 1) ? 1 : 2;
+    } else {
+      w = W - 1;
+      phase = 2;
+    }
+  }
+  __device__ PhasePlan plan(int w, int phase) const {
+    PhasePlan pp;
+    const int u0 = wave_lo(w), u1 = wave_lo(w + 1);
+    const int t = tiles[phase - 1], nbp = nb[phase - 1];
+    pp.n = (u1 - u0) * t * nbp;
+    pp.tiles = t;
+    pp.nb = nbp;
+    pp.w = w;
+    pp.u0 = u0;
+    pp.Ge = min(G, pp.n);
+    if (c >= pp.Ge) {
+      pp.lo = pp.hi = pp.n;
+    } else {
+      pp.lo = pp.lo_of(c);
+      pp.hi = pp.lo_of(c + 1);
+    }
+    return pp;
+  }
 };
-
-__device__ void make_phase(PhasePlan& pp, int n, int tiles, int nb, int G, int c) {
-  pp.n = n;
-  pp.tiles = tiles;
-  pp.nb = nb;
-  pp.Ge = min(G, n);
-  pp.lo = pp.lo_of(c);
-  pp.hi = pp.lo_of(c + 1 > pp.Ge ? pp.Ge : c + 1);
-  if (c >= pp.Ge) pp.lo = pp.hi = n;
-}
 
 struct Chunk {
   int phase, u, T, kb0, kc;
-  int tile, t0;  // global tile index and its first slot
+  int t0;  // first slot of the tile within its (wave, phase)
   bool last_of_seg;
+  PhasePlan pp;
 };
 
-// Walks this CTA's slots of both phases in chunks of at most kcmax K blocks
+// Walks this CTA's slots stage by stage in chunks of at most kcmax K blocks
 // that never cross a tile.
 struct Cursor {
-  int pos;
-  int phase;
+  int q = -1, pos = 0, phase = 1;
+  PhasePlan pp;
   __device__ bool next(const Plan& P, Chunk& ch) {
     while (true) {
-      const PhasePlan& pp = P.p[phase - 1];
-      if (pos < pp.lo) pos = pp.lo;
-      if (pos < pp.hi) {
+      if (q >= 0 && pos < pp.hi) {
         const int tile = pos / pp.nb;
         const int t0 = tile * pp.nb;
         const int seg1 = min(pp.hi, t0 + pp.nb);
+        const int uw = tile / pp.tiles;
         ch.phase = phase;
-        ch.u = tile / pp.tiles;
-        ch.T = tile - ch.u * pp.tiles;
-        ch.tile = tile;
+        ch.u = pp.u0 + uw;
+        ch.T = tile - uw * pp.tiles;
         ch.t0 = t0;
         ch.kb0 = pos - t0;
         ch.kc = min(P.kcmax, seg1 - pos);
         ch.last_of_seg = pos + ch.kc == seg1;
+        ch.pp = pp;
         pos += ch.kc;
         return true;
       }
-      if (phase == 2) return false;
-      phase = 2;
-      pos = P.p[1].lo;
+      if (++q >= 2 * P.W) return false;
+      int w;
+      P.stage(q, w, phase);
+      pp = P.plan(w, phase);
+      pos = pp.lo;
     }
   }
 };
@@ -361,9 +389,9 @@ __device__ bool fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
   const int items = ch.kc * r * 8;
   const int K = ch.phase == 1 ? a.H : a.I;
   constexpr int IPT = 2;  // items per thread per round: all loads first, then quantise
-  float v[IPT][16];
-  int tt[IPT], jj[IPT];
-  auto load_batch = [&](int base) {
+  float v[IPT][16], vn[IPT][16];
+  int tt[IPT], jj[IPT], ttn[IPT], jjn[IPT];
+  auto load_batch = [&](float (&v)[IPT][16], int (&tt)[IPT], int (&jj)[IPT], int base) {
 #pragma unroll
     for (int q = 0; q < IPT; ++q) {
       const int w = base + q * kFillThreads + fid;
@@ -402,7 +430,7 @@ __device__ bool fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
       }
     }
   };
-  auto store_batch = [&](int base) {
+  auto store_batch = [&](int base) {  // quantises v (tt, jj) of the round at `base`
 #pragma unroll
     for (int q = 0; q < IPT; ++q) {
       if (base + q * kFillThreads >= items) break;  // uniform over the fill warps
@@ -436,7 +464,7 @@ __device__ bool fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
       }
     }
   };
-  load_batch(0);
+  load_batch(v, tt, jj, 0);
   if (ci >= 2) {
     if (!mbar_wait(&S.mfree[b], ((ci >> 1) - 1) & 1, a.timeout_ns, &S.abort)) {
       if (!S.abort) tc_error(a, S, kErrRingWait);
@@ -447,10 +475,21 @@ __device__ bool fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
   // Buffer b is free: publish the chunk's routes, then quantise.
   for (int t = fid; t < r; t += kFillThreads) S.ctx_route[b][t] = S.ctx_route[2][t];
   if (fid == 0) S.ctx_n[b] = r;
-  store_batch(0);
-  for (int base = kFillThreads * IPT; base < items; base += kFillThreads * IPT) {
-    load_batch(base);
+  // Rounds of IPT items per thread; the next round's loads are in flight
+  // while this round is quantised.
+  for (int base = 0; base < items; base += kFillThreads * IPT) {
+    const bool more = base + kFillThreads * IPT < items;  // uniform over the fill warps
+    if (more) load_batch(vn, ttn, jjn, base + kFillThreads * IPT);
     store_batch(base);
+    if (more) {
+#pragma unroll
+      for (int q = 0; q < IPT; ++q) {
+        tt[q] = ttn[q];
+        jj[q] = jjn[q];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[q][k] = vn[q][k];
+      }
+    }
   }
   if (fid < 2 * kMaxKc) S.wsc[b][fid / kMaxKc][fid % kMaxKc] = wsv;
   fence_proxy_async_smem();
@@ -540,8 +579,8 @@ __device__ void finish_gemm2(const TcArgs& a, TcSmem& S, const Chunk& ch, int b,
   }
 }
 
-__device__ __forceinline__ float* part_slot(const TcArgs& a, int phase, int c, int slot) {
-  return a.part + ((static_cast<size_t>(phase - 1) * kFp8MaxCtas + c) * 2 + slot) * a.ptok * 128;
+__device__ __forceinline__ float* part_slot(const TcArgs& a, int w, int phase, int c, int slot) {
+  return a.part + (((static_cast<size_t>(w) * 2 + phase - 1) * kFp8MaxCtas + c) * 2 + slot) * a.ptok * 128;
 }
 
 // End of a segment: finish the tile directly when this CTA owns all of it.
@@ -553,7 +592,7 @@ __device__ __forceinline__ float* part_slot(const TcArgs& a, int phase, int c, i
 template <int TOK>
 __device__ void end_segment(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& ch, int b, float (&y)[TOK],
                             int row, int etid) {
-  const PhasePlan& pp = P.p[ch.phase - 1];
+  const PhasePlan& pp = ch.pp;
   const int cf = pp.cta_of(ch.t0), cl = pp.cta_of(ch.t0 + pp.nb - 1);
   const int r = S.seg_n;
   if (cf != cl) {
@@ -561,7 +600,7 @@ __device__ void end_segment(const TcArgs& a, TcSmem& S, const Plan& P, const Chu
     uint32_t* cnt = ch.phase == 1 ? a.cnt1 + static_cast<size_t>(e) * pp.tiles + ch.T
                                   : a.cnt2 + static_cast<size_t>(e) * pp.tiles + ch.T;
     if (P.c != cf) {
-      float* mine = part_slot(a, ch.phase, P.c, pp.lo >= ch.t0 ? 0 : 1);
+      float* mine = part_slot(a, pp.w, ch.phase, P.c, pp.lo >= ch.t0 ? 0 : 1);
 #pragma unroll
       for (int t = 0; t < TOK; ++t)
         if (t < r) __stcg(mine + t * 128 + row, y[t]);
@@ -596,7 +635,7 @@ __device__ void end_segment(const TcArgs& a, TcSmem& S, const Plan& P, const Chu
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int cc = min(c0 + q, cl);
-        src[q] = part_slot(a, ch.phase, cc, pp.lo_of(cc) >= ch.t0 ? 0 : 1) + row;
+        src[q] = part_slot(a, pp.w, ch.phase, cc, pp.lo_of(cc) >= ch.t0 ? 0 : 1) + row;
       }
       const int nq = min(4, cl - c0 + 1);
 #pragma unroll
@@ -620,10 +659,11 @@ __device__ void end_segment(const TcArgs& a, TcSmem& S, const Plan& P, const Chu
 
 // Wait until every GEMM1 tile of expert u is finished, then count this CTA in;
 // the last CTA with GEMM2 work on it re-arms the counters for the next call.
-__device__ bool wait_hidden(const TcArgs& a, TcSmem& S, const Plan& P, int u, int fid) {
+__device__ bool wait_hidden(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& ch, int fid) {
+  const int u = ch.u;
   if (fid == 0) {
     const int e = xinfo(a, S, u).id;
-    const uint32_t target = static_cast<uint32_t>(P.p[0].tiles);
+    const uint32_t target = static_cast<uint32_t>(P.tiles[0]);
     const uint64_t t0 = globaltimer_ns();
     bool ok = true;
     while (ld_acquire_gpu(a.done + e) < target) {
@@ -636,8 +676,8 @@ __device__ bool wait_hidden(const TcArgs& a, TcSmem& S, const Plan& P, int u, in
     if (!ok) {
       if (!S.abort) tc_error(a, S, kErrCrossWait);
     } else {
-      const PhasePlan& p2 = P.p[1];
-      const int s0 = u * p2.tiles * p2.nb;
+      const PhasePlan& p2 = ch.pp;
+      const int s0 = (u - p2.u0) * p2.tiles * p2.nb;
       const int s1 = s0 + p2.tiles * p2.nb - 1;
       const uint32_t ctas = static_cast<uint32_t>(p2.cta_of(s1) - p2.cta_of(s0) + 1);
       const uint32_t old = atomicAdd(a.passed + e, 1u);
@@ -775,8 +815,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
   P.N = 16 * ((S.rmax + 15) / 16);
   P.kcmax = min(kMaxKc, kTmemBuf / P.N);
   P.c = blockIdx.x;
-  make_phase(P.p[0], P.U * (a.I / 64) * (a.H / 128), a.I / 64, a.H / 128, gridDim.x, blockIdx.x);
-  make_phase(P.p[1], P.U * (a.H / 128) * (a.I / 128), a.H / 128, a.I / 128, gridDim.x, blockIdx.x);
+  P.G = gridDim.x;
+  P.W = min(P.U, max_waves(a.ptok));
+  P.tiles[0] = a.I / 64;
+  P.nb[0] = a.H / 128;
+  P.tiles[1] = a.H / 128;
+  P.nb[1] = a.I / 128;
   const uint32_t tmem = S.tmem_base;
 
   if (warp == 0) {
@@ -797,28 +841,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
           map = xi.m2;
         }
       };
-      // L2 prefetch of this CTA's GEMM2 slots [from, to) (two boxes each).
-      auto prefetch_gemm2 = [&](int from, int to) {
-        const PhasePlan& p2 = P.p[1];
-        for (int sl = from; sl < to; ++sl) {
-          const int tile = sl / p2.nb;
-          const int u = tile / p2.tiles;
-          const XInfo xi = xinfo(a, S, u);
-          const int ra = xi.row_e * a.H + 128 * (tile - u * p2.tiles);
-          const int xk = (sl - tile * p2.nb) * 128;
-          tma_prefetch_l2_2d(xi.m2, xk, ra);
-          tma_prefetch_l2_2d(xi.m2, xk, ra + 64);
-        }
-      };
-      Cursor cur{P.p[0].lo, 1};
+      Cursor cur;
       Chunk ch;
       int k = 0;
-      bool ok = true, issued1 = false, prefetched = false;
+      bool ok = true;
       while (ok && cur.next(P, ch)) {
-        if (ch.phase == 2 && !issued1) {
-          issued1 = true;  // every GEMM1 load of this CTA is issued
-          red_release_gpu_add(a.sync, 1u);
-        }
         int ra, rb;
         const void* map;
         coords(ch, ra, rb, map);
@@ -828,13 +855,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
             const uint32_t parity = ((k / kTcStages) - 1) & 1;
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait(&S.empty[s], parity)) {
-              // Blocked on the ring in GEMM2: once the whole grid's GEMM1
-              // loads are out, stream the next GEMM2 slots into L2.
-              if (ch.phase == 2 && !prefetched && ld_acquire_gpu(a.sync) >= gridDim.x) {
-                prefetched = true;
-                const int sl = ch.t0 + ch.kb0 + j;
-                prefetch_gemm2(sl, min(P.p[1].hi, sl + kL2PrefetchSlots));
-              }
               if (S.abort || globaltimer_ns() - t0 > a.timeout_ns) {
                 ok = false;
                 break;
@@ -851,13 +871,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
           tma_load_2d(S.A[s] + kAStageBytes / 2, map, xk, rb, &S.full[s], pol);
         }
       }
-      if (!issued1) red_release_gpu_add(a.sync, 1u);
-      // The last CTA past this point re-arms both sync counters (no CTA reads
-      // sync[0] after its own sync[1] increment).
-      if (atomicAdd(a.sync + 1, 1u) + 1u == gridDim.x) {
-        atomicExch(a.sync, 0u);
-        atomicExch(a.sync + 1, 0u);
-      }
       // Every load issued must land before the CTA may exit.
       for (int kk = max(0, k - kTcStages); kk < k; ++kk)
         if (!mbar_wait(&S.full[kk % kTcStages], (kk / kTcStages) & 1, a.timeout_ns, nullptr))
@@ -867,7 +880,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = f8_idesc(128, P.N);
-      Cursor cur{P.p[0].lo, 1};
+      Cursor cur;
       Chunk ch;
       int k = 0, ci = 0;
       bool ok = true;
@@ -910,7 +923,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
     const int quad = warp & 3;
     const int row = quad * 32 + lane;  // TMEM lane = tile row
     const int half = row < 64 ? 0 : 1;
-    Cursor cur{P.p[0].lo, 1};
+    Cursor cur;
     Chunk ch;
     int ci = 0;
     bool seg_first = true;
@@ -964,14 +977,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
     // Quantise each chunk's activations into the B operand and stage its
     // scales, up to two chunks ahead of the accumulate warps.
     const int fid = tid - 192;
-    Cursor cur{P.p[0].lo, 1};
+    Cursor cur;
     Chunk ch;
     int ci = 0, ctx_u = -1, ctx_phase = 0;
     while (cur.next(P, ch)) {
       const int b = ci & 1;
       if (ch.u != ctx_u) fill_context(a, S, ch.u, fid);
       if (ch.phase == 2 && (ch.u != ctx_u || ctx_phase != 2)) {
-        if (!wait_hidden(a, S, P, ch.u, fid)) break;
+        if (!wait_hidden(a, S, P, ch, fid)) break;
       }
       ctx_u = ch.u;
       ctx_phase = ch.phase;
@@ -1046,7 +1059,7 @@ static TcWorkspace tc_layout(void* base, int M, int routes, int H, int I, int E)
   off += align256(4 * static_cast<size_t>(routes) * I);
   w.ptok = M < kMaxTokens ? M : kMaxTokens;
   w.part = reinterpret_cast<float*>(p + off);
-  off += align256(4 * static_cast<size_t>(2) * kFp8MaxCtas * 2 * w.ptok * 128);
+  off += align256(4 * static_cast<size_t>(max_waves(w.ptok)) * 2 * kFp8MaxCtas * 2 * w.ptok * 128);
   w.bytes = off;
   return w;
 }
@@ -1058,7 +1071,6 @@ static int launch_tc(TcArgs& a, const uint8_t* w13, const uint8_t* w2, const uin
   if (workspace == nullptr || workspace_bytes < w.bytes)
     return set_last_error(FME_EWORKSPACE, "workspace of %zu bytes needed, %zu given", w.bytes, workspace_bytes);
   a.err = w.err;
-  a.sync = w.err + 1;
   a.done = w.done;
   a.passed = w.passed;
   a.cnt1 = w.cnt1;
