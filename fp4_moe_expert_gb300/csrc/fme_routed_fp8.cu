@@ -230,26 +230,29 @@ __device__ void route_token(const TcArgs& a, TcSmem& S, int t, int lane, bool wr
 
 // ---------------------------------------------------------------- work plan
 // The units are cut into W waves of consecutive units. The slots of one
-// (wave, phase) -- units x tiles x K blocks, at most 1024 x 128 x 64, so 32-bit
-// arithmetic suffices -- are split over Ge = min(G, n) CTAs: CTA c < Ge owns
-// [n*c/Ge, n*(c+1)/Ge), never empty; CTAs c >= Ge own nothing.
+// (wave, phase) -- units x tiles x K blocks, at most 1025 x 128 x 64 = 8.4M --
+// are split over Ge = min(G, n) CTAs: CTA c < Ge owns [n*c/Ge, n*(c+1)/Ge),
+// never empty; CTAs c >= Ge own nothing. The products stay below 8.4M x 161
+// < 2^32, so unsigned 32-bit arithmetic is exact.
 struct PhasePlan {
   int n, lo, hi;
   int Ge, tiles, nb;
   int w, u0;  // wave and its first unit
   __device__ int lo_of(int c) const {
-    return c >= Ge ? n : static_cast<int>(static_cast<long long>(n) * c / Ge);
+    return c >= Ge ? n : static_cast<int>(static_cast<uint32_t>(n) * static_cast<uint32_t>(c) /
+                                          static_cast<uint32_t>(Ge));
   }
   // The CTA whose slice holds slot x.
   __device__ int cta_of(int x) const {
-    return static_cast<int>((static_cast<long long>(x + 1) * Ge + n - 1) / n) - 1;
+    return static_cast<int>((static_cast<uint32_t>(x + 1) * static_cast<uint32_t>(Ge) + static_cast<uint32_t>(n) - 1u) /
+                            static_cast<uint32_t>(n)) - 1;
   }
 };
 
 struct Plan {
   int U, N, kcmax, c, G, W;
   int tiles[2], nb[2];  // per unit: GEMM1 64-row tiles x H/128 K blocks; GEMM2 128-row tiles x I/128
-  __device__ int wave_lo(int w) const { return static_cast<int>(static_cast<long long>(U) * w / W); }
+  __device__ int wave_lo(int w) const { return U * w / W; }
   // Stage q of 2W: GEMM1 of wave 0, then GEMM1(w + 1) / GEMM2(w) pairs, then
   // the last GEMM2.
   __device__ void stage(int q, int& w, int& phase) const {
@@ -657,8 +660,8 @@ __device__ void end_segment(const TcArgs& a, TcSmem& S, const Plan& P, const Chu
     finish_gemm2<TOK>(a, S, ch, b, y, row);
 }
 
-// Wait until every GEMM1 tile of expert u is finished, then count this CTA in;
-// the last CTA with GEMM2 work on it re-arms the counters for the next call.
+// Wait until every GEMM1 tile of expert u is finished. (pass_hidden counts
+// the CTA in afterwards, off the path to the first GEMM2 MMA.)
 __device__ bool wait_hidden(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& ch, int fid) {
   const int u = ch.u;
   if (fid == 0) {
@@ -673,22 +676,26 @@ __device__ bool wait_hidden(const TcArgs& a, TcSmem& S, const Plan& P, const Chu
       }
       __nanosleep(64);
     }
-    if (!ok) {
-      if (!S.abort) tc_error(a, S, kErrCrossWait);
-    } else {
-      const PhasePlan& p2 = ch.pp;
-      const int s0 = (u - p2.u0) * p2.tiles * p2.nb;
-      const int s1 = s0 + p2.tiles * p2.nb - 1;
-      const uint32_t ctas = static_cast<uint32_t>(p2.cta_of(s1) - p2.cta_of(s0) + 1);
-      const uint32_t old = atomicAdd(a.passed + e, 1u);
-      if (old + 1u == ctas) {
-        atomicExch(a.done + e, 0u);
-        atomicExch(a.passed + e, 0u);
-      }
-    }
+    if (!ok && !S.abort) tc_error(a, S, kErrCrossWait);
   }
   fill_bar();
   return !S.abort;
+}
+
+// Count this CTA past expert u's wait; the last CTA with GEMM2 work on it
+// re-arms both counters for the next call (every such CTA has read `done`
+// by then).
+__device__ void pass_hidden(const TcArgs& a, TcSmem& S, const Chunk& ch) {
+  const int e = xinfo(a, S, ch.u).id;
+  const PhasePlan& p2 = ch.pp;
+  const int s0 = (ch.u - p2.u0) * p2.tiles * p2.nb;
+  const int s1 = s0 + p2.tiles * p2.nb - 1;
+  const uint32_t ctas = static_cast<uint32_t>(p2.cta_of(s1) - p2.cta_of(s0) + 1);
+  const uint32_t old = atomicAdd(a.passed + e, 1u);
+  if (old + 1u == ctas) {
+    atomicExch(a.done + e, 0u);
+    atomicExch(a.passed + e, 0u);
+  }
 }
 
 // Scaled sum of one chunk's per-K-block partials: y[t] += D[j][t] *
@@ -764,11 +771,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
     tmem_relinquish();
   }
   for (int e = tid; e < a.E; e += kTcThreads) S.tokmask[e] = 0ull;
-  {  // B buffers start zero (read by the tensor cores through the async proxy)
-    uint4* z = reinterpret_cast<uint4*>(&S.B[0][0]);
-    for (int i = tid; i < 2 * kBBufBytes / 16; i += kTcThreads) z[i] = make_uint4(0u, 0u, 0u, 0u);
-    fence_proxy_async_smem();
-  }
   griddep_wait();
   tc_fence_before();
   __syncthreads();
@@ -983,12 +985,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
     while (cur.next(P, ch)) {
       const int b = ci & 1;
       if (ch.u != ctx_u) fill_context(a, S, ch.u, fid);
-      if (ch.phase == 2 && (ch.u != ctx_u || ctx_phase != 2)) {
-        if (!wait_hidden(a, S, P, ch, fid)) break;
-      }
+      const bool first2 = ch.phase == 2 && (ch.u != ctx_u || ctx_phase != 2);
+      if (first2 && !wait_hidden(a, S, P, ch, fid)) break;
       ctx_u = ch.u;
       ctx_phase = ch.phase;
       if (!fill_b(a, S, P, ch, b, ci, fid)) break;
+      if (first2 && fid == 0) pass_hidden(a, S, ch);
       ++ci;
     }
   }
