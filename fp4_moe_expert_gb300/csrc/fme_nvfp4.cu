@@ -1,4 +1,5 @@
-// NVFP4 slot MoE over one local expert range: one persistent sm_103a kernel.
+// NVFP4 slot MoE over one local expert range: one persistent sm_103a kernel
+// on the 5th-generation tensor cores.
 //
 // Computes what "nvfp4-megamoe-kernel README.md" describes (slot
 // representation; Data Formats; Bugs Found & Fixed 2, 4, 6, 7): a slot is a
@@ -7,637 +8,877 @@
 // scales, the L2 GEMM; the routing weights are applied once, in the final
 // scatter to [M, H]. The design is this library's own:
 //
-// * One CTA per SM; every CTA derives the same ascending list of touched
-//   local experts from topk_ids, so each touched expert streams once.
-// * Phase 1 items: 4*rg gate rows plus the matching up rows of one expert
-//   (packed E2M1 rows and their UE4M3 scale rows, both contiguous), so
-//   SwiGLU finishes in the item. Output h (BF16 value) goes to the workspace.
-// * Phase 2 items: 8*rg rows of W2; they wait (bounded) for all phase-1 items
-//   of their expert, quantise h per 16 themselves and write the slot outputs
-//   o (BF16) to the workspace.
-// * Phase 3: every CTA waits (bounded) for all phase-2 items, then sums, for
-//   its slice of columns, w[t, r] * o[slot] over the token's local picks in
-//   ascending order in FP32 and stores y once as BF16.
-// * Weight rows stream through the same cp.async.bulk ring as the FP8
-//   kernel; the math is cvt.rn.f16x2.e2m1x2 plus fma.rn.f32.f16 (exact
-//   products, exact group sums), times the exact product of the two UE4M3
-//   scales of each group.
+// * Every E2M1 value times its UE4M3 group scale is exact in FP16 (at most 6
+//   significant bits, magnitudes 2^-10 .. 2688), so both operands are folded
+//   into FP16 and multiplied on `tcgen05.mma kind::f16` with FP32
+//   accumulation: each product is exact and only the FP32 sums round, like
+//   the pages' block-scaled product.
+// * Weights: TMA streams the packed E2M1 rows (no swizzle) into a ring; four
+//   dequant warps expand each 128-row x 128-value K block with its group
+//   scales into an FP16 operand in the 128-byte-swizzled K-major layout.
+// * Activations: at start every CTA quantises a share of x into an FP16
+//   image in the workspace (all tokens, 16 or 64 rows); the GEMM1 epilogue
+//   quantises each slot's h (groups of 16 lie inside one 64-row tile) into a
+//   second image whose rows are the slots of each expert, consecutive. A
+//   second TMA thread loads both as the B operand; GEMM1 uses every token as
+//   a column and reads back the routed ones.
+// * Work split, split-tile finishing and bounded waits follow the routed FP8
+//   kernel: one CTA per SM, each phase's (expert, tile, K block) list cut
+//   into equal slices, a split tile finished by its first contributor.
+// * The scatter y[t] = bf16(sum over t's local picks, ascending, of
+//   w * o[slot]) in FP32 runs after every GEMM2 tile (bounded wait).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
 #include "fme_common.cuh"
 #include "fme_internal.h"
 
 namespace fme {
 
-struct Fp4Args {
+constexpr int kNvThreads = 352;        // A TMA, MMA, B TMA, 4 dequant, 4 epilogue warps
+constexpr int kNvRawBytes = 128 * 64;  // one K block: 128 rows x 64 packed bytes
+
+template <int TOK>
+struct NvCfg {
+  static constexpr int kStages = TOK == 16 ? 10 : 5;
+  static constexpr int kBBytes = 2 * TOK * 128;  // two 64-value halves, TOK rows of 128 bytes each
+};
+
+struct NvArgs {
+  CUtensorMap map13;  // W13 packed [L * 2N rows, H/2 bytes], box 64 rows x 64 bytes
+  CUtensorMap map2;   // W2 packed [L * H rows, N/2 bytes]
+  CUtensorMap mapx;   // x image [(H/64) * TOK rows, 128 bytes], box TOK rows, 128-byte swizzle
+  CUtensorMap maph;   // h image [(N/64) * Rp rows, 128 bytes]
   const __nv_bfloat16* x;
   const int32_t* ids;
-  const float* tw;  // topk weights
-  const uint8_t* w13;
+  const float* tw;
   const uint8_t* s13;
-  const uint8_t* w2;
   const uint8_t* s2;
   __nv_bfloat16* y;
   uint32_t* err;
-  uint32_t* done;      // [L] phase-1 items completed per local expert
-  uint32_t* consumed;  // [L] phase-2 items that passed the wait
-  uint32_t* done2;     // phase-2 items completed (all experts)
-  uint32_t* passed3;   // CTAs past the phase-3 wait
-  float* hbuf;         // [routes, N] SwiGLU output (BF16 values)
-  __nv_bfloat16* obuf; // [routes, H] slot outputs
-  int M, H, N, L, e0, top_k;
+  uint32_t* sync;     // [4]: x image shares written, CTAs past that wait, GEMM2 tiles done, CTAs past the scatter wait
+  uint32_t* done;     // [L] GEMM1 tiles finished per local expert
+  uint32_t* hpassed;  // [L] CTAs past the expert's hidden wait
+  uint32_t* cnt1;     // [L * N/64] contributors per GEMM1 tile
+  uint32_t* cnt2;     // [L * H/128]
+  uint8_t* ximg;
+  uint8_t* himg;
+  __nv_bfloat16* obuf;  // [M * top_k, H] slot outputs (route order)
+  float* part;          // [2][kFp8MaxCtas][2][TOK][128]
+  int M, H, N, L, e0, top_k, Rp;
   float limit;
-  PhaseGeom g1, g2;  // slices are 16 packed bytes = 32 values
-  int gp, r2;
   unsigned long long timeout_ns;
 };
 
-constexpr int kFp4Slice = 32;  // values per 16-byte slice
-
-struct Fp4Smem {
-  uint8_t ring[kStages][kStageBytes];
-  uint64_t full[kStages];
+template <int TOK>
+struct NvSmem {
+  uint8_t A16[2][2][128 * 128];  // FP16 weights [buffer][K half][128 rows x 128 B], 128-byte swizzle
+  uint8_t B[NvCfg<TOK>::kStages][NvCfg<TOK>::kBBytes];
+  uint8_t R[NvCfg<TOK>::kStages][kNvRawBytes];
+  uint64_t fullA[NvCfg<TOK>::kStages], fullB[NvCfg<TOK>::kStages];
+  uint64_t emptyA[NvCfg<TOK>::kStages], emptyB[NvCfg<TOK>::kStages];
+  uint64_t afull[2], afree[2], accfull[2], tmemfree[2], final_bar;
+  float ysm[16][128];
   unsigned long long tokmask[kMaxExperts];
   int16_t ulist[kMaxExperts];
-  float red[kComputeWarps][32];
-  float ysum[64][kTokChunk];
-  int16_t ctx_route[kMaxTokens];
-  int16_t ctx_tok[kMaxTokens];
-  int ctx_n;
+  int16_t uidx[kMaxExperts];      // local expert -> unit
+  int16_t uoff[kMaxExperts + 1];  // first compact slot row of each unit
+  int16_t stok[kMaxTokens * kMaxTopK];
+  int16_t sroute[kMaxTokens * kMaxTopK];
+  uint32_t tmem_base;
   int U;
   volatile int abort;
 };
 
-constexpr size_t kFp4SmemBytes = sizeof(Fp4Smem) + 1024;
+template <int TOK>
+constexpr size_t nv_smem_bytes() {
+  return sizeof(NvSmem<TOK>) + 1024;
+}
+static_assert(nv_smem_bytes<16>() <= 232448 && nv_smem_bytes<64>() <= 232448, "shared memory per CTA");
 
-__device__ __forceinline__ void fp4_error(const Fp4Args& a, Fp4Smem& S, uint32_t bit) {
+__device__ __forceinline__ void nv_epi_bar() { named_bar_sync(1, 128); }
+
+__device__ __forceinline__ void nv_error(const NvArgs& a, volatile int& abort, uint32_t bit) {
   atomicOr(a.err, bit);
-  S.abort = 1;
+  abort = 1;
 }
 
-__device__ __forceinline__ void fp4_bar() { named_bar_sync(1, kComputeThreads); }
-
-// E4M3 byte (UE4M3 scale) of amax / 6 and the value it stores.
-__device__ __forceinline__ float fp4_group_scale(float amax, uint32_t& byte) {
-  byte = f32x2_to_e4m3x2(__fdiv_rn(amax, 6.0f), 0.0f) & 0xFFu;
-  return e4m3_to_f32(byte);
+// tcgen05.mma kind::f16 (both operands F16, K-major, FP32 accumulation): the
+// instruction descriptor has the fields of kind::f8f6f4, format code 0 = F16.
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
-// Quantise 32 values (two groups of 16) to E2M1 nibbles with their group
-// scales, as exact f16 pairs: "nvfp4-megamoe-kernel README.md" Bugs Found &
-// Fixed 2 (stored scale = block_max / 6, also the divisor; signed E2M1).
-__device__ __forceinline__ void fp4_quant32(const float (&v)[32], uint32_t (&out)[16], float (&sc)[2]) {
-#pragma unroll
-  for (int g = 0; g < 2; ++g) {
-    float amax = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(v[16 * g + k]));
-    uint32_t byte;
-    const float d = fp4_group_scale(amax, byte);
-    sc[g] = d;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      uint32_t nib = 0u;
-      if (d > 0.0f) nib = f32x2_to_e2m1x2(__fdiv_rn(v[16 * g + 2 * k], d), __fdiv_rn(v[16 * g + 2 * k + 1], d));
-      out[8 * g + k] = e2m1x2_to_f16x2(nib);
-    }
+// 2-D tiled TMA load without an L2 cache hint (the activation images are small
+// and re-read by every CTA).
+__device__ __forceinline__ void tma_load_2d_plain(void* dst, const void* tmap, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// UE4M3 scale byte of a group: e4m3(amax / 6), saturating ("nvfp4-megamoe-kernel
+// README.md" Bugs Found & Fixed 2: the stored scale is also the divisor).
+__device__ __forceinline__ uint32_t nv_scale_byte(float amax) {
+  return f32x2_to_e4m3x2(__fdiv_rn(amax, 6.0f), 0.0f) & 0xFFu;
+}
+// f16x2 (s, s) of a UE4M3 byte.
+__device__ __forceinline__ uint32_t nv_scale_h2(uint32_t byte) {
+  uint32_t lo, hi;
+  e4m3x4_to_f16x2x2(byte & 0xFFu, lo, hi);
+  const uint32_t h = lo & 0xFFFFu;
+  return h | (h << 16);
+}
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// Two values -> their E2M1 codes times the group scale, as one f16x2 word
+// (exact). d == 0 gives zeros (a zero scale quantises its group to zeros).
+__device__ __forceinline__ uint32_t nv_fold2(float v0, float v1, float d, uint32_t sh2) {
+  if (!(d > 0.0f)) return 0u;
+  const uint32_t nib = f32x2_to_e2m1x2(__fdiv_rn(v0, d), __fdiv_rn(v1, d));
+  return hmul2_u32(e2m1x2_to_f16x2(nib), sh2);
+}
+
+// ---------------------------------------------------------------- work plan
+// Each phase's (unit, tile, K block) slots -- at most 1024 x 128 x 64 = 8.4M --
+// split over Ge = min(G, n) CTAs as in the routed FP8 kernel; the products stay
+// below 2^32, so unsigned 32-bit arithmetic is exact.
+struct NvPhase {
+  int n, lo, hi, Ge, tiles, nb;
+  __device__ int lo_of(int c) const {
+    return c >= Ge ? n : static_cast<int>(static_cast<uint32_t>(n) * static_cast<uint32_t>(c) /
+                                          static_cast<uint32_t>(Ge));
   }
-}
-
-template <int RTC>
-__device__ __forceinline__ void fp4_quant_x(const Fp4Args& a, const Fp4Smem& S, int c0, int rt, int gt,
-                                            uint32_t (&xa)[kTokChunk][16], float (&xs)[kTokChunk][2]) {
-  const PhaseGeom& g = a.g1;
-  const int s = gt;
-#pragma unroll
-  for (int t = 0; t < RTC; ++t) {
-    if (s < g.ns && t < rt) {
-      const int tok = S.ctx_tok[c0 + t];
-      const uint4* p = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(tok) * a.H + kFp4Slice * s);
-      float v[32];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 w = __ldg(p + q);
-        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          v[8 * q + 2 * k] = __uint_as_float(ww[k] << 16);
-          v[8 * q + 2 * k + 1] = __uint_as_float(ww[k] & 0xFFFF0000u);
-        }
-      }
-      fp4_quant32(v, xa[t], xs[t]);
-    } else {
-#pragma unroll
-      for (int k = 0; k < 16; ++k) xa[t][k] = 0u;
-      xs[t][0] = xs[t][1] = 0.0f;
-    }
+  __device__ int cta_of(int x) const {
+    return static_cast<int>((static_cast<uint32_t>(x + 1) * static_cast<uint32_t>(Ge) + static_cast<uint32_t>(n) - 1u) /
+                            static_cast<uint32_t>(n)) - 1;
   }
-}
-
-template <int RTC>
-__device__ __forceinline__ void fp4_quant_h(const Fp4Args& a, const Fp4Smem& S, int c0, int rt, int gt,
-                                            uint32_t (&xa)[kTokChunk][16], float (&xs)[kTokChunk][2]) {
-  const PhaseGeom& g = a.g2;
-  const int s = gt;
-#pragma unroll
-  for (int t = 0; t < RTC; ++t) {
-    if (s < g.ns && t < rt) {
-      const int route = S.ctx_route[c0 + t];
-      const float4* p = reinterpret_cast<const float4*>(a.hbuf + static_cast<size_t>(route) * a.N + kFp4Slice * s);
-      float v[32];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 f = __ldcg(p + q);
-        v[4 * q] = f.x;
-        v[4 * q + 1] = f.y;
-        v[4 * q + 2] = f.z;
-        v[4 * q + 3] = f.w;
-      }
-      fp4_quant32(v, xa[t], xs[t]);
-    } else {
-#pragma unroll
-      for (int k = 0; k < 16; ++k) xa[t][k] = 0u;
-      xs[t][0] = xs[t][1] = 0.0f;
-    }
-  }
-}
-
-// acc[q * RTC + t] += dot of row (row0 + q) slice s with token t, per group
-// times (weight group scale * activation group scale).
-template <int RTC>
-__device__ __forceinline__ void fp4_dot_rows(const uint8_t* packed, const uint8_t* scales, int rowbytes,
-                                             int scalebytes, int row0, int s, int ns,
-                                             const uint32_t (&xa)[kTokChunk][16], const float (&xs)[kTokChunk][2],
-                                             float (&acc)[kRowsPerGroup * RTC]) {
-  if (s >= ns) return;
-#pragma unroll
-  for (int q = 0; q < kRowsPerGroup; ++q) {
-    const int row = row0 + q;
-    const uint4 w = *reinterpret_cast<const uint4*>(packed + static_cast<size_t>(row) * rowbytes + 16 * s);
-    const uint32_t sb = *reinterpret_cast<const uint16_t*>(scales + static_cast<size_t>(row) * scalebytes + 2 * s);
-    const float sw0 = e4m3_to_f32(sb & 0xFFu), sw1 = e4m3_to_f32(sb >> 8);
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-    uint32_t wf[16];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-#pragma unroll
-      for (int b = 0; b < 4; ++b) wf[4 * k + b] = e2m1x2_to_f16x2(ww[k] >> (8 * b));
-    }
-#pragma unroll
-    for (int t = 0; t < RTC; ++t) {
-      float p0 = 0.0f, p1 = 0.0f;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) p0 = fma_f16x2_f32(wf[k], xa[t][k], p0);
-#pragma unroll
-      for (int k = 8; k < 16; ++k) p1 = fma_f16x2_f32(wf[k], xa[t][k], p1);
-      acc[q * RTC + t] = fmaf(p0, __fmul_rn(sw0, xs[t][0]), acc[q * RTC + t]);
-      acc[q * RTC + t] = fmaf(p1, __fmul_rn(sw1, xs[t][1]), acc[q * RTC + t]);
-    }
-  }
-}
-
-__device__ void fp4_context(const Fp4Args& a, Fp4Smem& S, int le, int ctid) {
-  if (ctid < 32) {
-    const int lane = ctid;
-    const unsigned long long mask = S.tokmask[le];
-    int base = 0;
-    for (int t0 = 0; t0 < a.M; t0 += 32) {
-      const int t = t0 + lane;
-      const bool has = (t < a.M) && ((mask >> t) & 1ull);
-      const uint32_t bal = __ballot_sync(0xFFFFFFFFu, has);
-      if (has) {
-        const int pos = base + __popc(bal & ((1u << lane) - 1u));
-        int r = 0;
-        for (int k = 0; k < a.top_k; ++k)
-          if (__ldg(a.ids + t * a.top_k + k) - a.e0 == le) r = k;
-        S.ctx_route[pos] = static_cast<int16_t>(t * a.top_k + r);
-        S.ctx_tok[pos] = static_cast<int16_t>(t);
-      }
-      base += __popc(bal);
-    }
-    if (lane == 0) S.ctx_n = base;
-  }
-  fp4_bar();
-}
-
-template <int RTC>
-__device__ __forceinline__ void fp4_reduce(Fp4Smem& S, float (&acc)[kRowsPerGroup * RTC], int warp, int lane) {
-  constexpr int V = kRowsPerGroup * RTC;
-  const float s = warp_transpose_sum<V>(acc, lane);
-  if ((lane % (32 / V)) == 0) S.red[warp][lane / (32 / V)] = s;
-}
-
-template <int RTC>
-__device__ void fp4_gemm1_chunk(const Fp4Args& a, Fp4Smem& S, const uint8_t* stage, int h0, int c0, int rt,
-                                bool requant, int ctid, int warp, int lane, uint32_t (&xa)[kTokChunk][16],
-                                float (&xs)[kTokChunk][2]) {
-  const PhaseGeom& g = a.g1;
-  const int grp = ctid / g.tpr, gt = ctid % g.tpr;
-  if (requant) fp4_quant_x<RTC>(a, S, c0, rt, gt, xa, xs);
-  float acc[kRowsPerGroup * RTC];
-#pragma unroll
-  for (int v = 0; v < kRowsPerGroup * RTC; ++v) acc[v] = 0.0f;
-  const int rows = 2 * a.gp;
-  const uint8_t* scales = stage + static_cast<size_t>(rows) * (a.H / 2);
-  fp4_dot_rows<RTC>(stage, scales, a.H / 2, a.H / 16, grp * kRowsPerGroup, gt, g.ns, xa, xs, acc);
-  fp4_reduce<RTC>(S, acc, warp, lane);
-  fp4_bar();
-  constexpr int V = kRowsPerGroup * RTC;
-  const int wpg = g.tpr / 32;
-  if (ctid < g.rg * V) {
-    const int fg = ctid / V, v = ctid % V;
-    float s = 0.0f;
-    for (int w = 0; w < wpg; ++w) s += S.red[fg * wpg + w][v];
-    S.ysum[fg * kRowsPerGroup + v / RTC][v % RTC] = s;
-  }
-  fp4_bar();
-  if (ctid < a.gp * RTC && ctid % RTC < rt) {
-    const int q = ctid / RTC, t = ctid % RTC;
-    // L1 rows: [gate; up] (README Bugs Found & Fixed 4); L1 output is BF16.
-    const float gate = __bfloat162float(__float2bfloat16_rn(S.ysum[q][t]));
-    const float up = __bfloat162float(__float2bfloat16_rn(S.ysum[a.gp + q][t]));
-    const float L = a.limit;
-    const float gc = fminf(gate, L);
-    const float uc = fmaxf(fminf(up, L), -L);
-    const float silu = __fdiv_rn(gc, __fadd_rn(1.0f, expf(-gc)));
-    const float h = __bfloat162float(__float2bfloat16_rn(__fmul_rn(silu, uc)));
-    a.hbuf[static_cast<size_t>(S.ctx_route[c0 + t]) * a.N + h0 + q] = h;
-  }
-  fp4_bar();
-}
-
-template <int RTC>
-__device__ void fp4_gemm2_chunk(const Fp4Args& a, Fp4Smem& S, const uint8_t* stage, int m0, int c0, int rt,
-                                bool requant, int ctid, int warp, int lane, uint32_t (&xa)[kTokChunk][16],
-                                float (&xs)[kTokChunk][2]) {
-  const PhaseGeom& g = a.g2;
-  const int grp = ctid / g.tpr, gt = ctid % g.tpr;
-  if (requant) fp4_quant_h<RTC>(a, S, c0, rt, gt, xa, xs);
-  float acc[kRowsPerGroup * RTC];
-#pragma unroll
-  for (int v = 0; v < kRowsPerGroup * RTC; ++v) acc[v] = 0.0f;
-  const uint8_t* scales = stage + static_cast<size_t>(a.r2) * (a.N / 2);
-  fp4_dot_rows<RTC>(stage, scales, a.N / 2, a.N / 16, grp * kRowsPerGroup, gt, g.ns, xa, xs, acc);
-  fp4_reduce<RTC>(S, acc, warp, lane);
-  fp4_bar();
-  constexpr int V = kRowsPerGroup * RTC;
-  const int wpg = g.tpr / 32;
-  if (ctid < g.rg * V && (ctid % V) % RTC < rt) {
-    const int fg = ctid / V, v = ctid % V;
-    float s = 0.0f;
-    for (int w = 0; w < wpg; ++w) s += S.red[fg * wpg + w][v];
-    const int m = m0 + fg * kRowsPerGroup + v / RTC;
-    a.obuf[static_cast<size_t>(S.ctx_route[c0 + v % RTC]) * a.H + m] = __float2bfloat16_rn(s);
-  }
-  fp4_bar();
-}
-
-struct Fp4Plan {
-  long long lo1, hi1, lo2, hi2;
-  int per_u1, per_u2;
-  __device__ int count() const { return static_cast<int>((hi1 - lo1) + (hi2 - lo2)); }
 };
 
-__device__ void fp4_issue(const Fp4Args& a, Fp4Smem& S, const Fp4Plan& P, int it, uint64_t pol) {
-  const int s = it % kStages;
-  uint8_t* dst = S.ring[s];
-  if (it < P.hi1 - P.lo1) {
-    const long long i = P.lo1 + it;
-    const int u = static_cast<int>(i / P.per_u1);
-    const int h0 = static_cast<int>(i % P.per_u1) * a.gp;
-    const int le = S.ulist[u];
-    const uint32_t pb = static_cast<uint32_t>(a.gp) * (a.H / 2);   // packed bytes per half
-    const uint32_t sb = static_cast<uint32_t>(a.gp) * (a.H / 16);  // scale bytes per half
-    mbar_arrive_expect_tx(&S.full[s], 2 * (pb + sb));
-    const size_t row_g = static_cast<size_t>(le) * 2 * a.N + h0;    // first gate row
-    const size_t row_u = row_g + a.N;                               // first up row
-    bulk_g2s(dst, a.w13 + row_g * (a.H / 2), pb, &S.full[s], pol);
-    bulk_g2s(dst + pb, a.w13 + row_u * (a.H / 2), pb, &S.full[s], pol);
-    bulk_g2s(dst + 2 * pb, a.s13 + row_g * (a.H / 16), sb, &S.full[s], pol);
-    bulk_g2s(dst + 2 * pb + sb, a.s13 + row_u * (a.H / 16), sb, &S.full[s], pol);
+__device__ NvPhase nv_phase(int n, int tiles, int nb, int G, int c) {
+  NvPhase p;
+  p.n = n;
+  p.tiles = tiles;
+  p.nb = nb;
+  p.Ge = min(G, n);
+  if (c >= p.Ge) {
+    p.lo = p.hi = n;
   } else {
-    const long long i = P.lo2 + (it - (P.hi1 - P.lo1));
-    const int u = static_cast<int>(i / P.per_u2), rb = static_cast<int>(i % P.per_u2);
-    const int le = S.ulist[u];
-    const uint32_t pb = static_cast<uint32_t>(a.r2) * (a.N / 2);
-    const uint32_t sb = static_cast<uint32_t>(a.r2) * (a.N / 16);
-    mbar_arrive_expect_tx(&S.full[s], pb + sb);
-    const size_t row = static_cast<size_t>(le) * a.H + static_cast<size_t>(rb) * a.r2;
-    bulk_g2s(dst, a.w2 + row * (a.N / 2), pb, &S.full[s], pol);
-    bulk_g2s(dst + pb, a.s2 + row * (a.N / 16), sb, &S.full[s], pol);
+    p.lo = p.lo_of(c);
+    p.hi = p.lo_of(c + 1);
   }
+  return p;
 }
 
-__device__ __forceinline__ bool fp4_wait_stage(const Fp4Args& a, Fp4Smem& S, int it) {
-  if (!mbar_wait(&S.full[it % kStages], (it / kStages) & 1, a.timeout_ns, &S.abort)) {
-    if (!S.abort) fp4_error(a, S, kErrRingWait);
-  }
-  fp4_bar();
-  return !S.abort;
-}
+// One K block of this CTA's slices, phase 1 then phase 2.
+struct NvStep {
+  int phase, u, T, kb;
+  int t0;            // first slot of the tile
+  bool first, last;  // first / last K block of its segment
+};
 
-__device__ void fp4_drain(const Fp4Args& a, Fp4Smem& S, const Fp4Plan& P, int consumed) {
-  if (threadIdx.x != 0) return;
-  const int issued = min(P.count(), consumed + kStages);
-  for (int k = consumed; k < issued; ++k)
-    if (!mbar_wait(&S.full[k % kStages], (k / kStages) & 1, a.timeout_ns, nullptr)) atomicOr(a.err, kErrDrain);
-}
-
-__device__ bool wait_counter(const Fp4Args& a, Fp4Smem& S, const uint32_t* ctr, uint32_t target) {
-  if (threadIdx.x == 0) {
-    const uint64_t t0 = globaltimer_ns();
-    while (ld_acquire_gpu(ctr) < target) {
-      if (globaltimer_ns() - t0 > a.timeout_ns) {
-        fp4_error(a, S, kErrCrossWait);
-        break;
+struct NvCursor {
+  int pos, phase;
+  __device__ bool next(const NvPhase (&P)[2], NvStep& st) {
+    while (true) {
+      const NvPhase& p = P[phase - 1];
+      if (pos < p.lo) pos = p.lo;
+      if (pos < p.hi) {
+        const int tile = pos / p.nb;
+        st.phase = phase;
+        st.u = tile / p.tiles;
+        st.T = tile - st.u * p.tiles;
+        st.t0 = tile * p.nb;
+        st.kb = pos - st.t0;
+        st.first = pos == p.lo || st.kb == 0;
+        st.last = pos + 1 == p.hi || st.kb == p.nb - 1;
+        ++pos;
+        return true;
       }
-      __nanosleep(64);
+      if (phase == 2) return false;
+      phase = 2;
+      pos = P[1].lo;
     }
   }
-  fp4_bar();
-  return !S.abort;
+};
+
+__device__ __forceinline__ float* nv_part(const NvArgs& a, int phase, int c, int slot, int tok) {
+  return a.part + ((static_cast<size_t>(phase - 1) * kFp8MaxCtas + c) * 2 + slot) * tok * 128;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) nvfp4_moe_kernel(const __grid_constant__ Fp4Args a) {
+// ---------------------------------------------------------------- epilogue
+// GEMM1 tile T of unit u (rows 0..63 gate 64T + q, 64..127 up): per slot of
+// the unit, g = bf16(gate), v = bf16(up), h = bf16(silu(min(g, L)) *
+// clamp(v, -L, L)) ("nvfp4-megamoe-kernel README.md" Bugs Found & Fixed 4
+// and 6), then h -> E2M1 x UE4M3 per 16 (groups 16j..16j+15 of the tile are
+// half-warps) folded into FP16 and written to the h image row of the slot.
+template <int TOK>
+__device__ void nv_finish1(const NvArgs& a, NvSmem<TOK>& S, int u, int T, const float (&y)[TOK], int row,
+                           int etid) {
+  const int le = S.ulist[u];
+  const int r0 = S.uoff[u], r = S.uoff[u + 1] - r0;
+  const int q = row & 63;
+  const float L = a.limit;
+  for (int g = 0; g * 16 < a.M; ++g) {
+#pragma unroll
+    for (int gg = 0; gg < TOK / 16; ++gg) {
+      if (gg == g) {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) S.ysm[t][row] = y[gg * 16 + t];
+      }
+    }
+    nv_epi_bar();
+    if (row < 64) {
+#pragma unroll 1
+      for (int i = 0; i < r; ++i) {
+        const int t = S.stok[r0 + i];
+        if (t < g * 16 || t >= g * 16 + 16) continue;  // uniform over the warp
+        const float gate = __bfloat162float(__float2bfloat16_rn(S.ysm[t - g * 16][q]));
+        const float up = __bfloat162float(__float2bfloat16_rn(S.ysm[t - g * 16][q + 64]));
+        const float gc = fminf(gate, L);
+        const float uc = fmaxf(fminf(up, L), -L);
+        const float silu = __fdiv_rn(gc, __fadd_rn(1.0f, expf(-gc)));
+        const float h = __bfloat162float(__float2bfloat16_rn(__fmul_rn(silu, uc)));
+        float amax = fabsf(h);
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 8));
+        const uint32_t sb = nv_scale_byte(amax);
+        const float d = e4m3_to_f32(sb);
+        // Pair with the neighbour lane: one f16x2 word per even lane.
+        const float hn = __shfl_xor_sync(0xFFFFFFFFu, h, 1);
+        if ((q & 1) == 0) {
+          const uint32_t w = nv_fold2(h, hn, d, nv_scale_h2(sb));
+          *reinterpret_cast<uint32_t*>(a.himg + (static_cast<size_t>(T) * a.Rp + r0 + i) * 128 + q * 2) = w;
+        }
+      }
+    }
+    nv_epi_bar();
+  }
+  // The barrier orders every thread's image writes before this release.
+  if (etid == 0) red_release_gpu_add(a.done + le, 1u);
+}
+
+// GEMM2 tile T2 of unit u: o[slot, 128*T2 + row] = bf16(y[i]) for slot i.
+template <int TOK>
+__device__ void nv_finish2(const NvArgs& a, NvSmem<TOK>& S, int u, int T2, const float (&y)[TOK], int row,
+                           int etid) {
+  const int r0 = S.uoff[u], r = S.uoff[u + 1] - r0;
+  const int m = 128 * T2 + row;
+#pragma unroll
+  for (int i = 0; i < TOK; ++i)
+    if (i < r) a.obuf[static_cast<size_t>(S.sroute[r0 + i]) * a.H + m] = __float2bfloat16_rn(y[i]);
+  nv_epi_bar();
+  if (etid == 0) red_release_gpu_add(a.sync + 2, 1u);
+}
+
+// End of a segment (see the routed FP8 kernel): a split tile is finished by
+// its first contributor, which adds the others' partials in CTA order.
+template <int TOK>
+__device__ void nv_end_segment(const NvArgs& a, NvSmem<TOK>& S, const NvPhase (&P)[2], const NvStep& st,
+                               float (&y)[TOK], int row, int etid) {
+  const NvPhase& pp = P[st.phase - 1];
+  const int cf = pp.cta_of(st.t0), cl = pp.cta_of(st.t0 + pp.nb - 1);
+  const int c = blockIdx.x;
+  const int ncols = st.phase == 1 ? a.M : S.uoff[st.u + 1] - S.uoff[st.u];
+  if (cf != cl) {
+    const int le = S.ulist[st.u];
+    uint32_t* cnt = st.phase == 1 ? a.cnt1 + static_cast<size_t>(le) * pp.tiles + st.T
+                                  : a.cnt2 + static_cast<size_t>(le) * pp.tiles + st.T;
+    if (c != cf) {
+      float* mine = nv_part(a, st.phase, c, pp.lo >= st.t0 ? 0 : 1, TOK);
+#pragma unroll
+      for (int t = 0; t < TOK; ++t)
+        if (t < ncols) __stcg(mine + t * 128 + row, y[t]);
+      nv_epi_bar();
+      if (etid == 0) red_release_gpu_add(cnt, 1u);
+      return;
+    }
+    if (etid == 0) {
+      const uint32_t want = static_cast<uint32_t>(cl - cf);
+      const uint64_t t0 = globaltimer_ns();
+      bool ok = true;
+      while (ld_acquire_gpu(cnt) < want) {
+        if (S.abort || globaltimer_ns() - t0 > a.timeout_ns) {
+          ok = false;
+          break;
+        }
+        __nanosleep(32);
+      }
+      if (ok)
+        atomicExch(cnt, 0u);
+      else if (!S.abort)
+        nv_error(a, S.abort, kErrCrossWait);
+    }
+    nv_epi_bar();
+    if (S.abort) return;
+    for (int c0 = cf + 1; c0 <= cl; c0 += 4) {
+      const float* src[4];
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        const int cc = min(c0 + qq, cl);
+        src[qq] = nv_part(a, st.phase, cc, pp.lo_of(cc) >= st.t0 ? 0 : 1, TOK) + row;
+      }
+      const int nq = min(4, cl - c0 + 1);
+#pragma unroll
+      for (int t = 0; t < TOK; ++t) {
+        if (t < ncols) {
+          float v[4];
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) v[qq] = __ldcg(src[qq] + t * 128);
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq)
+            if (qq < nq) y[t] += v[qq];
+        }
+      }
+    }
+  }
+  if (st.phase == 1)
+    nv_finish1<TOK>(a, S, st.u, st.T, y, row, etid);
+  else
+    nv_finish2<TOK>(a, S, st.u, st.T, y, row, etid);
+}
+
+// Bounded wait of one thread until *ctr >= target.
+__device__ bool nv_wait_ge(const NvArgs& a, volatile int& abort, const uint32_t* ctr, uint32_t target) {
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire_gpu(ctr) < target) {
+    if (abort || globaltimer_ns() - t0 > a.timeout_ns) {
+      if (!abort) nv_error(a, abort, kErrCrossWait);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------- kernel
+template <int TOK>
+__global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_constant__ NvArgs a) {
+  using C = NvCfg<TOK>;
+  constexpr int kS = C::kStages;
   extern __shared__ uint8_t smem_raw[];
-  Fp4Smem& S = *reinterpret_cast<Fp4Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  NvSmem<TOK>& S = *reinterpret_cast<NvSmem<TOK>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x, c = blockIdx.x;
+
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&S.full[s], 1);
+    for (int s = 0; s < kS; ++s) {
+      mbar_init(&S.fullA[s], 1);
+      mbar_init(&S.fullB[s], 1);
+      mbar_init(&S.emptyA[s], 4);
+      mbar_init(&S.emptyB[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&S.afull[b], 4);
+      mbar_init(&S.afree[b], 1);
+      mbar_init(&S.accfull[b], 1);
+      mbar_init(&S.tmemfree[b], 4);
+    }
+    mbar_init(&S.final_bar, 1);
     fence_mbar_init();
     S.abort = 0;
+    prefetch_tmap(&a.map13);
+    prefetch_tmap(&a.map2);
+    prefetch_tmap(&a.mapx);
+    prefetch_tmap(&a.maph);
   }
-  for (int e = tid; e < a.L; e += kThreads) S.tokmask[e] = 0ull;
+  if (warp == 1) {
+    tmem_alloc(&S.tmem_base, TOK == 16 ? 32 : 128);
+    tmem_relinquish();
+  }
+  for (int e = tid; e < a.L; e += kNvThreads) S.tokmask[e] = 0ull;
   griddep_wait();
+  tc_fence_before();
   __syncthreads();
-  // Local slots: picks whose expert lies in [e0, e0 + L).
-  for (int i = tid; i < a.M * a.top_k; i += kThreads) {
+  tc_fence_after();
+
+  // ---- x image: token t, group g of 16 -> FP16 (E2M1 x UE4M3), all CTAs share the work.
+  {
+    const int gpt = a.H / 16;
+    for (int i = c * kNvThreads + tid; i < a.M * gpt; i += G * kNvThreads) {
+      const int t = i / gpt, g = i % gpt;
+      const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * a.H + 16 * g);
+      const uint4 w0 = __ldg(src), w1 = __ldg(src + 1);
+      const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      float v[16];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        v[2 * k] = __uint_as_float(wd[k] << 16);
+        v[2 * k + 1] = __uint_as_float(wd[k] & 0xFFFF0000u);
+      }
+      float amax = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(v[k]));
+      const uint32_t sb = nv_scale_byte(amax);
+      const float d = e4m3_to_f32(sb);
+      const uint32_t sh2 = nv_scale_h2(sb);
+      uint32_t o[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) o[k] = nv_fold2(v[2 * k], v[2 * k + 1], d, sh2);
+      // image row (64-value half block g / 4, token t), 32 bytes at (g % 4) * 32
+      uint4* dst = reinterpret_cast<uint4*>(a.ximg + (static_cast<size_t>(g / 4) * TOK + t) * 128 + (g % 4) * 32);
+      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+  }
+  // ---- local slots and the unit list
+  for (int i = tid; i < a.M * a.top_k; i += kNvThreads) {
     const int le = __ldg(a.ids + i) - a.e0;
     if (le >= 0 && le < a.L) atomicOr(&S.tokmask[le], 1ull << (i / a.top_k));
   }
   __syncthreads();
+  if (tid == 0) red_release_gpu_add(a.sync, 1u);  // this CTA's share of the x image is written
   if (warp == 0) {
-    int U = 0;
-    for (int b = 0; b < a.L; b += 32) {
-      const int e = b + lane;
-      const bool has = (e < a.L) && (S.tokmask[e] != 0ull);
+    int U = 0, off = 0;
+    for (int b0 = 0; b0 < a.L; b0 += 32) {
+      const int e = b0 + lane;
+      const unsigned long long m = e < a.L ? S.tokmask[e] : 0ull;
+      const bool has = m != 0ull;
       const uint32_t bal = __ballot_sync(0xFFFFFFFFu, has);
-      if (has) S.ulist[U + __popc(bal & ((1u << lane) - 1u))] = static_cast<int16_t>(e);
+      const int cnt = __popcll(m);
+      // inclusive prefix of the slot counts over the lanes
+      int pre = cnt;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, pre, d);
+        if (lane >= d) pre += v;
+      }
+      const int total = __shfl_sync(0xFFFFFFFFu, pre, 31);
+      if (has) {
+        const int u = U + __popc(bal & ((1u << lane) - 1u));
+        S.ulist[u] = static_cast<int16_t>(e);
+        S.uidx[e] = static_cast<int16_t>(u);
+        S.uoff[u] = static_cast<int16_t>(off + pre - cnt);
+      }
       U += __popc(bal);
+      off += total;
     }
-    if (lane == 0) S.U = U;
+    if (lane == 0) {
+      S.U = U;
+      S.uoff[U] = static_cast<int16_t>(off);
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < a.M * a.top_k; i += kNvThreads) {
+    const int le = __ldg(a.ids + i) - a.e0;
+    if (le >= 0 && le < a.L) {
+      const int t = i / a.top_k;
+      const int u = S.uidx[le];
+      const int row = S.uoff[u] + __popcll(S.tokmask[le] & ((1ull << t) - 1ull));
+      S.stok[row] = static_cast<int16_t>(t);
+      S.sroute[row] = static_cast<int16_t>(i);
+    }
   }
   __syncthreads();
 
   const int U = S.U;
-  const int G = gridDim.x, c = blockIdx.x;
-  Fp4Plan P;
-  P.per_u1 = a.N / a.gp;
-  P.per_u2 = a.H / a.r2;
-  const long long n1 = static_cast<long long>(U) * P.per_u1, n2 = static_cast<long long>(U) * P.per_u2;
-  P.lo1 = n1 * c / G;
-  P.hi1 = n1 * (c + 1) / G;
-  P.lo2 = n2 * c / G;
-  P.hi2 = n2 * (c + 1) / G;
-  const int n_items = P.count();
+  NvPhase P[2];
+  P[0] = nv_phase(U * (a.N / 64) * (a.H / 128), a.N / 64, a.H / 128, G, c);
+  P[1] = nv_phase(U * (a.H / 128) * (a.N / 128), a.H / 128, a.N / 128, G, c);
+  const uint32_t tmem = S.tmem_base;
 
-  uint64_t pol = 0;
-  if (tid == 0 && n_items > 0) {
-    pol = l2_evict_first_policy();
-    for (int it = 0; it < min(kStages, n_items); ++it) fp4_issue(a, S, P, it, pol);
-  }
-  const int ctid = tid;
-  uint32_t xa[kTokChunk][16];
-  float xs[kTokChunk][2];
+  if (warp == 0) {
+    // ------------------------------------------------------------ A producer (packed weights)
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      NvCursor cur{P[0].lo, 1};
+      NvStep st;
+      int k = 0;
+      while (cur.next(P, st)) {
+        const int s = k % kS;
+        if (k >= kS && !mbar_wait(&S.emptyA[s], ((k / kS) - 1) & 1, a.timeout_ns, &S.abort)) {
+          if (!S.abort) nv_error(a, S.abort, kErrRingWait);
+          break;
+        }
+        const int le = S.ulist[st.u];
+        int r0, r1;
+        const void* map;
+        if (st.phase == 1) {
+          r0 = le * 2 * a.N + 64 * st.T;  // gate rows
+          r1 = r0 + a.N;                  // up rows
+          map = &a.map13;
+        } else {
+          r0 = le * a.H + 128 * st.T;
+          r1 = r0 + 64;
+          map = &a.map2;
+        }
+        mbar_arrive_expect_tx(&S.fullA[s], kNvRawBytes);
+        tma_load_2d(S.R[s], map, st.kb * 64, r0, &S.fullA[s], pol);
+        tma_load_2d(S.R[s] + kNvRawBytes / 2, map, st.kb * 64, r1, &S.fullA[s], pol);
+        ++k;
+      }
+      for (int kk = max(0, k - kS); kk < k; ++kk)
+        if (!mbar_wait(&S.fullA[kk % kS], (kk / kS) & 1, a.timeout_ns, nullptr)) atomicOr(a.err, kErrDrain);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ B producer (activation images)
+    if (lane == 0) {
+      bool ok = nv_wait_ge(a, S.abort, a.sync, static_cast<uint32_t>(G));
+      // The last CTA past the x-image wait re-arms both counters.
+      if (atomicAdd(a.sync + 1, 1u) + 1u == static_cast<uint32_t>(G)) {
+        atomicExch(a.sync, 0u);
+        atomicExch(a.sync + 1, 0u);
+      }
+      NvCursor cur{P[0].lo, 1};
+      NvStep st;
+      int k = 0, cur_u = -1;
+      while (ok && cur.next(P, st)) {
+        const int s = k % kS;
+        if (k >= kS && !mbar_wait(&S.emptyB[s], ((k / kS) - 1) & 1, a.timeout_ns, &S.abort)) {
+          if (!S.abort) nv_error(a, S.abort, kErrRingWait);
+          break;
+        }
+        if (st.phase == 1) {
+          mbar_arrive_expect_tx(&S.fullB[s], C::kBBytes);
+          tma_load_2d_plain(S.B[s], &a.mapx, 0, (2 * st.kb) * TOK, &S.fullB[s]);
+          tma_load_2d_plain(S.B[s] + TOK * 128, &a.mapx, 0, (2 * st.kb + 1) * TOK, &S.fullB[s]);
+        } else {
+          const int le = S.ulist[st.u];
+          if (st.u != cur_u) {
+            // Every GEMM1 tile of this expert must be in the h image.
+            if (!nv_wait_ge(a, S.abort, a.done + le, static_cast<uint32_t>(a.N / 64))) break;
+            cur_u = st.u;
+            const int s0 = st.u * P[1].tiles * P[1].nb, s1 = s0 + P[1].tiles * P[1].nb - 1;
+            const uint32_t ctas = static_cast<uint32_t>(P[1].cta_of(s1) - P[1].cta_of(s0) + 1);
+            if (atomicAdd(a.hpassed + le, 1u) + 1u == ctas) {
+              atomicExch(a.done + le, 0u);
+              atomicExch(a.hpassed + le, 0u);
+            }
+          }
+          const int roff = S.uoff[st.u];
+          mbar_arrive_expect_tx(&S.fullB[s], C::kBBytes);
+          tma_load_2d_plain(S.B[s], &a.maph, 0, (2 * st.kb) * a.Rp + roff, &S.fullB[s]);
+          tma_load_2d_plain(S.B[s] + TOK * 128, &a.maph, 0, (2 * st.kb + 1) * a.Rp + roff, &S.fullB[s]);
+        }
+        ++k;
+      }
+      for (int kk = max(0, k - kS); kk < k; ++kk)
+        if (!mbar_wait(&S.fullB[kk % kS], (kk / kS) & 1, a.timeout_ns, nullptr)) atomicOr(a.err, kErrDrain);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = f8_idesc(128, TOK);  // kind::f16 uses the same fields (F16 = format 0)
+      NvCursor cur{P[0].lo, 1};
+      NvStep st;
+      int k = 0, seg = 0;
+      while (cur.next(P, st)) {
+        const int s = k % kS, ab = k & 1, tb = seg & 1;
+        if (!mbar_wait(&S.afull[ab], (k >> 1) & 1, a.timeout_ns, &S.abort) ||
+            !mbar_wait(&S.fullB[s], (k / kS) & 1, a.timeout_ns, &S.abort) ||
+            (st.first && seg >= 2 && !mbar_wait(&S.tmemfree[tb], ((seg >> 1) - 1) & 1, a.timeout_ns, &S.abort))) {
+          if (!S.abort) nv_error(a, S.abort, kErrRingWait);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t abase = smem_u32(S.A16[ab][0]);
+        const uint32_t bbase = smem_u32(S.B[s]);
 #pragma unroll
-  for (int t = 0; t < kTokChunk; ++t) {
-    xs[t][0] = xs[t][1] = 0.0f;
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t ao = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+          const uint32_t bo = (kk >> 2) * (TOK * 128) + (kk & 3) * 32;
+          tc_mma_f16(tmem + tb * TOK, sw128_desc(abase + ao), sw128_desc(bbase + bo), idesc,
+                     (st.first && kk == 0) ? 0u : 1u);
+        }
+        tc_commit(&S.afree[ab]);
+        tc_commit(&S.emptyB[s]);
+        if (st.last) {
+          tc_commit(&S.accfull[tb]);
+          ++seg;
+        }
+        ++k;
+      }
+      tc_commit(&S.final_bar);
+      if (!mbar_wait(&S.final_bar, 0, a.timeout_ns, nullptr)) atomicOr(a.err, kErrDrain);
+    }
+  } else if (warp < 7) {
+    // ------------------------------------------------------------ dequant (one weight row per thread)
+    const int row = tid - 96;
+    NvCursor cur{P[0].lo, 1};
+    NvStep st;
+    int k = 0;
+    while (cur.next(P, st)) {
+      const int s = k % kS, ab = k & 1;
+      // Group scales of this row's 128 values (8 bytes), loaded before the waits.
+      const int le = S.ulist[st.u];
+      const uint8_t* sp;
+      if (st.phase == 1) {
+        const int grow = le * 2 * a.N + (row < 64 ? 64 * st.T + row : a.N + 64 * st.T + row - 64);
+        sp = a.s13 + static_cast<size_t>(grow) * (a.H / 16) + 8 * st.kb;
+      } else {
+        sp = a.s2 + (static_cast<size_t>(le) * a.H + 128 * st.T + row) * (a.N / 16) + 8 * st.kb;
+      }
+      const uint2 sw = __ldg(reinterpret_cast<const uint2*>(sp));
+      if (!mbar_wait(&S.fullA[s], (k / kS) & 1, a.timeout_ns, &S.abort) ||
+          (k >= 2 && !mbar_wait(&S.afree[ab], ((k >> 1) - 1) & 1, a.timeout_ns, &S.abort))) {
+        if (!S.abort) nv_error(a, S.abort, kErrRingWait);
+        break;
+      }
+      const uint4* src = reinterpret_cast<const uint4*>(S.R[s] + row * 64);
+      const uint32_t sw32[2] = {sw.x, sw.y};
 #pragma unroll
-    for (int k = 0; k < 16; ++k) xa[t][k] = 0u;
-  }
-
-  int it = 0, cur_u = -1;
-  for (long long i = P.lo1; i < P.hi1; ++i, ++it) {
-    const int u = static_cast<int>(i / P.per_u1);
-    const int h0 = static_cast<int>(i % P.per_u1) * a.gp;
-    const int le = S.ulist[u];
-    bool fresh = false;
-    if (u != cur_u) {
-      fp4_context(a, S, le, ctid);
-      cur_u = u;
-      fresh = true;
-    }
-    if (!fp4_wait_stage(a, S, it)) {
-      fp4_drain(a, S, P, it);
-      return;
-    }
-    const int nt = S.ctx_n;
-    const uint8_t* stage = S.ring[it % kStages];
-    for (int c0 = 0; c0 < nt; c0 += kTokChunk) {
-      const int rt = min(kTokChunk, nt - c0);
-      const bool requant = fresh || nt > kTokChunk;
-      switch (rt) {
-        case 1: fp4_gemm1_chunk<1>(a, S, stage, h0, c0, rt, requant, ctid, warp, lane, xa, xs); break;
-        case 2: fp4_gemm1_chunk<2>(a, S, stage, h0, c0, rt, requant, ctid, warp, lane, xa, xs); break;
-        default: fp4_gemm1_chunk<4>(a, S, stage, h0, c0, rt, requant, ctid, warp, lane, xa, xs); break;
-      }
-    }
-    if (ctid == 0) {
-      __threadfence();
-      red_release_gpu_add(a.done + le, 1u);
-      if (it + kStages < n_items) {
-        fence_proxy_async_smem();
-        fp4_issue(a, S, P, it + kStages, pol);
-      }
-    }
-  }
-
-  cur_u = -1;
-  for (long long i = P.lo2; i < P.hi2; ++i, ++it) {
-    const int u = static_cast<int>(i / P.per_u2), rb = static_cast<int>(i % P.per_u2);
-    const int le = S.ulist[u];
-    const int m0 = rb * a.r2;
-    bool fresh = false;
-    if (u != cur_u) {
-      fp4_context(a, S, le, ctid);
-      if (!wait_counter(a, S, a.done + le, static_cast<uint32_t>(P.per_u1))) {
-        fp4_drain(a, S, P, it);
-        return;
-      }
-      cur_u = u;
-      fresh = true;
-    }
-    if (!fp4_wait_stage(a, S, it)) {
-      fp4_drain(a, S, P, it);
-      return;
-    }
-    const int nt = S.ctx_n;
-    const uint8_t* stage = S.ring[it % kStages];
-    for (int c0 = 0; c0 < nt; c0 += kTokChunk) {
-      const int rt = min(kTokChunk, nt - c0);
-      const bool requant = fresh || nt > kTokChunk;
-      switch (rt) {
-        case 1: fp4_gemm2_chunk<1>(a, S, stage, m0, c0, rt, requant, ctid, warp, lane, xa, xs); break;
-        case 2: fp4_gemm2_chunk<2>(a, S, stage, m0, c0, rt, requant, ctid, warp, lane, xa, xs); break;
-        default: fp4_gemm2_chunk<4>(a, S, stage, m0, c0, rt, requant, ctid, warp, lane, xa, xs); break;
-      }
-    }
-    if (ctid == 0) {
-      __threadfence();
-      red_release_gpu_add(a.done2, 1u);
-      const uint32_t old = atomicAdd(a.consumed + le, 1u);
-      if (old + 1u == static_cast<uint32_t>(P.per_u2)) {
-        atomicExch(a.done + le, 0u);
-        atomicExch(a.consumed + le, 0u);
-      }
-      if (it + kStages < n_items) {
-        fence_proxy_async_smem();
-        fp4_issue(a, S, P, it + kStages, pol);
-      }
-    }
-  }
-
-  // ---- phase 3: y[t, m] = bf16(sum over t's local picks, ascending, of w * o)
-  if (!wait_counter(a, S, a.done2, static_cast<uint32_t>(n2))) return;
-  const int chunks = a.H / 8;  // 8 columns (16 bytes of BF16) per thread item
-  const int per_cta = (chunks + G - 1) / G;
-  const int ch0 = c * per_cta, nch = max(0, min(chunks, ch0 + per_cta) - ch0);
-  for (int w = tid; w < a.M * nch; w += kThreads) {
-    const int tt = w / nch;
-    const int ch = ch0 + w % nch;
-    float acc[8];
+      for (int g = 0; g < 8; ++g) {  // 16 values: 8 packed bytes
+        const uint4 pk = src[g / 2];
+        const uint32_t w0 = (g & 1) ? pk.z : pk.x, w1 = (g & 1) ? pk.w : pk.y;
+        const uint32_t sh2 = nv_scale_h2(sw32[g / 4] >> (8 * (g & 3)));
+        uint32_t o[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
-    for (int r = 0; r < a.top_k; ++r) {
-      const int le = __ldg(a.ids + tt * a.top_k + r) - a.e0;
-      if (le < 0 || le >= a.L) continue;
-      const float wt = __ldg(a.tw + tt * a.top_k + r);
-      const uint4 o = __ldcg(reinterpret_cast<const uint4*>(a.obuf + static_cast<size_t>(tt * a.top_k + r) * a.H + 8 * ch));
-      const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+        for (int b = 0; b < 4; ++b) {
+          o[b] = hmul2_u32(e2m1x2_to_f16x2(w0 >> (8 * b)), sh2);
+          o[4 + b] = hmul2_u32(e2m1x2_to_f16x2(w1 >> (8 * b)), sh2);
+        }
+        // values 16g..16g+15 = 32 bytes: K half g / 4, 16-byte chunks 2(g % 4) and +1 of the row
+        uint8_t* base = S.A16[ab][g / 4] + row * 128;
+        const int c0 = 2 * (g & 3);
+        *reinterpret_cast<uint4*>(base + ((c0 ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(base + (((c0 + 1) ^ (row & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&S.afull[ab]);
+        mbar_arrive(&S.emptyA[s]);
+      }
+      ++k;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (TMEM lane quadrant = warp % 4)
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int etid = tid - 224;
+    NvCursor cur{P[0].lo, 1};
+    NvStep st;
+    int seg = 0;
+    float y[TOK];
+    while (cur.next(P, st)) {
+      if (!st.last) continue;
+      const int tb = seg & 1;
+      if (!mbar_wait(&S.accfull[tb], (seg >> 1) & 1, a.timeout_ns, &S.abort)) {
+        if (!S.abort) nv_error(a, S.abort, kErrRingWait);
+      }
+      nv_epi_bar();
+      if (S.abort) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + tb * TOK;
+#pragma unroll
+      for (int g = 0; g < TOK / 16; ++g) {
+        uint32_t v[16];
+        tmem_ld<16>(taddr + 16 * g, v);
+        tc_wait_ld();
+#pragma unroll
+        for (int t = 0; t < 16; ++t) y[16 * g + t] = __uint_as_float(v[t]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.tmemfree[tb]);
+      nv_end_segment<TOK>(a, S, P, st, y, row, etid);
+      ++seg;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, TOK == 16 ? 32 : 128);
+
+  // ---- scatter: y[t, m] = bf16(sum over t's local picks, ascending, of w * o)
+  const uint32_t tiles2 = static_cast<uint32_t>(U) * static_cast<uint32_t>(a.H / 128);
+  if (tid == 0 && !S.abort) nv_wait_ge(a, S.abort, a.sync + 2, tiles2);
+  __syncthreads();
+  if (!S.abort) {
+    const int chunks = a.H / 8;  // 8 columns (16 bytes of BF16) per thread item
+    const int per_cta = (chunks + G - 1) / G;
+    const int ch0 = c * per_cta, nch = max(0, min(chunks, ch0 + per_cta) - ch0);
+    for (int w = tid; w < a.M * nch; w += kNvThreads) {
+      const int tt = w / nch;
+      const int chn = ch0 + w % nch;
+      float acc[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
+      for (int r = 0; r < a.top_k; ++r) {
+        const int le = __ldg(a.ids + tt * a.top_k + r) - a.e0;
+        if (le < 0 || le >= a.L) continue;
+        const float wt = __ldg(a.tw + tt * a.top_k + r);
+        const uint4 o =
+            __ldcg(reinterpret_cast<const uint4*>(a.obuf + static_cast<size_t>(tt * a.top_k + r) * a.H + 8 * chn));
+        const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          acc[2 * k] = __fadd_rn(acc[2 * k], __fmul_rn(wt, __uint_as_float(ow[k] << 16)));
+          acc[2 * k + 1] = __fadd_rn(acc[2 * k + 1], __fmul_rn(wt, __uint_as_float(ow[k] & 0xFFFF0000u)));
+        }
+      }
+      uint4 out;
+      uint32_t* ow = reinterpret_cast<uint32_t*>(&out);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        acc[2 * k] = __fadd_rn(acc[2 * k], __fmul_rn(wt, __uint_as_float(ow[k] << 16)));
-        acc[2 * k + 1] = __fadd_rn(acc[2 * k + 1], __fmul_rn(wt, __uint_as_float(ow[k] & 0xFFFF0000u)));
+        const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * k]));
+        const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * k + 1]));
+        ow[k] = lo | (hi << 16);
       }
+      *reinterpret_cast<uint4*>(a.y + static_cast<size_t>(tt) * a.H + 8 * chn) = out;
     }
-    uint4 out;
-    uint32_t* ow = reinterpret_cast<uint32_t*>(&out);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * k]));
-      const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * k + 1]));
-      ow[k] = lo | (hi << 16);
-    }
-    *reinterpret_cast<uint4*>(a.y + static_cast<size_t>(tt) * a.H + 8 * ch) = out;
   }
   __syncthreads();
   if (tid == 0) {
-    // The last CTA past the phase-3 wait re-arms the global counters.
-    const uint32_t old = atomicAdd(a.passed3, 1u);
-    if (old + 1u == static_cast<uint32_t>(G)) {
-      atomicExch(a.done2, 0u);
-      atomicExch(a.passed3, 0u);
+    // The last CTA past the scatter wait re-arms its counters.
+    if (atomicAdd(a.sync + 3, 1u) + 1u == static_cast<uint32_t>(G)) {
+      atomicExch(a.sync + 2, 0u);
+      atomicExch(a.sync + 3, 0u);
     }
   }
 }
 
 // ---------------------------------------------------------------- host side
-static PhaseGeom fp4_geom(int K) {
-  PhaseGeom g;
-  g.ns = K / kFp4Slice;
-  int tpr = 32;
-  while (tpr < g.ns && tpr < kComputeThreads) tpr *= 2;
-  g.tpr = tpr;
-  g.rg = kComputeThreads / tpr;
-  g.nspt = (g.ns + tpr - 1) / tpr;
-  return g;
+static PFN_cuTensorMapEncodeTiled_v12000 nv_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
 }
 
-struct Fp4Workspace {
-  uint32_t *err, *done, *consumed, *done2, *passed3;
-  float* hbuf;
+// 2-D byte tensor [rows, cols] (row-major) with a box of box_rows x box_cols bytes.
+static bool nv_map(CUtensorMap* map, const void* base, unsigned long long rows, unsigned long long cols,
+                   unsigned box_cols, unsigned box_rows, bool swizzle128) {
+  auto fn = nv_encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct NvWorkspace {
+  uint32_t *err, *sync, *done, *hpassed, *cnt1, *cnt2;
+  uint8_t *ximg, *himg;
   __nv_bfloat16* obuf;
+  float* part;
+  int tok, Rp;
   size_t bytes;
 };
 
 static size_t a256(size_t v) { return (v + 255) & ~size_t(255); }
 
-static Fp4Workspace fp4_layout(void* base, int M, int H, int N, int L, int top_k) {
-  Fp4Workspace w;
+static NvWorkspace nv_layout(void* base, int M, int H, int N, int L, int top_k) {
+  NvWorkspace w;
   uint8_t* p = static_cast<uint8_t*>(base);
   size_t off = 0;
+  w.tok = M <= 16 ? 16 : kMaxTokens;
+  w.Rp = M * top_k > w.tok ? M * top_k : w.tok;  // at least one box of rows
   w.err = reinterpret_cast<uint32_t*>(p + off);
+  w.sync = w.err + 1;  // words 1..4 of the first 256 bytes
   off += 256;
   w.done = reinterpret_cast<uint32_t*>(p + off);
   off += a256(4 * static_cast<size_t>(L));
-  w.consumed = reinterpret_cast<uint32_t*>(p + off);
+  w.hpassed = reinterpret_cast<uint32_t*>(p + off);
   off += a256(4 * static_cast<size_t>(L));
-  w.done2 = reinterpret_cast<uint32_t*>(p + off);
-  w.passed3 = w.done2 + 1;
-  off += 256;
-  const size_t routes = static_cast<size_t>(M) * top_k;
-  w.hbuf = reinterpret_cast<float*>(p + off);
-  off += a256(4 * routes * N);
+  w.cnt1 = reinterpret_cast<uint32_t*>(p + off);
+  off += a256(4 * static_cast<size_t>(L) * (N / 64));
+  w.cnt2 = reinterpret_cast<uint32_t*>(p + off);
+  off += a256(4 * static_cast<size_t>(L) * (H / 128));
+  w.ximg = p + off;
+  off += a256(static_cast<size_t>(H / 64) * w.tok * 128);
+  w.himg = p + off;
+  off += a256(static_cast<size_t>(N / 64) * w.Rp * 128);
   w.obuf = reinterpret_cast<__nv_bfloat16*>(p + off);
-  off += a256(2 * routes * H);
+  off += a256(2 * static_cast<size_t>(M) * top_k * H);
+  w.part = reinterpret_cast<float*>(p + off);
+  off += a256(4 * static_cast<size_t>(2) * kFp8MaxCtas * 2 * w.tok * 128);
   w.bytes = off;
   return w;
 }
 
 size_t nvfp4_workspace_bytes(int M, int H, int N, int L, int top_k) {
-  return fp4_layout(nullptr, M, H, N, L, top_k).bytes;
+  return nv_layout(nullptr, M, H, N, L, top_k).bytes;
 }
 
-int routed_nvfp4(const void* x, const int32_t* ids, const float* weights, const uint8_t* w13, const uint8_t* s13,
-                 const uint8_t* w2, const uint8_t* s2, int M, int H, int N, int L, int e0, int top_k, float limit,
-                 void* y, void* workspace, size_t workspace_bytes, cudaStream_t st) {
-  const Fp4Workspace w = fp4_layout(workspace, M, H, N, L, top_k);
-  if (workspace == nullptr || workspace_bytes < w.bytes)
-    return set_last_error(FME_EWORKSPACE, "workspace of %zu bytes needed, %zu given", w.bytes, workspace_bytes);
-  Fp4Args a = {};
-  a.x = static_cast<const __nv_bfloat16*>(x);
-  a.ids = ids;
-  a.tw = weights;
-  a.w13 = w13;
-  a.s13 = s13;
-  a.w2 = w2;
-  a.s2 = s2;
-  a.y = static_cast<__nv_bfloat16*>(y);
-  a.err = w.err;
-  a.done = w.done;
-  a.consumed = w.consumed;
-  a.done2 = w.done2;
-  a.passed3 = w.passed3;
-  a.hbuf = w.hbuf;
-  a.obuf = w.obuf;
-  a.M = M;
-  a.H = H;
-  a.N = N;
-  a.L = L;
-  a.e0 = e0;
-  a.top_k = top_k;
-  a.limit = limit;
-  a.g1 = fp4_geom(H);
-  a.g2 = fp4_geom(N);
-  a.gp = kRowsPerGroup * a.g1.rg / 2;
-  a.r2 = kRowsPerGroup * a.g2.rg;
-  a.timeout_ns = wait_timeout_ns();
+template <int TOK>
+static int nv_launch(NvArgs& a, cudaStream_t st) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return set_last_error(FME_ECUDA, "cudaGetDevice failed");
   const int sms = device_sm_count(dev);
   if (sms <= 0) return set_last_error(FME_ECUDA, "cannot query the SM count");
-  if (!ensure_smem_attr(dev, reinterpret_cast<const void*>(nvfp4_moe_kernel), kFp4SmemBytes)) return FME_ECUDA;
+  const void* kern = reinterpret_cast<const void*>(nvfp4_tc_kernel<TOK>);
+  if (!ensure_smem_attr(dev, kern, nv_smem_bytes<TOK>())) return FME_ECUDA;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(sms);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kFp4SmemBytes;
+  cfg.gridDim = dim3(sms < kFp8MaxCtas ? sms : kFp8MaxCtas);
+  cfg.blockDim = dim3(kNvThreads);
+  cfg.dynamicSmemBytes = nv_smem_bytes<TOK>();
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t err = cudaLaunchKernelEx(&cfg, nvfp4_moe_kernel, a);
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, nvfp4_tc_kernel<TOK>, a);
   if (err != cudaSuccess) return set_last_error(FME_ECUDA, "nvfp4 kernel launch: %s", cudaGetErrorString(err));
   return FME_OK;
+}
+
+int routed_nvfp4(const void* x, const int32_t* ids, const float* weights, const uint8_t* w13, const uint8_t* s13,
+                 const uint8_t* w2, const uint8_t* s2, int M, int H, int N, int L, int e0, int top_k, float limit,
+                 void* y, void* workspace, size_t workspace_bytes, cudaStream_t st) {
+  const NvWorkspace w = nv_layout(workspace, M, H, N, L, top_k);
+  if (workspace == nullptr || workspace_bytes < w.bytes)
+    return set_last_error(FME_EWORKSPACE, "workspace of %zu bytes needed, %zu given", w.bytes, workspace_bytes);
+  NvArgs a;
+  memset(&a, 0, sizeof(a));
+  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.ids = ids;
+  a.tw = weights;
+  a.s13 = s13;
+  a.s2 = s2;
+  a.y = static_cast<__nv_bfloat16*>(y);
+  a.err = w.err;
+  a.sync = w.sync;
+  a.done = w.done;
+  a.hpassed = w.hpassed;
+  a.cnt1 = w.cnt1;
+  a.cnt2 = w.cnt2;
+  a.ximg = w.ximg;
+  a.himg = w.himg;
+  a.obuf = w.obuf;
+  a.part = w.part;
+  a.M = M;
+  a.H = H;
+  a.N = N;
+  a.L = L;
+  a.e0 = e0;
+  a.top_k = top_k;
+  a.Rp = w.Rp;
+  a.limit = limit;
+  a.timeout_ns = wait_timeout_ns();
+  if (!nv_map(&a.map13, w13, static_cast<unsigned long long>(L) * 2 * N, H / 2, 64, 64, false) ||
+      !nv_map(&a.map2, w2, static_cast<unsigned long long>(L) * H, N / 2, 64, 64, false) ||
+      !nv_map(&a.mapx, w.ximg, static_cast<unsigned long long>(H / 64) * w.tok, 128, 128, w.tok, true) ||
+      !nv_map(&a.maph, w.himg, static_cast<unsigned long long>(N / 64) * w.Rp, 128, 128, w.tok, true))
+    return set_last_error(FME_ECUDA, "cuTensorMapEncodeTiled failed or unavailable");
+  return w.tok == 16 ? nv_launch<16>(a, st) : nv_launch<kMaxTokens>(a, st);
 }
 
 }  // namespace fme
