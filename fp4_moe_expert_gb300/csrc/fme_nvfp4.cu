@@ -38,12 +38,17 @@
 
 namespace fme {
 
-constexpr int kNvThreads = 352;        // A TMA, MMA, B TMA, 4 dequant, 4 epilogue warps
+constexpr int kNvThreads = 480;        // A TMA, MMA, B TMA, 2 x 4 dequant, 4 epilogue warps
 constexpr int kNvRawBytes = 128 * 64;  // one K block: 128 rows x 64 packed bytes
+
+// Weight group scales run kNvScaleAhead of a dequant group's K blocks ahead of
+// it (8-byte cp.async per row into a small shared ring), so their global
+// latency never stalls it.
+constexpr int kNvScaleAhead = 4;
 
 template <int TOK>
 struct NvCfg {
-  static constexpr int kStages = TOK == 16 ? 10 : 5;
+  static constexpr int kStages = TOK == 16 ? 9 : 4;
   static constexpr int kBBytes = 2 * TOK * 128;  // two 64-value halves, TOK rows of 128 bytes each
 };
 
@@ -82,6 +87,7 @@ struct NvSmem {
   uint64_t emptyA[NvCfg<TOK>::kStages], emptyB[NvCfg<TOK>::kStages];
   uint64_t afull[2], afree[2], accfull[2], tmemfree[2], final_bar;
   float ysm[16][128];
+  uint2 sc[2][kNvScaleAhead][128];  // [dequant group] weight group scales of its next K blocks, by row
   unsigned long long tokmask[kMaxExperts];
   int16_t ulist[kMaxExperts];
   int16_t uidx[kMaxExperts];      // local expert -> unit
@@ -124,6 +130,61 @@ __device__ __forceinline__ void tma_load_2d_plain(void* dst, const void* tmap, i
       "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+// Eight E2M1 codes (code j in bits 4j..4j+3, sign in bit 3) -> four exact
+// f16x2 words with plain integer ops: the magnitude code (3 bits) selects the
+// FP16 high byte {0, 0.5, 1, 1.5, 2, 3, 4, 6} through a byte permute, and
+// the sign bit moves to bit 15 of its half.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&o)[4]) {
+  const uint32_t mag = w & 0x77777777u;
+  const uint32_t hb_lo = prmt(0x3E3C3800u, 0x46444240u, mag);
+  const uint32_t hb_hi = prmt(0x3E3C3800u, 0x46444240u, mag >> 16);
+  const uint32_t s_odd = w & 0x80808080u;          // signs of codes 1, 3, 5, 7 at byte msbs
+  const uint32_t s_even = (w << 4) & 0x80808080u;  // signs of codes 0, 2, 4, 6 at byte msbs
+  // f16x2 of codes (2i, 2i+1): bytes [0, H(2i), 0, H(2i+1)]
+  o[0] = prmt(hb_lo, 0u, 0x1404u) | (prmt(s_even, s_odd, 0x4000u) & 0x80008000u);
+  o[1] = prmt(hb_lo, 0u, 0x3424u) | (prmt(s_even, s_odd, 0x5010u) & 0x80008000u);
+  o[2] = prmt(hb_hi, 0u, 0x1404u) | (prmt(s_even, s_odd, 0x6020u) & 0x80008000u);
+  o[3] = prmt(hb_hi, 0u, 0x3424u) | (prmt(s_even, s_odd, 0x7030u) & 0x80008000u);
+}
+
+// Bounded wait that polls with the non-blocking test_wait: for the per-K-block
+// hand-offs between the dequant warps and the MMA issuer, where a suspended
+// try_wait would add its wake-up latency to every K block.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, uint64_t limit_ns, const volatile int* abort) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_test(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // UE4M3 scale byte of a group: e4m3(amax / 6), saturating ("nvfp4-megamoe-kernel
@@ -605,47 +666,81 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
       tc_commit(&S.final_bar);
       if (!mbar_wait(&S.final_bar, 0, a.timeout_ns, nullptr)) atomicOr(a.err, kErrDrain);
     }
-  } else if (warp < 7) {
+  } else if (warp < 11) {
     // ------------------------------------------------------------ dequant (one weight row per thread)
-    const int row = tid - 96;
+    // Two groups of four warps take the even and the odd K blocks: each K
+    // block is a chain of latencies (shared loads, converts, stores, proxy
+    // fence), and two chains in flight double the throughput.
+    const int dg = (warp - 3) >> 2;
+    const int row = tid - 96 - 128 * dg;
+    // Address of this row's 8 scale bytes for K block st.
+    auto scale_src = [&](const NvStep& q) -> const uint8_t* {
+      const int le = S.ulist[q.u];
+      if (q.phase == 1) {
+        const int grow = le * 2 * a.N + (row < 64 ? 64 * q.T + row : a.N + 64 * q.T + row - 64);
+        return a.s13 + static_cast<size_t>(grow) * (a.H / 16) + 8 * q.kb;
+      }
+      return a.s2 + (static_cast<size_t>(le) * a.H + 128 * q.T + row) * (a.N / 16) + 8 * q.kb;
+    };
+    // Slots hold this group's K blocks n .. n + kNvScaleAhead - 2; a refill
+    // goes to the slot read one iteration earlier (its value already consumed).
+    NvCursor ahead{P[0].lo, 1};
+    NvStep qa;
+    int ka = 0;
+    auto next_own = [&](NvStep& q) -> bool {
+      while (ahead.next(P, q)) {
+        if (((ka++) & 1) == dg) return true;
+      }
+      return false;
+    };
+    for (int j = 0; j < kNvScaleAhead - 1; ++j) {
+      if (next_own(qa)) cp_async8(&S.sc[dg][j][row], scale_src(qa));
+      cp_async_commit();
+    }
     NvCursor cur{P[0].lo, 1};
     NvStep st;
-    int k = 0;
+    int k = 0, n = 0;
     while (cur.next(P, st)) {
-      const int s = k % kS, ab = k & 1;
-      // Group scales of this row's 128 values (8 bytes), loaded before the waits.
-      const int le = S.ulist[st.u];
-      const uint8_t* sp;
-      if (st.phase == 1) {
-        const int grow = le * 2 * a.N + (row < 64 ? 64 * st.T + row : a.N + 64 * st.T + row - 64);
-        sp = a.s13 + static_cast<size_t>(grow) * (a.H / 16) + 8 * st.kb;
-      } else {
-        sp = a.s2 + (static_cast<size_t>(le) * a.H + 128 * st.T + row) * (a.N / 16) + 8 * st.kb;
+      if ((k & 1) != dg) {
+        ++k;
+        continue;
       }
-      const uint2 sw = __ldg(reinterpret_cast<const uint2*>(sp));
+      const int s = k % kS, ab = dg;
+      cp_async_wait<kNvScaleAhead - 2>();  // this row's scales of K block k have landed
+      const uint2 sw = S.sc[dg][n % kNvScaleAhead][row];
+      if (next_own(qa)) cp_async8(&S.sc[dg][(n + kNvScaleAhead - 1) % kNvScaleAhead][row], scale_src(qa));
+      cp_async_commit();
       if (!mbar_wait(&S.fullA[s], (k / kS) & 1, a.timeout_ns, &S.abort) ||
           (k >= 2 && !mbar_wait(&S.afree[ab], ((k >> 1) - 1) & 1, a.timeout_ns, &S.abort))) {
         if (!S.abort) nv_error(a, S.abort, kErrRingWait);
         break;
       }
+      // The row's 64 packed bytes as four 16-byte chunks, read in an order
+      // rotated by row / 2 so a warp's reads spread over all banks.
       const uint4* src = reinterpret_cast<const uint4*>(S.R[s] + row * 64);
-      const uint32_t sw32[2] = {sw.x, sw.y};
+      const int rot = (row >> 1) & 3;
+      uint4 pk[4];
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {  // 16 values: 8 packed bytes
-        const uint4 pk = src[g / 2];
-        const uint32_t w0 = (g & 1) ? pk.z : pk.x, w1 = (g & 1) ? pk.w : pk.y;
-        const uint32_t sh2 = nv_scale_h2(sw32[g / 4] >> (8 * (g & 3)));
-        uint32_t o[8];
+      for (int j = 0; j < 4; ++j) pk[j] = src[(j + rot) & 3];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          o[b] = hmul2_u32(e2m1x2_to_f16x2(w0 >> (8 * b)), sh2);
-          o[4 + b] = hmul2_u32(e2m1x2_to_f16x2(w1 >> (8 * b)), sh2);
+      for (int j = 0; j < 4; ++j) {
+        const int ch = (j + rot) & 3;  // chunk ch: values 32ch .. 32ch + 31, groups 2ch and 2ch + 1
+        const uint32_t words[4] = {pk[j].x, pk[j].y, pk[j].z, pk[j].w};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int g = 2 * ch + h;  // group of 16 values
+          const uint32_t sh2 = nv_scale_h2((g < 4 ? sw.x : sw.y) >> (8 * (g & 3)));
+          uint32_t o[8];
+          e2m1x8_to_f16x2x4(words[2 * h], *reinterpret_cast<uint32_t(*)[4]>(&o[0]));
+          e2m1x8_to_f16x2x4(words[2 * h + 1], *reinterpret_cast<uint32_t(*)[4]>(&o[4]));
+#pragma unroll
+          for (int b = 0; b < 8; ++b) o[b] = hmul2_u32(o[b], sh2);
+          // values 16g..16g+15 = 32 bytes: K half g / 4, 16-byte chunks 2(g % 4) and +1 of the row
+          uint8_t* base = S.A16[ab][g >> 2] + row * 128;
+          const int c0 = 2 * (g & 3);
+          *reinterpret_cast<uint4*>(base + ((c0 ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(base + (((c0 + 1) ^ (row & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
         }
-        // values 16g..16g+15 = 32 bytes: K half g / 4, 16-byte chunks 2(g % 4) and +1 of the row
-        uint8_t* base = S.A16[ab][g / 4] + row * 128;
-        const int c0 = 2 * (g & 3);
-        *reinterpret_cast<uint4*>(base + ((c0 ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(base + (((c0 + 1) ^ (row & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -654,12 +749,14 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
         mbar_arrive(&S.emptyA[s]);
       }
       ++k;
+      ++n;
     }
+    cp_async_wait<0>();
   } else {
     // ------------------------------------------------------------ epilogue (TMEM lane quadrant = warp % 4)
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
-    const int etid = tid - 224;
+    const int etid = tid - 352;
     NvCursor cur{P[0].lo, 1};
     NvStep st;
     int seg = 0;
