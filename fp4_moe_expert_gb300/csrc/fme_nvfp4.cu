@@ -48,7 +48,10 @@ constexpr int kNvScaleAhead = 4;
 
 template <int TOK>
 struct NvCfg {
-  static constexpr int kStages = TOK == 16 ? 9 : 4;
+  static constexpr int kStages = TOK == 16 ? 7 : 4;
+  // FP16 weight buffers: the dequant may run kAbuf - 1 K blocks ahead of the
+  // MMAs that read them, which hides the tensor-core completion latency.
+  static constexpr int kAbuf = TOK == 16 ? 3 : 2;
   static constexpr int kBBytes = 2 * TOK * 128;  // two 64-value halves, TOK rows of 128 bytes each
 };
 
@@ -80,12 +83,12 @@ struct NvArgs {
 
 template <int TOK>
 struct NvSmem {
-  uint8_t A16[2][2][128 * 128];  // FP16 weights [buffer][K half][128 rows x 128 B], 128-byte swizzle
+  uint8_t A16[NvCfg<TOK>::kAbuf][2][128 * 128];  // FP16 weights [buffer][K half][128 rows x 128 B], swizzled
   uint8_t B[NvCfg<TOK>::kStages][NvCfg<TOK>::kBBytes];
   uint8_t R[NvCfg<TOK>::kStages][kNvRawBytes];
   uint64_t fullA[NvCfg<TOK>::kStages], fullB[NvCfg<TOK>::kStages];
   uint64_t emptyA[NvCfg<TOK>::kStages], emptyB[NvCfg<TOK>::kStages];
-  uint64_t afull[2], afree[2], accfull[2], tmemfree[2], final_bar;
+  uint64_t afull[NvCfg<TOK>::kAbuf], afree[NvCfg<TOK>::kAbuf], accfull[2], tmemfree[2], final_bar;
   float ysm[16][128];
   uint2 sc[2][kNvScaleAhead][128];  // [dequant group] weight group scales of its next K blocks, by row
   unsigned long long tokmask[kMaxExperts];
@@ -443,9 +446,11 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
       mbar_init(&S.emptyA[s], 4);
       mbar_init(&S.emptyB[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::kAbuf; ++b) {
       mbar_init(&S.afull[b], 4);
       mbar_init(&S.afree[b], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(&S.accfull[b], 1);
       mbar_init(&S.tmemfree[b], 4);
     }
@@ -638,8 +643,8 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
       NvStep st;
       int k = 0, seg = 0;
       while (cur.next(P, st)) {
-        const int s = k % kS, ab = k & 1, tb = seg & 1;
-        if (!mbar_wait(&S.afull[ab], (k >> 1) & 1, a.timeout_ns, &S.abort) ||
+        const int s = k % kS, ab = k % C::kAbuf, tb = seg & 1;
+        if (!mbar_wait(&S.afull[ab], (k / C::kAbuf) & 1, a.timeout_ns, &S.abort) ||
             !mbar_wait(&S.fullB[s], (k / kS) & 1, a.timeout_ns, &S.abort) ||
             (st.first && seg >= 2 && !mbar_wait(&S.tmemfree[tb], ((seg >> 1) - 1) & 1, a.timeout_ns, &S.abort))) {
           if (!S.abort) nv_error(a, S.abort, kErrRingWait);
@@ -705,13 +710,13 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
         ++k;
         continue;
       }
-      const int s = k % kS, ab = dg;
+      const int s = k % kS, ab = k % C::kAbuf;
       cp_async_wait<kNvScaleAhead - 2>();  // this row's scales of K block k have landed
       const uint2 sw = S.sc[dg][n % kNvScaleAhead][row];
       if (next_own(qa)) cp_async8(&S.sc[dg][(n + kNvScaleAhead - 1) % kNvScaleAhead][row], scale_src(qa));
       cp_async_commit();
       if (!mbar_wait(&S.fullA[s], (k / kS) & 1, a.timeout_ns, &S.abort) ||
-          (k >= 2 && !mbar_wait(&S.afree[ab], ((k >> 1) - 1) & 1, a.timeout_ns, &S.abort))) {
+          (k >= C::kAbuf && !mbar_wait(&S.afree[ab], ((k / C::kAbuf) - 1) & 1, a.timeout_ns, &S.abort))) {
         if (!S.abort) nv_error(a, S.abort, kErrRingWait);
         break;
       }
