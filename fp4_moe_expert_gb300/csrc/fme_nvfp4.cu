@@ -48,10 +48,12 @@ constexpr int kNvScaleAhead = 4;
 
 template <int TOK>
 struct NvCfg {
-  static constexpr int kStages = TOK == 16 ? 7 : 4;
-  // FP16 weight buffers: the dequant may run kAbuf - 1 K blocks ahead of the
-  // MMAs that read them, which hides the tensor-core completion latency.
-  static constexpr int kAbuf = TOK == 16 ? 3 : 2;
+  // Packed-weight ring: the TMA latency under a full weight stream is 2-3 us,
+  // so it holds as many K blocks as shared memory allows; the activation
+  // operand comes from L2 and needs only a short ring of its own.
+  static constexpr int kStages = TOK == 16 ? 13 : 9;
+  static constexpr int kBStages = 3;
+  static constexpr int kAbuf = 2;  // FP16 weight buffers
   static constexpr int kBBytes = 2 * TOK * 128;  // two 64-value halves, TOK rows of 128 bytes each
 };
 
@@ -84,10 +86,10 @@ struct NvArgs {
 template <int TOK>
 struct NvSmem {
   uint8_t A16[NvCfg<TOK>::kAbuf][2][128 * 128];  // FP16 weights [buffer][K half][128 rows x 128 B], swizzled
-  uint8_t B[NvCfg<TOK>::kStages][NvCfg<TOK>::kBBytes];
+  uint8_t B[NvCfg<TOK>::kBStages][NvCfg<TOK>::kBBytes];
   uint8_t R[NvCfg<TOK>::kStages][kNvRawBytes];
-  uint64_t fullA[NvCfg<TOK>::kStages], fullB[NvCfg<TOK>::kStages];
-  uint64_t emptyA[NvCfg<TOK>::kStages], emptyB[NvCfg<TOK>::kStages];
+  uint64_t fullA[NvCfg<TOK>::kStages], emptyA[NvCfg<TOK>::kStages];
+  uint64_t fullB[NvCfg<TOK>::kBStages], emptyB[NvCfg<TOK>::kBStages];
   uint64_t afull[NvCfg<TOK>::kAbuf], afree[NvCfg<TOK>::kAbuf], accfull[2], tmemfree[2], final_bar;
   float ysm[16][128];
   uint2 sc[2][kNvScaleAhead][128];  // [dequant group] weight group scales of its next K blocks, by row
@@ -140,23 +142,6 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
   return d;
 }
-// Eight E2M1 codes (code j in bits 4j..4j+3, sign in bit 3) -> four exact
-// f16x2 words with plain integer ops: the magnitude code (3 bits) selects the
-// FP16 high byte {0, 0.5, 1, 1.5, 2, 3, 4, 6} through a byte permute, and
-// the sign bit moves to bit 15 of its half.
-__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&o)[4]) {
-  const uint32_t mag = w & 0x77777777u;
-  const uint32_t hb_lo = prmt(0x3E3C3800u, 0x46444240u, mag);
-  const uint32_t hb_hi = prmt(0x3E3C3800u, 0x46444240u, mag >> 16);
-  const uint32_t s_odd = w & 0x80808080u;          // signs of codes 1, 3, 5, 7 at byte msbs
-  const uint32_t s_even = (w << 4) & 0x80808080u;  // signs of codes 0, 2, 4, 6 at byte msbs
-  // f16x2 of codes (2i, 2i+1): bytes [0, H(2i), 0, H(2i+1)]
-  o[0] = prmt(hb_lo, 0u, 0x1404u) | (prmt(s_even, s_odd, 0x4000u) & 0x80008000u);
-  o[1] = prmt(hb_lo, 0u, 0x3424u) | (prmt(s_even, s_odd, 0x5010u) & 0x80008000u);
-  o[2] = prmt(hb_hi, 0u, 0x1404u) | (prmt(s_even, s_odd, 0x6020u) & 0x80008000u);
-  o[3] = prmt(hb_hi, 0u, 0x3424u) | (prmt(s_even, s_odd, 0x7030u) & 0x80008000u);
-}
-
 // Bounded wait that polls with the non-blocking test_wait: for the per-K-block
 // hand-offs between the dequant warps and the MMA issuer, where a suspended
 // try_wait would add its wake-up latency to every K block.
@@ -433,7 +418,7 @@ __device__ bool nv_wait_ge(const NvArgs& a, volatile int& abort, const uint32_t*
 template <int TOK>
 __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_constant__ NvArgs a) {
   using C = NvCfg<TOK>;
-  constexpr int kS = C::kStages;
+  constexpr int kS = C::kStages, kSB = C::kBStages;
   extern __shared__ uint8_t smem_raw[];
   NvSmem<TOK>& S = *reinterpret_cast<NvSmem<TOK>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -442,8 +427,10 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
   if (tid == 0) {
     for (int s = 0; s < kS; ++s) {
       mbar_init(&S.fullA[s], 1);
-      mbar_init(&S.fullB[s], 1);
       mbar_init(&S.emptyA[s], 4);
+    }
+    for (int s = 0; s < kSB; ++s) {
+      mbar_init(&S.fullB[s], 1);
       mbar_init(&S.emptyB[s], 1);
     }
     for (int b = 0; b < C::kAbuf; ++b) {
@@ -603,8 +590,8 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
       NvStep st;
       int k = 0, cur_u = -1;
       while (ok && cur.next(P, st)) {
-        const int s = k % kS;
-        if (k >= kS && !mbar_wait(&S.emptyB[s], ((k / kS) - 1) & 1, a.timeout_ns, &S.abort)) {
+        const int s = k % kSB;
+        if (k >= kSB && !mbar_wait(&S.emptyB[s], ((k / kSB) - 1) & 1, a.timeout_ns, &S.abort)) {
           if (!S.abort) nv_error(a, S.abort, kErrRingWait);
           break;
         }
@@ -632,8 +619,8 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
         }
         ++k;
       }
-      for (int kk = max(0, k - kS); kk < k; ++kk)
-        if (!mbar_wait(&S.fullB[kk % kS], (kk / kS) & 1, a.timeout_ns, nullptr)) atomicOr(a.err, kErrDrain);
+      for (int kk = max(0, k - kSB); kk < k; ++kk)
+        if (!mbar_wait(&S.fullB[kk % kSB], (kk / kSB) & 1, a.timeout_ns, nullptr)) atomicOr(a.err, kErrDrain);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -643,25 +630,28 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
       NvStep st;
       int k = 0, seg = 0;
       while (cur.next(P, st)) {
-        const int s = k % kS, ab = k % C::kAbuf, tb = seg & 1;
+        const int sb = k % kSB, ab = k % C::kAbuf, tb = seg & 1;
         if (!mbar_wait(&S.afull[ab], (k / C::kAbuf) & 1, a.timeout_ns, &S.abort) ||
-            !mbar_wait(&S.fullB[s], (k / kS) & 1, a.timeout_ns, &S.abort) ||
+            !mbar_wait(&S.fullB[sb], (k / kSB) & 1, a.timeout_ns, &S.abort) ||
             (st.first && seg >= 2 && !mbar_wait(&S.tmemfree[tb], ((seg >> 1) - 1) & 1, a.timeout_ns, &S.abort))) {
           if (!S.abort) nv_error(a, S.abort, kErrRingWait);
           break;
         }
         tc_fence_after();
-        const uint32_t abase = smem_u32(S.A16[ab][0]);
-        const uint32_t bbase = smem_u32(S.B[s]);
+        // Descriptors of the first K step; later steps add their byte offset
+        // in 16-byte units to the start-address field (shared addresses stay
+        // far below 256 KB, so the 14-bit field never carries).
+        const uint64_t adesc = sw128_desc(smem_u32(S.A16[ab][0]));
+        const uint64_t bdesc = sw128_desc(smem_u32(S.B[sb]));
+        const uint32_t dtm = tmem + tb * TOK;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t ao = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
-          const uint32_t bo = (kk >> 2) * (TOK * 128) + (kk & 3) * 32;
-          tc_mma_f16(tmem + tb * TOK, sw128_desc(abase + ao), sw128_desc(bbase + bo), idesc,
-                     (st.first && kk == 0) ? 0u : 1u);
+          const uint32_t ao = ((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4;
+          const uint32_t bo = ((kk >> 2) * (TOK * 128) + (kk & 3) * 32) >> 4;
+          tc_mma_f16(dtm, adesc + ao, bdesc + bo, idesc, (st.first && kk == 0) ? 0u : 1u);
         }
         tc_commit(&S.afree[ab]);
-        tc_commit(&S.emptyB[s]);
+        tc_commit(&S.emptyB[sb]);
         if (st.last) {
           tc_commit(&S.accfull[tb]);
           ++seg;
@@ -736,8 +726,11 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
           const int g = 2 * ch + h;  // group of 16 values
           const uint32_t sh2 = nv_scale_h2((g < 4 ? sw.x : sw.y) >> (8 * (g & 3)));
           uint32_t o[8];
-          e2m1x8_to_f16x2x4(words[2 * h], *reinterpret_cast<uint32_t(*)[4]>(&o[0]));
-          e2m1x8_to_f16x2x4(words[2 * h + 1], *reinterpret_cast<uint32_t(*)[4]>(&o[4]));
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            o[b] = e2m1x2_to_f16x2(words[2 * h] >> (8 * b));
+            o[4 + b] = e2m1x2_to_f16x2(words[2 * h + 1] >> (8 * b));
+          }
 #pragma unroll
           for (int b = 0; b < 8; ++b) o[b] = hmul2_u32(o[b], sh2);
           // values 16g..16g+15 = 32 bytes: K half g / 4, 16-byte chunks 2(g % 4) and +1 of the row
