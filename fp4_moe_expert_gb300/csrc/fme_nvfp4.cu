@@ -46,6 +46,13 @@ constexpr int kNvRawBytes = 128 * 64;  // one K block: 128 rows x 64 packed byte
 // latency never stalls it.
 constexpr int kNvScaleAhead = 4;
 
+// Tensor memory: the accumulators (two buffers of TOK columns) sit in
+// columns 0 .. 127 and the FP16 weight buffers, 64 columns each (128 rows x
+// 128 K values), from column 128 on. One CTA per SM (shared memory), so the
+// CTA takes all 512 columns.
+constexpr uint32_t kNvTmemCols = 512;
+__device__ __forceinline__ uint32_t nv_acol(int ab) { return 128u + 64u * static_cast<uint32_t>(ab); }
+
 template <int TOK>
 struct NvCfg {
   // Packed-weight ring: the TMA latency under a full weight stream is 2-3 us,
@@ -53,7 +60,7 @@ struct NvCfg {
   // operand comes from L2 and needs only a short ring of its own.
   static constexpr int kStages = TOK == 16 ? 13 : 9;
   static constexpr int kBStages = 3;
-  static constexpr int kAbuf = 2;  // FP16 weight buffers
+  static constexpr int kAbuf = 4;  // FP16 weight buffers in tensor memory
   static constexpr int kBBytes = 2 * TOK * 128;  // two 64-value halves, TOK rows of 128 bytes each
 };
 
@@ -85,7 +92,6 @@ struct NvArgs {
 
 template <int TOK>
 struct NvSmem {
-  uint8_t A16[NvCfg<TOK>::kAbuf][2][128 * 128];  // FP16 weights [buffer][K half][128 rows x 128 B], swizzled
   uint8_t B[NvCfg<TOK>::kBStages][NvCfg<TOK>::kBBytes];
   uint8_t R[NvCfg<TOK>::kStages][kNvRawBytes];
   uint64_t fullA[NvCfg<TOK>::kStages], emptyA[NvCfg<TOK>::kStages];
@@ -109,6 +115,14 @@ constexpr size_t nv_smem_bytes() {
   return sizeof(NvSmem<TOK>) + 1024;
 }
 static_assert(nv_smem_bytes<16>() <= 232448 && nv_smem_bytes<64>() <= 232448, "shared memory per CTA");
+static_assert(128 + 64 * NvCfg<16>::kAbuf <= kNvTmemCols && 128 + 64 * NvCfg<64>::kAbuf <= kNvTmemCols,
+              "tensor memory columns");
+// Swizzled TMA destinations: the activation ring (128-byte swizzle) and the
+// packed-weight ring (64-byte swizzle) start on 1024-byte boundaries.
+static_assert(offsetof(NvSmem<16>, R) % 1024 == 0 && offsetof(NvSmem<64>, R) % 1024 == 0, "ring alignment");
+// A second CTA on the SM would wait in its TMEM allocation while the first
+// may wait on it through the cross-CTA counters: shared memory keeps it out.
+static_assert(nv_smem_bytes<16>() > 233472 / 2 && nv_smem_bytes<64>() > 233472 / 2, "one CTA per SM");
 
 __device__ __forceinline__ void nv_epi_bar() { named_bar_sync(1, 128); }
 
@@ -119,11 +133,14 @@ __device__ __forceinline__ void nv_error(const NvArgs& a, volatile int& abort, u
 
 // tcgen05.mma kind::f16 (both operands F16, K-major, FP32 accumulation): the
 // instruction descriptor has the fields of kind::f8f6f4, format code 0 = F16.
-__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                           uint32_t accumulate) {
+// D (TMEM) += A (TMEM, 128 lanes = rows, two FP16 values of K per column)
+// x B (shared memory descriptor), FP16 inputs, FP32 accumulation.
+__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
   asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -450,7 +467,7 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
     prefetch_tmap(&a.maph);
   }
   if (warp == 1) {
-    tmem_alloc(&S.tmem_base, TOK == 16 ? 32 : 128);
+    tmem_alloc(&S.tmem_base, kNvTmemCols);
     tmem_relinquish();
   }
   for (int e = tid; e < a.L; e += kNvThreads) S.tokmask[e] = 0ull;
@@ -638,17 +655,17 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
           break;
         }
         tc_fence_after();
-        // Descriptors of the first K step; later steps add their byte offset
-        // in 16-byte units to the start-address field (shared addresses stay
-        // far below 256 KB, so the 14-bit field never carries).
-        const uint64_t adesc = sw128_desc(smem_u32(S.A16[ab][0]));
+        // A (FP16 weights) comes from tensor memory: K step kk is columns
+        // 8kk .. 8kk + 7 of the buffer. B's descriptor of the first K step
+        // gets later steps' byte offsets added in 16-byte units to its
+        // start-address field (shared addresses stay far below 256 KB, so the
+        // 14-bit field never carries).
         const uint64_t bdesc = sw128_desc(smem_u32(S.B[sb]));
         const uint32_t dtm = tmem + tb * TOK;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t ao = ((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4;
           const uint32_t bo = ((kk >> 2) * (TOK * 128) + (kk & 3) * 32) >> 4;
-          tc_mma_f16(dtm, adesc + ao, bdesc + bo, idesc, (st.first && kk == 0) ? 0u : 1u);
+          tc_mma_f16_ts(dtm, tmem + nv_acol(ab) + 8 * kk, bdesc + bo, idesc, (st.first && kk == 0) ? 0u : 1u);
         }
         tc_commit(&S.afree[ab]);
         tc_commit(&S.emptyB[sb]);
@@ -664,10 +681,12 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
   } else if (warp < 11) {
     // ------------------------------------------------------------ dequant (one weight row per thread)
     // Two groups of four warps take the even and the odd K blocks: each K
-    // block is a chain of latencies (shared loads, converts, stores, proxy
-    // fence), and two chains in flight double the throughput.
+    // block is a chain of latencies (shared loads, converts, TMEM stores),
+    // and two chains in flight double the throughput. A warp may only reach
+    // the TMEM lane quadrant warp % 4, so that quadrant's rows are its own.
     const int dg = (warp - 3) >> 2;
-    const int row = tid - 96 - 128 * dg;
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t tq = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     // Address of this row's 8 scale bytes for K block st.
     auto scale_src = [&](const NvStep& q) -> const uint8_t* {
       const int le = S.ulist[q.u];
@@ -710,20 +729,22 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
         if (!S.abort) nv_error(a, S.abort, kErrRingWait);
         break;
       }
-      // The row's 64 packed bytes as four 16-byte chunks, read in an order
-      // rotated by row / 2 so a warp's reads spread over all banks.
+      tc_fence_after();
+      // The row's 64 packed bytes as four 16-byte chunks. The 64-byte TMA
+      // swizzle put chunk ch of row r at chunk ch ^ ((r / 2) % 4) of the
+      // row, so the warp's reads of one chunk spread over all banks while the
+      // chunk, and with it the TMEM column, stays the same across the warp.
       const uint4* src = reinterpret_cast<const uint4*>(S.R[s] + row * 64);
-      const int rot = (row >> 1) & 3;
+      const int sw64 = (row >> 1) & 3;
       uint4 pk[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) pk[j] = src[(j + rot) & 3];
+      for (int ch = 0; ch < 4; ++ch) pk[ch] = src[ch ^ sw64];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int ch = (j + rot) & 3;  // chunk ch: values 32ch .. 32ch + 31, groups 2ch and 2ch + 1
-        const uint32_t words[4] = {pk[j].x, pk[j].y, pk[j].z, pk[j].w};
+      for (int ch = 0; ch < 4; ++ch) {  // chunk ch: values 32ch .. 32ch + 31, groups 2ch and 2ch + 1
+        const uint32_t words[4] = {pk[ch].x, pk[ch].y, pk[ch].z, pk[ch].w};
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int g = 2 * ch + h;  // group of 16 values
+          const int g = 2 * ch + h;  // group of 16 values = TMEM columns 8g .. 8g + 7
           const uint32_t sh2 = nv_scale_h2((g < 4 ? sw.x : sw.y) >> (8 * (g & 3)));
           uint32_t o[8];
 #pragma unroll
@@ -733,14 +754,11 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
           }
 #pragma unroll
           for (int b = 0; b < 8; ++b) o[b] = hmul2_u32(o[b], sh2);
-          // values 16g..16g+15 = 32 bytes: K half g / 4, 16-byte chunks 2(g % 4) and +1 of the row
-          uint8_t* base = S.A16[ab][g >> 2] + row * 128;
-          const int c0 = 2 * (g & 3);
-          *reinterpret_cast<uint4*>(base + ((c0 ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(base + (((c0 + 1) ^ (row & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          tmem_st8(tq + nv_acol(ab) + 8 * g, o);
         }
       }
-      fence_proxy_async_smem();
+      tc_wait_st();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&S.afull[ab]);
@@ -788,7 +806,7 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, TOK == 16 ? 32 : 128);
+  if (warp == 1) tmem_dealloc(tmem, kNvTmemCols);
 
   // ---- scatter: y[t, m] = bf16(sum over t's local picks, ascending, of w * o)
   const uint32_t tiles2 = static_cast<uint32_t>(U) * static_cast<uint32_t>(a.H / 128);
@@ -856,7 +874,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 nv_encode_fn() {
 
 // 2-D byte tensor [rows, cols] (row-major) with a box of box_rows x box_cols bytes.
 static bool nv_map(CUtensorMap* map, const void* base, unsigned long long rows, unsigned long long cols,
-                   unsigned box_cols, unsigned box_rows, bool swizzle128) {
+                   unsigned box_cols, unsigned box_rows, CUtensorMapSwizzle swizzle) {
   auto fn = nv_encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -864,7 +882,7 @@ static bool nv_map(CUtensorMap* map, const void* base, unsigned long long rows, 
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -968,10 +986,12 @@ int routed_nvfp4(const void* x, const int32_t* ids, const float* weights, const 
   a.Rp = w.Rp;
   a.limit = limit;
   a.timeout_ns = wait_timeout_ns();
-  if (!nv_map(&a.map13, w13, static_cast<unsigned long long>(L) * 2 * N, H / 2, 64, 64, false) ||
-      !nv_map(&a.map2, w2, static_cast<unsigned long long>(L) * H, N / 2, 64, 64, false) ||
-      !nv_map(&a.mapx, w.ximg, static_cast<unsigned long long>(H / 64) * w.tok, 128, 128, w.tok, true) ||
-      !nv_map(&a.maph, w.himg, static_cast<unsigned long long>(N / 64) * w.Rp, 128, 128, w.tok, true))
+  if (!nv_map(&a.map13, w13, static_cast<unsigned long long>(L) * 2 * N, H / 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !nv_map(&a.map2, w2, static_cast<unsigned long long>(L) * H, N / 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !nv_map(&a.mapx, w.ximg, static_cast<unsigned long long>(H / 64) * w.tok, 128, 128, w.tok,
+              CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !nv_map(&a.maph, w.himg, static_cast<unsigned long long>(N / 64) * w.Rp, 128, 128, w.tok,
+              CU_TENSOR_MAP_SWIZZLE_128B))
     return set_last_error(FME_ECUDA, "cuTensorMapEncodeTiled failed or unavailable");
   return w.tok == 16 ? nv_launch<16>(a, st) : nv_launch<kMaxTokens>(a, st);
 }
