@@ -13,9 +13,10 @@
 //   into FP16 and multiplied on `tcgen05.mma kind::f16` with FP32
 //   accumulation: each product is exact and only the FP32 sums round, like
 //   the pages' block-scaled product.
-// * Weights: TMA streams the packed E2M1 rows (no swizzle) into a ring; four
-//   dequant warps expand each 128-row x 128-value K block with its group
-//   scales into an FP16 operand in the 128-byte-swizzled K-major layout.
+// * Weights: TMA streams the packed E2M1 rows, 128 bytes (256 values) of
+//   each of 128 rows per K block, into a ring; dequant warps expand each
+//   block with its group scales into FP16 and store it to tensor memory,
+//   where the MMA reads it as the A operand.
 // * Activations: at start every CTA quantises a share of x into an FP16
 //   image in the workspace (all tokens, 16 or 64 rows); the GEMM1 epilogue
 //   quantises each slot's h (groups of 16 lie inside one 64-row tile) into a
@@ -38,37 +39,38 @@
 
 namespace fme {
 
-constexpr int kNvThreads = 480;        // A TMA, MMA, B TMA, 2 x 4 dequant, 4 epilogue warps
-constexpr int kNvRawBytes = 128 * 64;  // one K block: 128 rows x 64 packed bytes
+constexpr int kNvThreads = 480;         // A TMA, MMA, B TMA, 2 x 4 dequant, 4 epilogue warps
+constexpr int kNvKB = 256;              // K values per K block
+constexpr int kNvRawBytes = 128 * 128;  // one K block: 128 rows x 128 packed bytes
 
 // Weight group scales run kNvScaleAhead of a dequant group's K blocks ahead of
-// it (8-byte cp.async per row into a small shared ring), so their global
+// it (two 8-byte cp.async per row into a small shared ring), so their global
 // latency never stalls it.
 constexpr int kNvScaleAhead = 4;
 
 // Tensor memory: the accumulators (two buffers of TOK columns) sit in
-// columns 0 .. 127 and the FP16 weight buffers, 64 columns each (128 rows x
-// 128 K values), from column 128 on. One CTA per SM (shared memory), so the
+// columns 0 .. 127 and the FP16 weight buffers, 128 columns each (128 rows x
+// 256 K values), from column 128 on. One CTA per SM (shared memory), so the
 // CTA takes all 512 columns.
 constexpr uint32_t kNvTmemCols = 512;
-__device__ __forceinline__ uint32_t nv_acol(int ab) { return 128u + 64u * static_cast<uint32_t>(ab); }
+__device__ __forceinline__ uint32_t nv_acol(int ab) { return 128u + 128u * static_cast<uint32_t>(ab); }
 
 template <int TOK>
 struct NvCfg {
-  // Packed-weight ring: the TMA latency under a full weight stream is 2-3 us,
-  // so it holds as many K blocks as shared memory allows; the activation
-  // operand comes from L2 and needs only a short ring of its own.
-  static constexpr int kStages = TOK == 16 ? 13 : 9;
-  static constexpr int kBStages = 3;
-  static constexpr int kAbuf = 4;  // FP16 weight buffers in tensor memory
-  static constexpr int kBBytes = 2 * TOK * 128;  // two 64-value halves, TOK rows of 128 bytes each
+  // Packed-weight ring: about 100 KB in flight keeps the weight stream at
+  // the copy rate (deeper rings measured slower); the activation operand
+  // comes from L2 and needs only a short ring of its own.
+  static constexpr int kStages = TOK == 16 ? 7 : 6;
+  static constexpr int kBStages = TOK == 16 ? 3 : 2;
+  static constexpr int kAbuf = 3;                 // FP16 weight buffers in tensor memory
+  static constexpr int kBBytes = 4 * TOK * 128;   // four 64-value quarters, TOK rows of 128 bytes each
 };
 
 struct NvArgs {
-  CUtensorMap map13;  // W13 packed [L * 2N rows, H/2 bytes], box 64 rows x 64 bytes
-  CUtensorMap map2;   // W2 packed [L * H rows, N/2 bytes]
-  CUtensorMap mapx;   // x image [(H/64) * TOK rows, 128 bytes], box TOK rows, 128-byte swizzle
-  CUtensorMap maph;   // h image [(N/64) * Rp rows, 128 bytes]
+  CUtensorMap map13;  // W13 packed [L * 2N rows, H/2 bytes], box 64 rows x 128 bytes, 128-byte swizzle
+  CUtensorMap map2;   // W2 packed [L * H rows, N/2 bytes], same box
+  CUtensorMap mapx;   // x image [(H/64) * TOK rows, 128 bytes], box 4 * TOK rows, 128-byte swizzle
+  CUtensorMap maph;   // h image [(N/64) * Rp rows, 128 bytes], box TOK rows
   const __nv_bfloat16* x;
   const int32_t* ids;
   const float* tw;
@@ -98,7 +100,7 @@ struct NvSmem {
   uint64_t fullB[NvCfg<TOK>::kBStages], emptyB[NvCfg<TOK>::kBStages];
   uint64_t afull[NvCfg<TOK>::kAbuf], afree[NvCfg<TOK>::kAbuf], accfull[2], tmemfree[2], final_bar;
   float ysm[16][128];
-  uint2 sc[2][kNvScaleAhead][128];  // [dequant group] weight group scales of its next K blocks, by row
+  uint4 sc[2][kNvScaleAhead][128];  // [dequant group] weight group scales of its next K blocks, by row
   unsigned long long tokmask[kMaxExperts];
   int16_t ulist[kMaxExperts];
   int16_t uidx[kMaxExperts];      // local expert -> unit
@@ -117,8 +119,7 @@ constexpr size_t nv_smem_bytes() {
 static_assert(nv_smem_bytes<16>() <= 232448 && nv_smem_bytes<64>() <= 232448, "shared memory per CTA");
 static_assert(128 + 64 * NvCfg<16>::kAbuf <= kNvTmemCols && 128 + 64 * NvCfg<64>::kAbuf <= kNvTmemCols,
               "tensor memory columns");
-// Swizzled TMA destinations: the activation ring (128-byte swizzle) and the
-// packed-weight ring (64-byte swizzle) start on 1024-byte boundaries.
+// Swizzled TMA destinations (128-byte swizzle) start on 1024-byte boundaries.
 static_assert(offsetof(NvSmem<16>, R) % 1024 == 0 && offsetof(NvSmem<64>, R) % 1024 == 0, "ring alignment");
 // A second CTA on the SM would wait in its TMEM allocation while the first
 // may wait on it through the cross-CTA counters: shared memory keeps it out.
@@ -183,8 +184,10 @@ __device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, uint64
   }
 }
 
-__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+// 8-byte copy of which the first src_bytes (8 or 0) come from src, the rest zeros.
+__device__ __forceinline__ void cp_async8(void* dst, const void* src, uint32_t src_bytes = 8) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -218,7 +221,7 @@ __device__ __forceinline__ uint32_t nv_fold2(float v0, float v1, float d, uint32
 }
 
 // ---------------------------------------------------------------- work plan
-// Each phase's (unit, tile, K block) slots -- at most 1024 x 128 x 64 = 8.4M --
+// Each phase's (unit, tile, K block) slots -- at most 1024 x 128 x 32 = 4.2M --
 // split over Ge = min(G, n) CTAs as in the routed FP8 kernel; the products stay
 // below 2^32, so unsigned 32-bit arithmetic is exact.
 struct NvPhase {
@@ -557,8 +560,12 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
 
   const int U = S.U;
   NvPhase P[2];
-  P[0] = nv_phase(U * (a.N / 64) * (a.H / 128), a.N / 64, a.H / 128, G, c);
-  P[1] = nv_phase(U * (a.H / 128) * (a.N / 128), a.H / 128, a.N / 128, G, c);
+  // K blocks of 256 values; an odd number of 128-value halves leaves a last
+  // block whose second half lies past the row: the weight and activation
+  // loads fill it with zeros and its scales are zero.
+  const int nb1 = (a.H + kNvKB - 1) / kNvKB, nb2 = (a.N + kNvKB - 1) / kNvKB;
+  P[0] = nv_phase(U * (a.N / 64) * nb1, a.N / 64, nb1, G, c);
+  P[1] = nv_phase(U * (a.H / 128) * nb2, a.H / 128, nb2, G, c);
   const uint32_t tmem = S.tmem_base;
 
   if (warp == 0) {
@@ -587,8 +594,8 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
           map = &a.map2;
         }
         mbar_arrive_expect_tx(&S.fullA[s], kNvRawBytes);
-        tma_load_2d(S.R[s], map, st.kb * 64, r0, &S.fullA[s], pol);
-        tma_load_2d(S.R[s] + kNvRawBytes / 2, map, st.kb * 64, r1, &S.fullA[s], pol);
+        tma_load_2d(S.R[s], map, st.kb * (kNvKB / 2), r0, &S.fullA[s], pol);
+        tma_load_2d(S.R[s] + kNvRawBytes / 2, map, st.kb * (kNvKB / 2), r1, &S.fullA[s], pol);
         ++k;
       }
       for (int kk = max(0, k - kS); kk < k; ++kk)
@@ -614,8 +621,7 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
         }
         if (st.phase == 1) {
           mbar_arrive_expect_tx(&S.fullB[s], C::kBBytes);
-          tma_load_2d_plain(S.B[s], &a.mapx, 0, (2 * st.kb) * TOK, &S.fullB[s]);
-          tma_load_2d_plain(S.B[s] + TOK * 128, &a.mapx, 0, (2 * st.kb + 1) * TOK, &S.fullB[s]);
+          tma_load_2d_plain(S.B[s], &a.mapx, 0, (4 * st.kb) * TOK, &S.fullB[s]);
         } else {
           const int le = S.ulist[st.u];
           if (st.u != cur_u) {
@@ -631,8 +637,9 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
           }
           const int roff = S.uoff[st.u];
           mbar_arrive_expect_tx(&S.fullB[s], C::kBBytes);
-          tma_load_2d_plain(S.B[s], &a.maph, 0, (2 * st.kb) * a.Rp + roff, &S.fullB[s]);
-          tma_load_2d_plain(S.B[s] + TOK * 128, &a.maph, 0, (2 * st.kb + 1) * a.Rp + roff, &S.fullB[s]);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            tma_load_2d_plain(S.B[s] + q * TOK * 128, &a.maph, 0, (4 * st.kb + q) * a.Rp + roff, &S.fullB[s]);
         }
         ++k;
       }
@@ -655,15 +662,15 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
           break;
         }
         tc_fence_after();
-        // A (FP16 weights) comes from tensor memory: K step kk is columns
-        // 8kk .. 8kk + 7 of the buffer. B's descriptor of the first K step
+        // A (FP16 weights) comes from tensor memory: K step kk (16 values)
+        // is columns 8kk .. 8kk + 7 of the buffer. B's descriptor of the first K step
         // gets later steps' byte offsets added in 16-byte units to its
         // start-address field (shared addresses stay far below 256 KB, so the
         // 14-bit field never carries).
         const uint64_t bdesc = sw128_desc(smem_u32(S.B[sb]));
         const uint32_t dtm = tmem + tb * TOK;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = 0; kk < kNvKB / 16; ++kk) {
           const uint32_t bo = ((kk >> 2) * (TOK * 128) + (kk & 3) * 32) >> 4;
           tc_mma_f16_ts(dtm, tmem + nv_acol(ab) + 8 * kk, bdesc + bo, idesc, (st.first && kk == 0) ? 0u : 1u);
         }
@@ -687,14 +694,24 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
     const int dg = (warp - 3) >> 2;
     const int row = (warp & 3) * 32 + lane;
     const uint32_t tq = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    // Address of this row's 8 scale bytes for K block st.
-    auto scale_src = [&](const NvStep& q) -> const uint8_t* {
+    // This row's 16 scale bytes of K block q into dst: two 8-byte copies
+    // (rows are 8-byte aligned); the second is zeros when the block's second
+    // half lies past the row.
+    auto fetch_scales = [&](uint4* dst, const NvStep& q) {
       const int le = S.ulist[q.u];
+      const uint8_t* src;
+      int K;
       if (q.phase == 1) {
         const int grow = le * 2 * a.N + (row < 64 ? 64 * q.T + row : a.N + 64 * q.T + row - 64);
-        return a.s13 + static_cast<size_t>(grow) * (a.H / 16) + 8 * q.kb;
+        src = a.s13 + static_cast<size_t>(grow) * (a.H / 16) + 16 * q.kb;
+        K = a.H;
+      } else {
+        src = a.s2 + (static_cast<size_t>(le) * a.H + 128 * q.T + row) * (a.N / 16) + 16 * q.kb;
+        K = a.N;
       }
-      return a.s2 + (static_cast<size_t>(le) * a.H + 128 * q.T + row) * (a.N / 16) + 8 * q.kb;
+      const bool full = (q.kb + 1) * kNvKB <= K;
+      cp_async8(dst, src);
+      cp_async8(reinterpret_cast<uint8_t*>(dst) + 8, full ? src + 8 : src, full ? 8u : 0u);
     };
     // Slots hold this group's K blocks n .. n + kNvScaleAhead - 2; a refill
     // goes to the slot read one iteration earlier (its value already consumed).
@@ -708,7 +725,7 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
       return false;
     };
     for (int j = 0; j < kNvScaleAhead - 1; ++j) {
-      if (next_own(qa)) cp_async8(&S.sc[dg][j][row], scale_src(qa));
+      if (next_own(qa)) fetch_scales(&S.sc[dg][j][row], qa);
       cp_async_commit();
     }
     NvCursor cur{P[0].lo, 1};
@@ -721,8 +738,8 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
       }
       const int s = k % kS, ab = k % C::kAbuf;
       cp_async_wait<kNvScaleAhead - 2>();  // this row's scales of K block k have landed
-      const uint2 sw = S.sc[dg][n % kNvScaleAhead][row];
-      if (next_own(qa)) cp_async8(&S.sc[dg][(n + kNvScaleAhead - 1) % kNvScaleAhead][row], scale_src(qa));
+      const uint4 sw = S.sc[dg][n % kNvScaleAhead][row];
+      if (next_own(qa)) fetch_scales(&S.sc[dg][(n + kNvScaleAhead - 1) % kNvScaleAhead][row], qa);
       cp_async_commit();
       if (!mbar_wait(&S.fullA[s], (k / kS) & 1, a.timeout_ns, &S.abort) ||
           (k >= C::kAbuf && !mbar_wait(&S.afree[ab], ((k / C::kAbuf) - 1) & 1, a.timeout_ns, &S.abort))) {
@@ -730,22 +747,21 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
         break;
       }
       tc_fence_after();
-      // The row's 64 packed bytes as four 16-byte chunks. The 64-byte TMA
-      // swizzle put chunk ch of row r at chunk ch ^ ((r / 2) % 4) of the
-      // row, so the warp's reads of one chunk spread over all banks while the
-      // chunk, and with it the TMEM column, stays the same across the warp.
-      const uint4* src = reinterpret_cast<const uint4*>(S.R[s] + row * 64);
-      const int sw64 = (row >> 1) & 3;
-      uint4 pk[4];
+      // The row's 128 packed bytes as eight 16-byte chunks. The 128-byte TMA
+      // swizzle put chunk ch of row r at chunk ch ^ (r % 8) of the row, so
+      // the warp's reads of one chunk spread over all banks while the chunk,
+      // and with it the TMEM column, stays the same across the warp.
+      const uint4* src = reinterpret_cast<const uint4*>(S.R[s] + row * 128);
+      const int sw128 = row & 7;
+      const uint32_t scw[4] = {sw.x, sw.y, sw.z, sw.w};
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) pk[ch] = src[ch ^ sw64];
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {  // chunk ch: values 32ch .. 32ch + 31, groups 2ch and 2ch + 1
-        const uint32_t words[4] = {pk[ch].x, pk[ch].y, pk[ch].z, pk[ch].w};
+      for (int ch = 0; ch < 8; ++ch) {  // chunk ch: values 32ch .. 32ch + 31, groups 2ch and 2ch + 1
+        const uint4 pk = src[ch ^ sw128];
+        const uint32_t words[4] = {pk.x, pk.y, pk.z, pk.w};
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int g = 2 * ch + h;  // group of 16 values = TMEM columns 8g .. 8g + 7
-          const uint32_t sh2 = nv_scale_h2((g < 4 ? sw.x : sw.y) >> (8 * (g & 3)));
+          const uint32_t sh2 = nv_scale_h2(scw[g >> 2] >> (8 * (g & 3)));
           uint32_t o[8];
 #pragma unroll
           for (int b = 0; b < 4; ++b) {
@@ -986,9 +1002,9 @@ int routed_nvfp4(const void* x, const int32_t* ids, const float* weights, const 
   a.Rp = w.Rp;
   a.limit = limit;
   a.timeout_ns = wait_timeout_ns();
-  if (!nv_map(&a.map13, w13, static_cast<unsigned long long>(L) * 2 * N, H / 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !nv_map(&a.map2, w2, static_cast<unsigned long long>(L) * H, N / 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !nv_map(&a.mapx, w.ximg, static_cast<unsigned long long>(H / 64) * w.tok, 128, 128, w.tok,
+  if (!nv_map(&a.map13, w13, static_cast<unsigned long long>(L) * 2 * N, H / 2, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !nv_map(&a.map2, w2, static_cast<unsigned long long>(L) * H, N / 2, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !nv_map(&a.mapx, w.ximg, static_cast<unsigned long long>(H / 64) * w.tok, 128, 128, 4 * w.tok,
               CU_TENSOR_MAP_SWIZZLE_128B) ||
       !nv_map(&a.maph, w.himg, static_cast<unsigned long long>(N / 64) * w.Rp, 128, 128, w.tok,
               CU_TENSOR_MAP_SWIZZLE_128B))

@@ -45,9 +45,12 @@ def _run(fme, cfg, M, seed, weights_scale=1.0, tokens=None, device_weights=False
 
 SMALL = W.Nvfp4Config("nvfp4_small", 256, 128, 6, 12, 3, 3, float("inf"), (5,))
 RAGGED = W.Nvfp4Config("nvfp4_ragged", 1024, 384, 10, 40, 20, 4, float("inf"), (7,))
+# H and N odd multiples of 128: the last 256-value K block of both GEMMs is half past the row.
+ODD = W.Nvfp4Config("nvfp4_odd", 384, 640, 7, 14, 2, 3, float("inf"), (9,))
 
 
-@pytest.mark.parametrize("cfg,M", [(SMALL, 5), (RAGGED, 7), (dataclasses.replace(SMALL, limit=2.0), 6)])
+@pytest.mark.parametrize("cfg,M", [(SMALL, 5), (RAGGED, 7), (dataclasses.replace(SMALL, limit=2.0), 6),
+                                   (ODD, 9), (ODD, 33)])
 def test_nvfp4_small_full_parity(fme, cfg, M):
     got, ref, ids = _run(fme, cfg, M, seed=41)
     local = ((ids >= cfg.e0) & (ids < cfg.e0 + cfg.L)).any(axis=1)
