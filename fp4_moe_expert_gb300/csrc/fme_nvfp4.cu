@@ -8,21 +8,21 @@
 // scales, the L2 GEMM; the routing weights are applied once, in the final
 // scatter to [M, H]. The design is this library's own:
 //
-// * Every E2M1 value times its UE4M3 group scale is exact in FP16 (at most 6
-//   significant bits, magnitudes 2^-10 .. 2688), so both operands are folded
-//   into FP16 and multiplied on `tcgen05.mma kind::f16` with FP32
-//   accumulation: each product is exact and only the FP32 sums round, like
-//   the pages' block-scaled product.
+// * Both GEMMs run on `tcgen05.mma kind::mxf4nvf4` (block-scaled E2M1 x E2M1
+//   with one UE4M3 scale per 16 values on each side, FP32 accumulation):
+//   exactly the pages' block-scaled product, with the packed weights read
+//   straight from the TMA ring and no dequantisation.
 // * Weights: TMA streams the packed E2M1 rows, 128 bytes (256 values) of
-//   each of 128 rows per K block, into a ring; dequant warps expand each
-//   block with its group scales into FP16 and store it to tensor memory,
-//   where the MMA reads it as the A operand.
-// * Activations: at start every CTA quantises a share of x into an FP16
-//   image in the workspace (all tokens, 16 or 64 rows); the GEMM1 epilogue
-//   quantises each slot's h (groups of 16 lie inside one 64-row tile) into a
-//   second image whose rows are the slots of each expert, consecutive. A
-//   second TMA thread loads both as the B operand; GEMM1 uses every token as
-//   a column and reads back the routed ones.
+//   each of 128 rows per K block, 128-byte swizzle, into a ring; their group
+//   scales come ahead through cp.async and four scale warps write them, with
+//   the activation scales, into tensor memory for the MMA.
+// * Activations: at start every CTA quantises a share of x to E2M1 with
+//   UE4M3 group scales into a packed image in the workspace (all tokens, 16
+//   or 64 rows); the GEMM1 epilogue quantises each slot's h (groups of 16 lie
+//   inside one 64-row tile) into a second packed image whose rows are the
+//   slots of each expert, consecutive. A second TMA thread loads image and
+//   scales as the B operand; GEMM1 uses every token as a column and reads
+//   back the routed ones.
 // * Work split, split-tile finishing and bounded waits follow the routed FP8
 //   kernel: one CTA per SM, each phase's (expert, tile, K block) list cut
 //   into equal slices, a split tile finished by its first contributor.
@@ -39,38 +39,40 @@
 
 namespace fme {
 
-constexpr int kNvThreads = 480;         // A TMA, MMA, B TMA, 2 x 4 dequant, 4 epilogue warps
+constexpr int kNvThreads = 352;         // A TMA, MMA, B TMA, 4 scale, 4 epilogue warps
 constexpr int kNvKB = 256;              // K values per K block
 constexpr int kNvRawBytes = 128 * 128;  // one K block: 128 rows x 128 packed bytes
 
-// Weight group scales run kNvScaleAhead of a dequant group's K blocks ahead of
-// it (two 8-byte cp.async per row into a small shared ring), so their global
-// latency never stalls it.
+// Weight group scales run kNvScaleAhead K blocks ahead of the scale warps
+// (two 8-byte cp.async per row into a small shared ring), so their global
+// latency never stalls them.
 constexpr int kNvScaleAhead = 4;
 
 // Tensor memory: the accumulators (two buffers of TOK columns) sit in
-// columns 0 .. 127 and the FP16 weight buffers, 128 columns each (128 rows x
-// 256 K values), from column 128 on. One CTA per SM (shared memory), so the
-// CTA takes all 512 columns.
-constexpr uint32_t kNvTmemCols = 512;
-__device__ __forceinline__ uint32_t nv_acol(int ab) { return 128u + 128u * static_cast<uint32_t>(ab); }
+// columns 0 .. 127, the scale vectors of a K block (16 columns for A, 16 for
+// B: four per MMA) in buffers of 32 columns from column 128 on.
+constexpr uint32_t kNvTmemCols = 256;
+__device__ __forceinline__ uint32_t nv_sfcol(int sf) { return 128u + 32u * static_cast<uint32_t>(sf); }
 
 template <int TOK>
 struct NvCfg {
   // Packed-weight ring: about 100 KB in flight keeps the weight stream at
   // the copy rate (deeper rings measured slower); the activation operand
   // comes from L2 and needs only a short ring of its own.
-  static constexpr int kStages = TOK == 16 ? 7 : 6;
-  static constexpr int kBStages = TOK == 16 ? 3 : 2;
-  static constexpr int kAbuf = 3;                 // FP16 weight buffers in tensor memory
-  static constexpr int kBBytes = 4 * TOK * 128;   // four 64-value quarters, TOK rows of 128 bytes each
+  static constexpr int kStages = 7;
+  static constexpr int kBStages = 4;
+  static constexpr int kSfBuf = 4;                // scale-vector buffers in tensor memory
+  static constexpr int kBBytes = TOK * 128;       // TOK rows of 128 packed bytes (256 values)
+  static constexpr int kBsBytes = TOK * 16;       // their 16 group scales
 };
 
 struct NvArgs {
   CUtensorMap map13;  // W13 packed [L * 2N rows, H/2 bytes], box 64 rows x 128 bytes, 128-byte swizzle
   CUtensorMap map2;   // W2 packed [L * H rows, N/2 bytes], same box
-  CUtensorMap mapx;   // x image [(H/64) * TOK rows, 128 bytes], box 4 * TOK rows, 128-byte swizzle
-  CUtensorMap maph;   // h image [(N/64) * Rp rows, 128 bytes], box TOK rows
+  CUtensorMap mapx;   // x image [nb1 * TOK rows, 128 bytes], box TOK rows, 128-byte swizzle
+  CUtensorMap mapxs;  // x image scales [nb1 * TOK rows, 16 bytes], box TOK rows
+  CUtensorMap maph;   // h image [nb2 * Rp rows, 128 bytes], box TOK rows, 128-byte swizzle
+  CUtensorMap maphs;  // h image scales [nb2 * Rp rows, 16 bytes], box TOK rows
   const __nv_bfloat16* x;
   const int32_t* ids;
   const float* tw;
@@ -83,8 +85,10 @@ struct NvArgs {
   uint32_t* hpassed;  // [L] CTAs past the expert's hidden wait
   uint32_t* cnt1;     // [L * N/64] contributors per GEMM1 tile
   uint32_t* cnt2;     // [L * H/128]
-  uint8_t* ximg;
-  uint8_t* himg;
+  uint8_t* ximg;  // [nb1][TOK][128]: packed E2M1 of x, K block kb of token t at row kb * TOK + t
+  uint8_t* xsc;   // [nb1][TOK][16]: its UE4M3 group scales
+  uint8_t* himg;  // [nb2][Rp][128]: packed E2M1 of h, slot rows of each unit consecutive
+  uint8_t* hsc;   // [nb2][Rp][16]
   __nv_bfloat16* obuf;  // [M * top_k, H] slot outputs (route order)
   float* part;          // [2][kFp8MaxCtas][2][TOK][128]
   int M, H, N, L, e0, top_k, Rp;
@@ -96,11 +100,12 @@ template <int TOK>
 struct NvSmem {
   uint8_t B[NvCfg<TOK>::kBStages][NvCfg<TOK>::kBBytes];
   uint8_t R[NvCfg<TOK>::kStages][kNvRawBytes];
+  alignas(128) uint8_t Bs[NvCfg<TOK>::kBStages][NvCfg<TOK>::kBsBytes];
   uint64_t fullA[NvCfg<TOK>::kStages], emptyA[NvCfg<TOK>::kStages];
   uint64_t fullB[NvCfg<TOK>::kBStages], emptyB[NvCfg<TOK>::kBStages];
-  uint64_t afull[NvCfg<TOK>::kAbuf], afree[NvCfg<TOK>::kAbuf], accfull[2], tmemfree[2], final_bar;
+  uint64_t sffull[NvCfg<TOK>::kSfBuf], sffree[NvCfg<TOK>::kSfBuf], accfull[2], tmemfree[2], final_bar;
   float ysm[16][128];
-  uint4 sc[2][kNvScaleAhead][128];  // [dequant group] weight group scales of its next K blocks, by row
+  uint4 sc[4][kNvScaleAhead][4][32];  // [scale warp][K block slot][c][lane]: scales of weight row lane + 32c
   unsigned long long tokmask[kMaxExperts];
   int16_t ulist[kMaxExperts];
   int16_t uidx[kMaxExperts];      // local expert -> unit
@@ -117,7 +122,7 @@ constexpr size_t nv_smem_bytes() {
   return sizeof(NvSmem<TOK>) + 1024;
 }
 static_assert(nv_smem_bytes<16>() <= 232448 && nv_smem_bytes<64>() <= 232448, "shared memory per CTA");
-static_assert(128 + 64 * NvCfg<16>::kAbuf <= kNvTmemCols && 128 + 64 * NvCfg<64>::kAbuf <= kNvTmemCols,
+static_assert(128 + 32 * NvCfg<16>::kSfBuf <= kNvTmemCols && 128 + 32 * NvCfg<64>::kSfBuf <= kNvTmemCols,
               "tensor memory columns");
 // Swizzled TMA destinations (128-byte swizzle) start on 1024-byte boundaries.
 static_assert(offsetof(NvSmem<16>, R) % 1024 == 0 && offsetof(NvSmem<64>, R) % 1024 == 0, "ring alignment");
@@ -132,16 +137,22 @@ __device__ __forceinline__ void nv_error(const NvArgs& a, volatile int& abort, u
   abort = 1;
 }
 
-// tcgen05.mma kind::f16 (both operands F16, K-major, FP32 accumulation): the
-// instruction descriptor has the fields of kind::f8f6f4, format code 0 = F16.
-// D (TMEM) += A (TMEM, 128 lanes = rows, two FP16 values of K per column)
-// x B (shared memory descriptor), FP16 inputs, FP32 accumulation.
-__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                              uint32_t accumulate) {
+// Instruction descriptor of tcgen05.mma kind::mxf4nvf4: A and B E2M1 (type
+// code 1 in bits 7-9 and 10-12), both K-major, UE4M3 scales (bit 23 clear),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28, scale-vector ids 0 (four
+// scales per row per MMA take the whole 32-bit TMEM cell).
+__host__ __device__ constexpr uint32_t nv_idesc(int M, int N) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+// D (TMEM) (+)= sum over the 4 groups of 16 of (A x B) * sfa * sfb: A and B
+// packed E2M1 in shared memory (64 values, 32 bytes, per row), the scale
+// vectors in TMEM.
+__device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
   asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(
-          d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "{ .reg .pred p; setp.ne.b32 p, %6, 0; tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X "
+      "[%0], %1, %2, %3, [%4], [%5], p; }" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
 
@@ -153,35 +164,6 @@ __device__ __forceinline__ void tma_load_2d_plain(void* dst, const void* tmap, i
       "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
-}
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-  return d;
-}
-// Bounded wait that polls with the non-blocking test_wait: for the per-K-block
-// hand-offs between the dequant warps and the MMA issuer, where a suspended
-// try_wait would add its wake-up latency to every K block.
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, uint64_t limit_ns, const volatile int* abort) {
-  if (mbar_test(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_test(bar, parity)) return true;
-    if (*abort) return false;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
-  }
 }
 
 // 8-byte copy of which the first src_bytes (8 or 0) come from src, the rest zeros.
@@ -200,24 +182,12 @@ __device__ __forceinline__ void cp_async_wait() {
 __device__ __forceinline__ uint32_t nv_scale_byte(float amax) {
   return f32x2_to_e4m3x2(__fdiv_rn(amax, 6.0f), 0.0f) & 0xFFu;
 }
-// f16x2 (s, s) of a UE4M3 byte.
-__device__ __forceinline__ uint32_t nv_scale_h2(uint32_t byte) {
-  uint32_t lo, hi;
-  e4m3x4_to_f16x2x2(byte & 0xFFu, lo, hi);
-  const uint32_t h = lo & 0xFFFFu;
-  return h | (h << 16);
-}
-__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-// Two values -> their E2M1 codes times the group scale, as one f16x2 word
-// (exact). d == 0 gives zeros (a zero scale quantises its group to zeros).
-__device__ __forceinline__ uint32_t nv_fold2(float v0, float v1, float d, uint32_t sh2) {
+// Two values -> their E2M1 codes (v0 in the low nibble) against the group's
+// stored scale d; d == 0 gives zeros (a zero scale quantises its group to
+// zeros).
+__device__ __forceinline__ uint32_t nv_quant2(float v0, float v1, float d) {
   if (!(d > 0.0f)) return 0u;
-  const uint32_t nib = f32x2_to_e2m1x2(__fdiv_rn(v0, d), __fdiv_rn(v1, d));
-  return hmul2_u32(e2m1x2_to_f16x2(nib), sh2);
+  return f32x2_to_e2m1x2(__fdiv_rn(v0, d), __fdiv_rn(v1, d));
 }
 
 // ---------------------------------------------------------------- work plan
@@ -291,8 +261,10 @@ __device__ __forceinline__ float* nv_part(const NvArgs& a, int phase, int c, int
 // GEMM1 tile T of unit u (rows 0..63 gate 64T + q, 64..127 up): per slot of
 // the unit, g = bf16(gate), v = bf16(up), h = bf16(silu(min(g, L)) *
 // clamp(v, -L, L)) ("nvfp4-megamoe-kernel README.md" Bugs Found & Fixed 4
-// and 6), then h -> E2M1 x UE4M3 per 16 (groups 16j..16j+15 of the tile are
-// half-warps) folded into FP16 and written to the h image row of the slot.
+// and 6), then h -> E2M1 with a UE4M3 scale per 16 (groups 16j..16j+15 of
+// the tile are half-warps), written to the slot's row of the h image: the
+// tile's 64 values are bytes 32 (T % 4) .. + 31 of K block T / 4, its four
+// scales bytes 4 (T % 4) .. + 3.
 template <int TOK>
 __device__ void nv_finish1(const NvArgs& a, NvSmem<TOK>& S, int u, int T, const float (&y)[TOK], int row,
                            int etid) {
@@ -327,12 +299,11 @@ __device__ void nv_finish1(const NvArgs& a, NvSmem<TOK>& S, int u, int T, const 
         amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 8));
         const uint32_t sb = nv_scale_byte(amax);
         const float d = e4m3_to_f32(sb);
-        // Pair with the neighbour lane: one f16x2 word per even lane.
+        // Pair with the neighbour lane: one byte (two nibbles) per even lane.
         const float hn = __shfl_xor_sync(0xFFFFFFFFu, h, 1);
-        if ((q & 1) == 0) {
-          const uint32_t w = nv_fold2(h, hn, d, nv_scale_h2(sb));
-          *reinterpret_cast<uint32_t*>(a.himg + (static_cast<size_t>(T) * a.Rp + r0 + i) * 128 + q * 2) = w;
-        }
+        const size_t hrow = static_cast<size_t>(T >> 2) * a.Rp + r0 + i;
+        if ((q & 1) == 0) a.himg[hrow * 128 + (T & 3) * 32 + (q >> 1)] = static_cast<uint8_t>(nv_quant2(h, hn, d));
+        if ((q & 15) == 0) a.hsc[hrow * 16 + (T & 3) * 4 + (q >> 4)] = static_cast<uint8_t>(sb);
       }
     }
     nv_epi_bar();
@@ -447,15 +418,15 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
   if (tid == 0) {
     for (int s = 0; s < kS; ++s) {
       mbar_init(&S.fullA[s], 1);
-      mbar_init(&S.emptyA[s], 4);
+      mbar_init(&S.emptyA[s], 1);
     }
     for (int s = 0; s < kSB; ++s) {
       mbar_init(&S.fullB[s], 1);
       mbar_init(&S.emptyB[s], 1);
     }
-    for (int b = 0; b < C::kAbuf; ++b) {
-      mbar_init(&S.afull[b], 4);
-      mbar_init(&S.afree[b], 1);
+    for (int b = 0; b < C::kSfBuf; ++b) {
+      mbar_init(&S.sffull[b], 4);
+      mbar_init(&S.sffree[b], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&S.accfull[b], 1);
@@ -467,7 +438,9 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
     prefetch_tmap(&a.map13);
     prefetch_tmap(&a.map2);
     prefetch_tmap(&a.mapx);
+    prefetch_tmap(&a.mapxs);
     prefetch_tmap(&a.maph);
+    prefetch_tmap(&a.maphs);
   }
   if (warp == 1) {
     tmem_alloc(&S.tmem_base, kNvTmemCols);
@@ -479,33 +452,44 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
   __syncthreads();
   tc_fence_after();
 
-  // ---- x image: token t, group g of 16 -> FP16 (E2M1 x UE4M3), all CTAs share the work.
+  // ---- x image: token t, group g of 16 -> 8 packed bytes and a scale byte,
+  // all CTAs share the work. Groups past H (an odd number of 128-value
+  // halves) get zero data and zero scales, and so do the h image's scales of
+  // that kind: the MMA multiplies every group by its scales.
   {
-    const int gpt = a.H / 16;
+    const int nb1 = (a.H + kNvKB - 1) / kNvKB, nb2 = (a.N + kNvKB - 1) / kNvKB;
+    const int gpt = nb1 * (kNvKB / 16);
     for (int i = c * kNvThreads + tid; i < a.M * gpt; i += G * kNvThreads) {
       const int t = i / gpt, g = i % gpt;
-      const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * a.H + 16 * g);
-      const uint4 w0 = __ldg(src), w1 = __ldg(src + 1);
-      const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-      float v[16];
+      const size_t xrow = static_cast<size_t>(g >> 4) * TOK + t;
+      uint32_t lo = 0u, hi = 0u, sb = 0u;
+      if (16 * g < a.H) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * a.H + 16 * g);
+        const uint4 w0 = __ldg(src), w1 = __ldg(src + 1);
+        const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        float v[16];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        v[2 * k] = __uint_as_float(wd[k] << 16);
-        v[2 * k + 1] = __uint_as_float(wd[k] & 0xFFFF0000u);
+        for (int k = 0; k < 8; ++k) {
+          v[2 * k] = __uint_as_float(wd[k] << 16);
+          v[2 * k + 1] = __uint_as_float(wd[k] & 0xFFFF0000u);
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(v[k]));
+        sb = nv_scale_byte(amax);
+        const float d = e4m3_to_f32(sb);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          lo |= nv_quant2(v[2 * k], v[2 * k + 1], d) << (8 * k);
+          hi |= nv_quant2(v[8 + 2 * k], v[8 + 2 * k + 1], d) << (8 * k);
+        }
       }
-      float amax = 0.0f;
-#pragma unroll
-      for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(v[k]));
-      const uint32_t sb = nv_scale_byte(amax);
-      const float d = e4m3_to_f32(sb);
-      const uint32_t sh2 = nv_scale_h2(sb);
-      uint32_t o[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) o[k] = nv_fold2(v[2 * k], v[2 * k + 1], d, sh2);
-      // image row (64-value half block g / 4, token t), 32 bytes at (g % 4) * 32
-      uint4* dst = reinterpret_cast<uint4*>(a.ximg + (static_cast<size_t>(g / 4) * TOK + t) * 128 + (g % 4) * 32);
-      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+      *reinterpret_cast<uint2*>(a.ximg + xrow * 128 + (g & 15) * 8) = make_uint2(lo, hi);
+      a.xsc[xrow * 16 + (g & 15)] = static_cast<uint8_t>(sb);
+    }
+    if (a.N % kNvKB != 0) {
+      for (int r = c * kNvThreads + tid; r < a.Rp; r += G * kNvThreads)
+        *reinterpret_cast<uint2*>(a.hsc + (static_cast<size_t>(nb2 - 1) * a.Rp + r) * 16 + 8) = make_uint2(0u, 0u);
     }
   }
   // ---- local slots and the unit list
@@ -598,11 +582,12 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
         tma_load_2d(S.R[s] + kNvRawBytes / 2, map, st.kb * (kNvKB / 2), r1, &S.fullA[s], pol);
         ++k;
       }
+      // Let every issued copy land before the CTA can exit.
       for (int kk = max(0, k - kS); kk < k; ++kk)
         if (!mbar_wait(&S.fullA[kk % kS], (kk / kS) & 1, a.timeout_ns, nullptr)) atomicOr(a.err, kErrDrain);
     }
   } else if (warp == 2) {
-    // ------------------------------------------------------------ B producer (activation images)
+    // ------------------------------------------------------------ B producer (activation images and their scales)
     if (lane == 0) {
       bool ok = nv_wait_ge(a, S.abort, a.sync, static_cast<uint32_t>(G));
       // The last CTA past the x-image wait re-arms both counters.
@@ -620,8 +605,9 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
           break;
         }
         if (st.phase == 1) {
-          mbar_arrive_expect_tx(&S.fullB[s], C::kBBytes);
-          tma_load_2d_plain(S.B[s], &a.mapx, 0, (4 * st.kb) * TOK, &S.fullB[s]);
+          mbar_arrive_expect_tx(&S.fullB[s], C::kBBytes + C::kBsBytes);
+          tma_load_2d_plain(S.B[s], &a.mapx, 0, st.kb * TOK, &S.fullB[s]);
+          tma_load_2d_plain(S.Bs[s], &a.mapxs, 0, st.kb * TOK, &S.fullB[s]);
         } else {
           const int le = S.ulist[st.u];
           if (st.u != cur_u) {
@@ -635,11 +621,10 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
               atomicExch(a.hpassed + le, 0u);
             }
           }
-          const int roff = S.uoff[st.u];
-          mbar_arrive_expect_tx(&S.fullB[s], C::kBBytes);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            tma_load_2d_plain(S.B[s] + q * TOK * 128, &a.maph, 0, (4 * st.kb + q) * a.Rp + roff, &S.fullB[s]);
+          const int y0 = st.kb * a.Rp + S.uoff[st.u];
+          mbar_arrive_expect_tx(&S.fullB[s], C::kBBytes + C::kBsBytes);
+          tma_load_2d_plain(S.B[s], &a.maph, 0, y0, &S.fullB[s]);
+          tma_load_2d_plain(S.Bs[s], &a.maphs, 0, y0, &S.fullB[s]);
         }
         ++k;
       }
@@ -649,33 +634,35 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = f8_idesc(128, TOK);  // kind::f16 uses the same fields (F16 = format 0)
+      const uint32_t idesc = nv_idesc(128, TOK);
       NvCursor cur{P[0].lo, 1};
       NvStep st;
       int k = 0, seg = 0;
       while (cur.next(P, st)) {
-        const int sb = k % kSB, ab = k % C::kAbuf, tb = seg & 1;
-        if (!mbar_wait(&S.afull[ab], (k / C::kAbuf) & 1, a.timeout_ns, &S.abort) ||
+        const int s = k % kS, sb = k % kSB, sf = k % C::kSfBuf, tb = seg & 1;
+        if (!mbar_wait(&S.fullA[s], (k / kS) & 1, a.timeout_ns, &S.abort) ||
             !mbar_wait(&S.fullB[sb], (k / kSB) & 1, a.timeout_ns, &S.abort) ||
+            !mbar_wait(&S.sffull[sf], (k / C::kSfBuf) & 1, a.timeout_ns, &S.abort) ||
             (st.first && seg >= 2 && !mbar_wait(&S.tmemfree[tb], ((seg >> 1) - 1) & 1, a.timeout_ns, &S.abort))) {
           if (!S.abort) nv_error(a, S.abort, kErrRingWait);
           break;
         }
         tc_fence_after();
-        // A (FP16 weights) comes from tensor memory: K step kk (16 values)
-        // is columns 8kk .. 8kk + 7 of the buffer. B's descriptor of the first K step
-        // gets later steps' byte offsets added in 16-byte units to its
-        // start-address field (shared addresses stay far below 256 KB, so the
-        // 14-bit field never carries).
+        // Both operands are 128-byte-swizzled K-major tiles of 128-byte rows
+        // (256 values); MMA j takes values 64j .. 64j + 63, 32 bytes further
+        // in each row (start address in 16-byte units; shared addresses stay
+        // far below 256 KB, so the 14-bit field never carries).
+        const uint64_t adesc = sw128_desc(smem_u32(S.R[s]));
         const uint64_t bdesc = sw128_desc(smem_u32(S.B[sb]));
         const uint32_t dtm = tmem + tb * TOK;
+        const uint32_t sfa = tmem + nv_sfcol(sf), sfb = sfa + 16;
 #pragma unroll
-        for (int kk = 0; kk < kNvKB / 16; ++kk) {
-          const uint32_t bo = ((kk >> 2) * (TOK * 128) + (kk & 3) * 32) >> 4;
-          tc_mma_f16_ts(dtm, tmem + nv_acol(ab) + 8 * kk, bdesc + bo, idesc, (st.first && kk == 0) ? 0u : 1u);
-        }
-        tc_commit(&S.afree[ab]);
+        for (int j = 0; j < kNvKB / 64; ++j)
+          tc_mma_nvf4(dtm, adesc + 2 * j, bdesc + 2 * j, idesc, sfa + 4 * j, sfb + 4 * j,
+                      (st.first && j == 0) ? 0u : 1u);
+        tc_commit(&S.emptyA[s]);
         tc_commit(&S.emptyB[sb]);
+        tc_commit(&S.sffree[sf]);
         if (st.last) {
           tc_commit(&S.accfull[tb]);
           ++seg;
@@ -685,19 +672,19 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
       tc_commit(&S.final_bar);
       if (!mbar_wait(&S.final_bar, 0, a.timeout_ns, nullptr)) atomicOr(a.err, kErrDrain);
     }
-  } else if (warp < 11) {
-    // ------------------------------------------------------------ dequant (one weight row per thread)
-    // Two groups of four warps take the even and the odd K blocks: each K
-    // block is a chain of latencies (shared loads, converts, TMEM stores),
-    // and two chains in flight double the throughput. A warp may only reach
-    // the TMEM lane quadrant warp % 4, so that quadrant's rows are its own.
-    const int dg = (warp - 3) >> 2;
-    const int row = (warp & 3) * 32 + lane;
-    const uint32_t tq = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    // This row's 16 scale bytes of K block q into dst: two 8-byte copies
+  } else if (warp < 7) {
+    // ------------------------------------------------------------ scale vectors -> TMEM
+    // Per K block and MMA j: lane r of each lane quadrant, column c holds the
+    // four UE4M3 scales of row r + 32c (A: weight rows, B: token columns),
+    // written identically into all four quadrants (each warp writes its own,
+    // from its own copies of the weight scales, so the warps never wait on
+    // one another).
+    const int quad = warp & 3;
+    const uint32_t tq = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    // The 16 scale bytes of weight row `row` of K block q: two 8-byte copies
     // (rows are 8-byte aligned); the second is zeros when the block's second
     // half lies past the row.
-    auto fetch_scales = [&](uint4* dst, const NvStep& q) {
+    auto fetch_row = [&](uint4* dst, const NvStep& q, int row) {
       const int le = S.ulist[q.u];
       const uint8_t* src;
       int K;
@@ -713,82 +700,64 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
       cp_async8(dst, src);
       cp_async8(reinterpret_cast<uint8_t*>(dst) + 8, full ? src + 8 : src, full ? 8u : 0u);
     };
-    // Slots hold this group's K blocks n .. n + kNvScaleAhead - 2; a refill
-    // goes to the slot read one iteration earlier (its value already consumed).
+    auto fetch = [&](int slot, const NvStep& q) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) fetch_row(&S.sc[quad][slot][c][lane], q, lane + 32 * c);
+    };
+    // Slot n % kNvScaleAhead holds K block n; a refill goes to the slot read
+    // one iteration earlier (each thread reads only its own copies).
     NvCursor ahead{P[0].lo, 1};
     NvStep qa;
-    int ka = 0;
-    auto next_own = [&](NvStep& q) -> bool {
-      while (ahead.next(P, q)) {
-        if (((ka++) & 1) == dg) return true;
-      }
-      return false;
-    };
     for (int j = 0; j < kNvScaleAhead - 1; ++j) {
-      if (next_own(qa)) fetch_scales(&S.sc[dg][j][row], qa);
+      if (ahead.next(P, qa)) fetch(j, qa);
       cp_async_commit();
     }
     NvCursor cur{P[0].lo, 1};
     NvStep st;
-    int k = 0, n = 0;
+    int k = 0;
     while (cur.next(P, st)) {
-      if ((k & 1) != dg) {
-        ++k;
-        continue;
+      const int sb = k % kSB, sf = k % C::kSfBuf;
+      cp_async_wait<kNvScaleAhead - 2>();  // this thread's scales of K block k have landed
+      uint32_t ra[16], rb[16];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint4 w = S.sc[quad][k % kNvScaleAhead][c][lane];
+        ra[c] = w.x;
+        ra[4 + c] = w.y;
+        ra[8 + c] = w.z;
+        ra[12 + c] = w.w;
       }
-      const int s = k % kS, ab = k % C::kAbuf;
-      cp_async_wait<kNvScaleAhead - 2>();  // this row's scales of K block k have landed
-      const uint4 sw = S.sc[dg][n % kNvScaleAhead][row];
-      if (next_own(qa)) fetch_scales(&S.sc[dg][(n + kNvScaleAhead - 1) % kNvScaleAhead][row], qa);
+      if (ahead.next(P, qa)) fetch((k + kNvScaleAhead - 1) % kNvScaleAhead, qa);
       cp_async_commit();
-      if (!mbar_wait(&S.fullA[s], (k / kS) & 1, a.timeout_ns, &S.abort) ||
-          (k >= C::kAbuf && !mbar_wait(&S.afree[ab], ((k / C::kAbuf) - 1) & 1, a.timeout_ns, &S.abort))) {
+      if (!mbar_wait(&S.fullB[sb], (k / kSB) & 1, a.timeout_ns, &S.abort) ||
+          (k >= C::kSfBuf && !mbar_wait(&S.sffree[sf], ((k / C::kSfBuf) - 1) & 1, a.timeout_ns, &S.abort))) {
         if (!S.abort) nv_error(a, S.abort, kErrRingWait);
         break;
       }
-      tc_fence_after();
-      // The row's 128 packed bytes as eight 16-byte chunks. The 128-byte TMA
-      // swizzle put chunk ch of row r at chunk ch ^ (r % 8) of the row, so
-      // the warp's reads of one chunk spread over all banks while the chunk,
-      // and with it the TMEM column, stays the same across the warp.
-      const uint4* src = reinterpret_cast<const uint4*>(S.R[s] + row * 128);
-      const int sw128 = row & 7;
-      const uint32_t scw[4] = {sw.x, sw.y, sw.z, sw.w};
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {  // chunk ch: values 32ch .. 32ch + 31, groups 2ch and 2ch + 1
-        const uint4 pk = src[ch ^ sw128];
-        const uint32_t words[4] = {pk.x, pk.y, pk.z, pk.w};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int g = 2 * ch + h;  // group of 16 values = TMEM columns 8g .. 8g + 7
-          const uint32_t sh2 = nv_scale_h2(scw[g >> 2] >> (8 * (g & 3)));
-          uint32_t o[8];
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            o[b] = e2m1x2_to_f16x2(words[2 * h] >> (8 * b));
-            o[4 + b] = e2m1x2_to_f16x2(words[2 * h + 1] >> (8 * b));
-          }
-#pragma unroll
-          for (int b = 0; b < 8; ++b) o[b] = hmul2_u32(o[b], sh2);
-          tmem_st8(tq + nv_acol(ab) + 8 * g, o);
-        }
+      for (int c = 0; c < 4; ++c) {
+        const int t = lane + 32 * c;  // token column
+        const uint4 w = t < TOK ? *reinterpret_cast<const uint4*>(S.Bs[sb] + 16 * t) : make_uint4(0u, 0u, 0u, 0u);
+        rb[c] = w.x;
+        rb[4 + c] = w.y;
+        rb[8 + c] = w.z;
+        rb[12 + c] = w.w;
       }
+      tc_fence_after();
+      tmem_st16(tq + nv_sfcol(sf), ra);
+      tmem_st16(tq + nv_sfcol(sf) + 16, rb);
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&S.afull[ab]);
-        mbar_arrive(&S.emptyA[s]);
-      }
+      if (lane == 0) mbar_arrive(&S.sffull[sf]);
       ++k;
-      ++n;
     }
     cp_async_wait<0>();
   } else {
     // ------------------------------------------------------------ epilogue (TMEM lane quadrant = warp % 4)
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
-    const int etid = tid - 352;
+    const int etid = tid - 224;
     NvCursor cur{P[0].lo, 1};
     NvStep st;
     int seg = 0;
@@ -904,7 +873,7 @@ static bool nv_map(CUtensorMap* map, const void* base, unsigned long long rows, 
 
 struct NvWorkspace {
   uint32_t *err, *sync, *done, *hpassed, *cnt1, *cnt2;
-  uint8_t *ximg, *himg;
+  uint8_t *ximg, *xsc, *himg, *hsc;
   __nv_bfloat16* obuf;
   float* part;
   int tok, Rp;
@@ -930,10 +899,15 @@ static NvWorkspace nv_layout(void* base, int M, int H, int N, int L, int top_k) 
   off += a256(4 * static_cast<size_t>(L) * (N / 64));
   w.cnt2 = reinterpret_cast<uint32_t*>(p + off);
   off += a256(4 * static_cast<size_t>(L) * (H / 128));
+  const size_t nb1 = static_cast<size_t>((H + kNvKB - 1) / kNvKB), nb2 = static_cast<size_t>((N + kNvKB - 1) / kNvKB);
   w.ximg = p + off;
-  off += a256(static_cast<size_t>(H / 64) * w.tok * 128);
+  off += a256(nb1 * w.tok * 128);
+  w.xsc = p + off;
+  off += a256(nb1 * w.tok * 16);
   w.himg = p + off;
-  off += a256(static_cast<size_t>(N / 64) * w.Rp * 128);
+  off += a256(nb2 * w.Rp * 128);
+  w.hsc = p + off;
+  off += a256(nb2 * w.Rp * 16);
   w.obuf = reinterpret_cast<__nv_bfloat16*>(p + off);
   off += a256(2 * static_cast<size_t>(M) * top_k * H);
   w.part = reinterpret_cast<float*>(p + off);
@@ -990,7 +964,9 @@ int routed_nvfp4(const void* x, const int32_t* ids, const float* weights, const 
   a.cnt1 = w.cnt1;
   a.cnt2 = w.cnt2;
   a.ximg = w.ximg;
+  a.xsc = w.xsc;
   a.himg = w.himg;
+  a.hsc = w.hsc;
   a.obuf = w.obuf;
   a.part = w.part;
   a.M = M;
@@ -1002,12 +978,14 @@ int routed_nvfp4(const void* x, const int32_t* ids, const float* weights, const 
   a.Rp = w.Rp;
   a.limit = limit;
   a.timeout_ns = wait_timeout_ns();
+  const unsigned long long nb1 = static_cast<unsigned long long>((H + kNvKB - 1) / kNvKB);
+  const unsigned long long nb2 = static_cast<unsigned long long>((N + kNvKB - 1) / kNvKB);
   if (!nv_map(&a.map13, w13, static_cast<unsigned long long>(L) * 2 * N, H / 2, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !nv_map(&a.map2, w2, static_cast<unsigned long long>(L) * H, N / 2, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !nv_map(&a.mapx, w.ximg, static_cast<unsigned long long>(H / 64) * w.tok, 128, 128, 4 * w.tok,
-              CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !nv_map(&a.maph, w.himg, static_cast<unsigned long long>(N / 64) * w.Rp, 128, 128, w.tok,
-              CU_TENSOR_MAP_SWIZZLE_128B))
+      !nv_map(&a.mapx, w.ximg, nb1 * w.tok, 128, 128, w.tok, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !nv_map(&a.mapxs, w.xsc, nb1 * w.tok, 16, 16, w.tok, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !nv_map(&a.maph, w.himg, nb2 * w.Rp, 128, 128, w.tok, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !nv_map(&a.maphs, w.hsc, nb2 * w.Rp, 16, 16, w.tok, CU_TENSOR_MAP_SWIZZLE_NONE))
     return set_last_error(FME_ECUDA, "cuTensorMapEncodeTiled failed or unavailable");
   return w.tok == 16 ? nv_launch<16>(a, st) : nv_launch<kMaxTokens>(a, st);
 }
