@@ -105,7 +105,7 @@ struct NvSmem {
   uint64_t fullB[NvCfg<TOK>::kBStages], emptyB[NvCfg<TOK>::kBStages];
   uint64_t sffull[NvCfg<TOK>::kSfBuf], sffree[NvCfg<TOK>::kSfBuf], accfull[2], tmemfree[2], final_bar;
   float ysm[16][128];
-  uint4 sc[4][kNvScaleAhead][4][32];  // [scale warp][K block slot][c][lane]: scales of weight row lane + 32c
+  uint4 sc[kNvScaleAhead][128];  // weight group scales of the next K blocks, by row
   unsigned long long tokmask[kMaxExperts];
   int16_t ulist[kMaxExperts];
   int16_t uidx[kMaxExperts];      // local expert -> unit
@@ -674,12 +674,13 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
     }
   } else if (warp < 7) {
     // ------------------------------------------------------------ scale vectors -> TMEM
-    // Per K block and MMA j: lane r of each lane quadrant, column c holds the
-    // four UE4M3 scales of row r + 32c (A: weight rows, B: token columns),
-    // written identically into all four quadrants (each warp writes its own,
-    // from its own copies of the weight scales, so the warps never wait on
-    // one another).
+    // Per K block, MMA j reads four TMEM columns of scale vectors (four
+    // UE4M3 bytes per 32-bit cell, groups 4j .. 4j + 3): for A, weight row m
+    // from lane m, column m / 32; for B, token column n from lane n % 32,
+    // column n / 32, in each lane quadrant. So each warp writes its own
+    // quadrant: its 32 weight rows (in every column) and all token columns.
     const int quad = warp & 3;
+    const int srow = quad * 32 + lane;  // weight row = TMEM lane
     const uint32_t tq = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     // The 16 scale bytes of weight row `row` of K block q: two 8-byte copies
     // (rows are 8-byte aligned); the second is zeros when the block's second
@@ -700,10 +701,7 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
       cp_async8(dst, src);
       cp_async8(reinterpret_cast<uint8_t*>(dst) + 8, full ? src + 8 : src, full ? 8u : 0u);
     };
-    auto fetch = [&](int slot, const NvStep& q) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) fetch_row(&S.sc[quad][slot][c][lane], q, lane + 32 * c);
-    };
+    auto fetch = [&](int slot, const NvStep& q) { fetch_row(&S.sc[slot][srow], q, srow); };
     // Slot n % kNvScaleAhead holds K block n; a refill goes to the slot read
     // one iteration earlier (each thread reads only its own copies).
     NvCursor ahead{P[0].lo, 1};
@@ -719,13 +717,15 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
       const int sb = k % kSB, sf = k % C::kSfBuf;
       cp_async_wait<kNvScaleAhead - 2>();  // this thread's scales of K block k have landed
       uint32_t ra[16], rb[16];
+      {
+        const uint4 w = S.sc[k % kNvScaleAhead][srow];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint4 w = S.sc[quad][k % kNvScaleAhead][c][lane];
-        ra[c] = w.x;
-        ra[4 + c] = w.y;
-        ra[8 + c] = w.z;
-        ra[12 + c] = w.w;
+        for (int c = 0; c < 4; ++c) {
+          ra[c] = w.x;
+          ra[4 + c] = w.y;
+          ra[8 + c] = w.z;
+          ra[12 + c] = w.w;
+        }
       }
       if (ahead.next(P, qa)) fetch((k + kNvScaleAhead - 1) % kNvScaleAhead, qa);
       cp_async_commit();
