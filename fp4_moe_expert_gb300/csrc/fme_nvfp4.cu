@@ -117,9 +117,11 @@ struct NvSmem {
   volatile int abort;
 };
 
+// At least 120 KB are requested whatever the rings take, so that a second
+// CTA never fits on the SM (see below).
 template <int TOK>
 constexpr size_t nv_smem_bytes() {
-  return sizeof(NvSmem<TOK>) + 1024;
+  return sizeof(NvSmem<TOK>) + 1024 > 120 * 1024 ? sizeof(NvSmem<TOK>) + 1024 : 120 * 1024;
 }
 static_assert(nv_smem_bytes<16>() <= 232448 && nv_smem_bytes<64>() <= 232448, "shared memory per CTA");
 static_assert(128 + 32 * NvCfg<16>::kSfBuf <= kNvTmemCols && 128 + 32 * NvCfg<64>::kSfBuf <= kNvTmemCols,
