@@ -232,25 +232,44 @@ struct NvStep {
 
 struct NvCursor {
   int pos, phase;
+  int u = 0, T = 0, kb = 0;  // of slot pos, once `at` is set (kept by increments, no divisions)
+  bool at = false;
   __device__ bool next(const NvPhase (&P)[2], NvStep& st) {
     while (true) {
       const NvPhase& p = P[phase - 1];
-      if (pos < p.lo) pos = p.lo;
+      if (pos < p.lo) {
+        pos = p.lo;
+        at = false;
+      }
       if (pos < p.hi) {
-        const int tile = pos / p.nb;
+        if (!at) {
+          const int tile = pos / p.nb;
+          kb = pos - tile * p.nb;
+          u = tile / p.tiles;
+          T = tile - u * p.tiles;
+          at = true;
+        }
         st.phase = phase;
-        st.u = tile / p.tiles;
-        st.T = tile - st.u * p.tiles;
-        st.t0 = tile * p.nb;
-        st.kb = pos - st.t0;
-        st.first = pos == p.lo || st.kb == 0;
-        st.last = pos + 1 == p.hi || st.kb == p.nb - 1;
+        st.u = u;
+        st.T = T;
+        st.kb = kb;
+        st.t0 = pos - kb;
+        st.first = pos == p.lo || kb == 0;
+        st.last = pos + 1 == p.hi || kb == p.nb - 1;
         ++pos;
+        if (++kb == p.nb) {
+          kb = 0;
+          if (++T == p.tiles) {
+            T = 0;
+            ++u;
+          }
+        }
         return true;
       }
       if (phase == 2) return false;
       phase = 2;
       pos = P[1].lo;
+      at = false;
     }
   }
 };
