@@ -55,6 +55,8 @@ def parse_args():
                     help="experts resident on the device (smaller for profiler captures; 32 x 44 MB = 1.4 GB)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--nvfp4-launches", action="store_true",
+                    help="only launch the NVFP4 slot MoE twice at each of M = 1, 8, 64 (for profiler launch lists)")
     return ap.parse_args()
 
 
@@ -480,13 +482,12 @@ def side_measurements(fme, dev, args):
                                          "GBps": round(shared_bytes / (us * 1e-6) / 1e9, 1)}
     # NVFP4 slot MoE: 48 local experts of a 384-expert router (bytes = unique
     # local experts x 37,158,912 B of packed E2M1 weights + UE4M3 scales).
-    from oracle import routing
     ncfg = W.NVFP4
     nw = W.nvfp4_weights_device(ncfg, args.seed, dev)
     per_expert = 6144 * 3584 + 7168 * 1536 + 6144 * 448 + 7168 * 192
     for M in ncfg.Ms:
-        x, logits, rbias = W.nvfp4_activations(ncfg, M, args.seed, 5)
-        ids, wts, _ = routing.route(logits, rbias, ncfg.top_k, 1.0)
+        x = W.nvfp4_activations(ncfg, M, args.seed, 5)[0]
+        ids, wts = W.nvfp4_routes(ncfg, M, args.seed, 5)
         uniq = len({int(e) for e in ids.reshape(-1) if ncfg.e0 <= e < ncfg.e0 + ncfg.L})
         xd = torch.from_numpy(x).to(dev).to(torch.bfloat16)
         idd, wd = torch.from_numpy(ids).to(dev), torch.from_numpy(wts).to(dev)
@@ -507,8 +508,31 @@ def side_measurements(fme, dev, args):
     return res
 
 
+def nvfp4_launches(args):
+    """Two NVFP4 slot-MoE calls at each of M = 1, 8, 64 on the 48-expert workload, nothing
+    else: the command the profiler launch lists of this kernel are taken on."""
+    import torch
+    import fp4_moe_expert_gb300 as fme
+    from synth import workloads as W
+    dev = torch.device("cuda", 0)
+    ncfg = W.NVFP4
+    nw = W.nvfp4_weights_device(ncfg, args.seed, dev)
+    for M in (1, 8, 64):
+        x = W.nvfp4_activations(ncfg, M, args.seed, 5)[0]
+        ids, wts = W.nvfp4_routes(ncfg, M, args.seed, 5)
+        xd = torch.from_numpy(x).to(dev).to(torch.bfloat16)
+        idd, wd = torch.from_numpy(ids).to(dev), torch.from_numpy(wts).to(dev)
+        for _ in range(2):
+            fme.moe_routed_nvfp4(xd, idd, wd, *nw, ncfg.e0, ncfg.limit)
+        torch.cuda.synchronize()
+    print(json.dumps({"nvfp4_launches": 6}))
+
+
 def main():
     args = parse_args()
+    if args.nvfp4_launches:
+        nvfp4_launches(args)
+        return
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
