@@ -51,8 +51,15 @@ constexpr int kMaxKc = 16;
 // mixes experts hit by different token counts. Every wave adds split tiles,
 // each with a partial round trip. Measured on the DeepSeek-V3 shape: three
 // waves pay off at 5-8 tokens (M = 8: 414 -> 389 us); at 1-4 tokens two
-// waves were slower than one.
+// waves were slower than one. With the shared expert as one more unit (the
+// one-launch layer, run as one launch up to 4 tokens) two waves pay off at
+// 3-4 tokens (M = 4: 269 -> 244 us).
 __host__ __device__ constexpr int max_waves(int ptok) { return ptok > 4 && ptok <= 8 ? 3 : 1; }
+__host__ __device__ constexpr int layer_waves(int ptok) { return ptok > 2 && ptok <= 4 ? 2 : 1; }
+// Waves the partial-sum region is sized for, any call.
+__host__ __device__ constexpr int waves_cap(int ptok) {
+  return max_waves(ptok) > layer_waves(ptok) ? max_waves(ptok) : layer_waves(ptok);
+}
 
 struct TcArgs {
   CUtensorMap map13;   // routed W13 as [E * 2I rows, H bytes], box 64 rows x 128 bytes
@@ -818,7 +825,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
   P.kcmax = min(kMaxKc, kTmemBuf / P.N);
   P.c = blockIdx.x;
   P.G = gridDim.x;
-  P.W = min(P.U, max_waves(a.ptok));
+  P.W = min(P.U, a.has_shared ? layer_waves(a.ptok) : max_waves(a.ptok));
   P.tiles[0] = a.I / 64;
   P.nb[0] = a.H / 128;
   P.tiles[1] = a.H / 128;
@@ -1061,15 +1068,18 @@ static TcWorkspace tc_layout(void* base, int M, int routes, int H, int I, int E)
   off += align256(4 * static_cast<size_t>(routes) * I);
   w.ptok = M < kMaxTokens ? M : kMaxTokens;
   w.part = reinterpret_cast<float*>(p + off);
-  off += align256(4 * static_cast<size_t>(max_waves(w.ptok)) * 2 * kFp8MaxCtas * 2 * w.ptok * 128);
+  off += align256(4 * static_cast<size_t>(waves_cap(w.ptok)) * 2 * kFp8MaxCtas * 2 * w.ptok * 128);
   w.bytes = off;
   return w;
 }
 
+// lay_routes / lay_slots: hidden rows and counter slots of the workspace
+// layout (by default this call's own).
 static int launch_tc(TcArgs& a, const uint8_t* w13, const uint8_t* w2, const uint8_t* sw13, const uint8_t* sw2,
-                     void* workspace, size_t workspace_bytes, cudaStream_t st) {
-  const int routes = a.M * a.top_k + (a.has_shared ? a.M : 0);
-  const TcWorkspace w = tc_layout(workspace, a.M, routes, a.H, a.I, a.E + 1);
+                     void* workspace, size_t workspace_bytes, cudaStream_t st, int lay_routes = -1,
+                     int lay_slots = -1) {
+  const int routes = lay_routes >= 0 ? lay_routes : a.M * a.top_k + (a.has_shared ? a.M : 0);
+  const TcWorkspace w = tc_layout(workspace, a.M, routes, a.H, a.I, lay_slots >= 0 ? lay_slots : a.E + 1);
   if (workspace == nullptr || workspace_bytes < w.bytes)
     return set_last_error(FME_EWORKSPACE, "workspace of %zu bytes needed, %zu given", w.bytes, workspace_bytes);
   a.err = w.err;
@@ -1109,8 +1119,28 @@ static int launch_tc(TcArgs& a, const uint8_t* w13, const uint8_t* w2, const uin
   return FME_OK;
 }
 
+static int layer_launch(const RoutedFp8& r, const SharedFp8& sh, int M, int H, int I, void* workspace,
+                        size_t workspace_bytes, cudaStream_t st, int lay_routes, int lay_slots);
+
 int layer_fp8(const RoutedFp8& r, const SharedFp8& sh, int M, int H, int I, void* workspace, size_t workspace_bytes,
               cudaStream_t st) {
+  // Above 4 tokens the shared expert as the last unit of the routed schedule
+  // costs more than it saves (M = 8: 490 us in one launch against 418 us for
+  // the two calls): run it alone, then the routed experts, on the stream.
+  // Both launches use the one-launch call's workspace layout (the shared
+  // expert alone takes counter slot 0, zero before and after it), and each
+  // leaves the zeroed prefix zero for the next.
+  if (r.E > 0 && sh.w13 != nullptr && M > 4) {
+    const int lay_routes = M * r.top_k + M, lay_slots = r.E + 1;
+    const int err = layer_launch(RoutedFp8{}, sh, M, H, I, workspace, workspace_bytes, st, lay_routes, lay_slots);
+    if (err != FME_OK) return err;
+    return layer_launch(r, SharedFp8{}, M, H, I, workspace, workspace_bytes, st, lay_routes, lay_slots);
+  }
+  return layer_launch(r, sh, M, H, I, workspace, workspace_bytes, st, -1, -1);
+}
+
+static int layer_launch(const RoutedFp8& r, const SharedFp8& sh, int M, int H, int I, void* workspace,
+                        size_t workspace_bytes, cudaStream_t st, int lay_routes, int lay_slots) {
   TcArgs a;
   memset(&a, 0, sizeof(a));
   a.M = M;
@@ -1143,7 +1173,7 @@ int layer_fp8(const RoutedFp8& r, const SharedFp8& sh, int M, int H, int I, void
     a.slimit = sh.limit;
     a.sue8m0 = sh.ue8m0 ? 1 : 0;
   }
-  return launch_tc(a, r.w13, r.w2, sh.w13, sh.w2, workspace, workspace_bytes, st);
+  return launch_tc(a, r.w13, r.w2, sh.w13, sh.w2, workspace, workspace_bytes, st, lay_routes, lay_slots);
 }
 
 // Counter slots are sized for the routed experts plus the shared expert

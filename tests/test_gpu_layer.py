@@ -72,7 +72,7 @@ def _check_layer(fme, cfg, scfg, M, seed, ws=None, shared_ws=None):
     _close(sout, sout2, "shared")
 
 
-@pytest.mark.parametrize("M", [1, 5, 64])
+@pytest.mark.parametrize("M", [1, 4, 5, 64])
 @pytest.mark.parametrize("shared_ue8m0", [False, True])
 def test_layer_small_matches_oracle_and_separate_calls(fme, M, shared_ue8m0):
     scfg = W.SharedConfig("small_shared", W.RAGGED.H, W.RAGGED.I, 5.0, shared_ue8m0)
