@@ -18,6 +18,9 @@ Sources (cited by page title and section in every function):
   ``block_scales``.
 * "nvfp4-megamoe-kernel README.md" — "Data Formats", "Bugs Found & Fixed"
   sections 1, 2, 6 and 7 (slot pipeline, E2M1 staging, routing weights once).
+* "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.ep.comm" —
+  ``EpCombine`` (the routing-weighted sum, FP32 in a fixed order, one BF16
+  rounding): the local finalize.
 
 Pins: every function here is checked in ``tests/test_oracle_*.py`` against
 something other than itself (closed forms, exhaustive code tables, library
@@ -25,4 +28,4 @@ casts, brute force on tiny inputs, algebraic identities, invariants). No
 function is "parity unpinned".
 """
 
-from . import codecs, routing, quant, moe_fp8, moe_nvfp4  # noqa: F401
+from . import codecs, routing, quant, moe_fp8, moe_nvfp4, finalize  # noqa: F401
