@@ -40,6 +40,7 @@ SIGNATURES = {
     "fme_moe_routed_nvfp4": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                       _c_int, _c_float, _vp, _vp, _c_size, _vp]),
     "fme_moe_routed_nvfp4_workspace": (_c_size, [_c_int] * 5),
+    "fme_moe_finalize": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp]),
     "fme_workspace_clear": (_c_int, [_vp, _c_size, _vp]),
     "fme_selftest_wait_timeout": (_c_int, [_vp, _c_size, _c_int, _vp]),
     "fme_workspace_error": (_c_int, [_vp, ctypes.POINTER(_c_int), _vp]),
@@ -241,6 +242,24 @@ def moe_layer_fp8(x, logits, bias, w13, s13, w2, s2, top_k, limit, scale, ue8m0,
                                  float(shared_limit), int(bool(shared_ue8m0)), _ptr(out), _ptr(ids),
                                  _ptr(weights), _ptr(shared_out), ws.ptr(), ws.nbytes, _stream(dev)))
     return out, ids, weights, shared_out
+
+
+def moe_finalize(out, weights, shared_out=None, y=None):
+    """y [M, H] BF16 = bf16(sum over r of weights[t, r] * out[t * top_k + r] (+ shared_out[t]))
+    (fme_moe_finalize): out [M * top_k, H] BF16 unweighted expert rows as the routed
+    call returns them, weights [M, top_k] FP32, shared_out [M, H] BF16 or None."""
+    dev = out.device
+    M, top_k = weights.shape
+    H = out.shape[1]
+    _need(out, torch.bfloat16, (M * top_k, H), "out")
+    _need(weights, torch.float32, (M, top_k), "weights")
+    if shared_out is not None:
+        _need(shared_out, torch.bfloat16, (M, H), "shared_out")
+    if y is None:
+        y = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    _need(y, torch.bfloat16, (M, H), "y")
+    _check(lib.fme_moe_finalize(_ptr(out), _ptr(weights), _ptr(shared_out), M, H, top_k, _ptr(y), _stream(dev)))
+    return y
 
 
 def ue8m0_unpack(packed, n, k, check=True):

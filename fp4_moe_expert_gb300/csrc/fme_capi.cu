@@ -275,6 +275,18 @@ int fme_ue8m0_unpack(const int32_t* packed, int n, int k, float* dst, int check,
   return ue8m0_unpack(packed, n, k, dst, check, mismatch, static_cast<cudaStream_t>(stream));
 }
 
+int fme_moe_finalize(const void* out, const float* weights, const void* shared_out, int M, int H, int top_k,
+                     void* y, void* stream) {
+  FME_REQUIRE(out && weights && y, FME_EINVAL, "null pointer argument");
+  FME_REQUIRE(M >= 1 && M <= (1 << 20), FME_EINVAL, "M=%d outside [1, 2^20]", M);
+  FME_REQUIRE(H >= 8 && H % 8 == 0 && H <= (1 << 20), FME_EINVAL, "H=%d must be a positive multiple of 8", H);
+  FME_REQUIRE(top_k >= 1 && top_k <= kMaxTopK, FME_EINVAL, "top_k=%d outside [1, %d]", top_k, kMaxTopK);
+  FME_REQUIRE(!misaligned(out) && !misaligned(y) && (shared_out == nullptr || !misaligned(shared_out)) &&
+                  reinterpret_cast<uintptr_t>(weights) % 4 == 0,
+              FME_EALIGN, "out, shared_out and y must be 16-byte aligned, weights 4-byte aligned");
+  return finalize(out, weights, shared_out, M, H, top_k, y, static_cast<cudaStream_t>(stream));
+}
+
 size_t fme_moe_routed_nvfp4_workspace(int M, int H, int N, int L, int top_k) {
   if (M < 1 || M > kMaxTokens || H < 128 || H % 128 || N < 128 || N % 128 || L < 1 || L > kMaxExperts ||
       top_k < 1 || top_k > kMaxTopK || H > 8192 || N > 8192)

@@ -65,6 +65,10 @@ int layer_fp8(const RoutedFp8& r, const SharedFp8& sh, int M, int H, int I, void
 size_t layer_fp8_workspace_bytes(int M, int H, int I, int E, int top_k, bool shared);
 size_t layer_fp8_zero_bytes(int M, int H, int I, int E, int top_k, bool shared);
 
+// y[t] = bf16(sum_r w[t, r] * out[t * top_k + r] (+ shared_out[t])) (arguments validated).
+int finalize(const void* out, const float* weights, const void* shared_out, int M, int H, int top_k, void* y,
+             cudaStream_t st);
+
 int routed_nvfp4(const void* x, const int32_t* ids, const float* weights, const uint8_t* w13, const uint8_t* s13,
                  const uint8_t* w2, const uint8_t* s2, int M, int H, int N, int L, int e0, int top_k, float limit,
                  void* y, void* workspace, size_t workspace_bytes, cudaStream_t st);

@@ -193,6 +193,30 @@ int fme_moe_layer_fp8(const void* x, const void* logits, int logits_dtype, const
 size_t fme_moe_layer_fp8_workspace(int M, int H, int I, int E, int top_k);
 
 /*
+ * Local finalize: y[t] = bf16(sum over r = 0 .. top_k-1, in that order, of
+ * weights[t, r] * out[t * top_k + r], plus shared_out[t] when given).
+ *
+ * Sources: "vllm.models.glm5next.nvidia.specialized_decode.mega_moe" (the
+ * routed kernel returns unweighted rows t * top_k + r and the routing weights,
+ * combined by a finalize step) and "vllm.models.kimi_k3.nvidia.
+ * specialized_decode.cutedsl.moe.ep.comm" (EpCombine: the routing-weighted
+ * sum, an FP32 sum in a fixed order, rounded once to BF16). Each product and
+ * each sum is one FP32 rounding (no fused multiply-add); the shared row is
+ * added after the routed sum; one BF16 rounding at the end.
+ *
+ * Arguments: out [M * top_k, H] BF16 (the routed call's out), weights
+ * [M, top_k] FP32 (its weights), shared_out [M, H] BF16 or NULL (the shared
+ * expert's out), y [M, H] BF16. 1 <= M <= 2^20, H a positive multiple of 8,
+ * 1 <= top_k <= 32. out, shared_out and y 16-byte aligned, weights 4-byte
+ * aligned; y must not overlap the inputs. Caller-owned buffers, no
+ * workspace. Asynchronous on `stream`; the launch allows programmatic
+ * dependent launch and waits for the preceding kernel before reading.
+ * Returns FME_OK, FME_EINVAL, FME_EALIGN or FME_ECUDA.
+ */
+int fme_moe_finalize(const void* out, const float* weights, const void* shared_out, int M, int H, int top_k,
+                     void* y, void* stream);
+
+/*
  * Packed UE8M0 block scales -> FP32 block scales.
  *
  * Source: "vllm.models.glm5next.nvidia.specialized_decode.shared_expert",

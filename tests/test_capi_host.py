@@ -79,10 +79,22 @@ def test_nvfp4_and_unpack_validation(fme):
     assert fme.lib.fme_ue8m0_unpack(None, 128, 512, vp(16), 0, None, None) == -1
 
 
+def test_finalize_validation(fme):
+    vp = ctypes.c_void_p
+    fin = fme.lib.fme_moe_finalize
+    assert fin(vp(16), vp(16), None, 1, 7168, 8, None, None) == -1       # y missing
+    assert fin(vp(16), vp(16), None, 0, 7168, 8, vp(16), None) == -1     # M
+    assert fin(vp(16), vp(16), None, 2, 7164, 8, vp(16), None) == -1     # H not a multiple of 8
+    assert fin(vp(16), vp(16), None, 2, 7168, 33, vp(16), None) == -1    # top_k
+    assert fin(vp(24), vp(16), None, 2, 7168, 8, vp(16), None) == -3     # out misaligned
+    assert fin(vp(16), vp(18), None, 2, 7168, 8, vp(16), None) == -3     # weights misaligned
+    assert fin(vp(16), vp(16), vp(8), 2, 7168, 8, vp(16), None) == -3    # shared_out misaligned
+
+
 def test_binding_exposes_a_wrapper_per_entry_point(fme):
     for name in ("moe_routed_fp8", "moe_routed_fp8_workspace", "moe_layer_fp8", "moe_layer_fp8_workspace",
                  "shared_expert_fp8", "shared_expert_fp8_workspace", "moe_routed_nvfp4",
-                 "moe_routed_nvfp4_workspace", "ue8m0_unpack"):
+                 "moe_routed_nvfp4_workspace", "ue8m0_unpack", "moe_finalize"):
         assert callable(getattr(fme, name)), name
 
 
