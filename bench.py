@@ -434,6 +434,13 @@ def layer_measurements(fme, dev, args, shared_w, shared_bytes, flush):
         us_sep = _event_us(separate, flush)
         us_fused = _event_us(fused, flush)
         us_shared = _event_us(lambda: fme.shared_expert_fp8(xd, *shared, workspace=ws_s), flush)
+        # local finalize of the layer's outputs: y = bf16(sum_r w * out + shared_out)
+        lo, _, lw, lso = outs["l"]
+        ybuf = torch.empty(M, cfg.H, dtype=torch.bfloat16, device=dev)
+        us_fin = _event_us(lambda: fme.moe_finalize(lo, lw, lso, y=ybuf), flush)
+        us_layer_y = _event_us(lambda: fme.moe_finalize(*(lambda r: (r[0], r[2], r[3]))(
+            fme.moe_layer_fp8(*routed, *shared, workspace=ws_l)), y=ybuf), flush)
+        fin_bytes = (M * cfg.top_k * cfg.H + 2 * M * cfg.H) * 2 + M * cfg.top_k * 4
         for w in (ws_r, ws_s, ws_l):
             if w.error() != 0:
                 raise RuntimeError("device wait timed out in the layer measurement")
@@ -448,6 +455,9 @@ def layer_measurements(fme, dev, args, shared_w, shared_bytes, flush):
             "one_launch_layer_us": round(us_fused, 2),
             "one_launch_layer_GBps": round(nbytes / (us_fused * 1e-6) / 1e9, 1),
             "shared_then_routed_GBps": round(nbytes / (us_sep * 1e-6) / 1e9, 1),
+            "finalize_us": round(us_fin, 2),
+            "finalize_GBps": round(fin_bytes / (us_fin * 1e-6) / 1e9, 1),
+            "layer_plus_finalize_us": round(us_layer_y, 2),
         }
     del w13, w2
     return res
