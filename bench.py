@@ -492,21 +492,23 @@ def side_measurements(fme, dev, args):
                                          "GBps": round(shared_bytes / (us * 1e-6) / 1e9, 1)}
     # NVFP4 slot MoE: 48 local experts of a 384-expert router (bytes = unique
     # local experts x 37,158,912 B of packed E2M1 weights + UE4M3 scales).
+    # Routing fused in (fme_moe_layer_nvfp4): the router's logits and bias over its
+    # 384 experts pick the routes; unique local experts counted from the kernel's ids.
     ncfg = W.NVFP4
     nw = W.nvfp4_weights_device(ncfg, args.seed, dev)
     per_expert = 6144 * 3584 + 7168 * 1536 + 6144 * 448 + 7168 * 192
     for M in ncfg.Ms:
-        x = W.nvfp4_activations(ncfg, M, args.seed, 5)[0]
-        ids, wts = W.nvfp4_routes(ncfg, M, args.seed, 5)
-        uniq = len({int(e) for e in ids.reshape(-1) if ncfg.e0 <= e < ncfg.e0 + ncfg.L})
+        x, logits, rbias = W.nvfp4_activations(ncfg, M, args.seed, 5)
         xd = torch.from_numpy(x).to(dev).to(torch.bfloat16)
-        idd, wd = torch.from_numpy(ids).to(dev), torch.from_numpy(wts).to(dev)
+        ld, bd = torch.from_numpy(logits).to(dev), torch.from_numpy(rbias).to(dev)
+        _, ids, _ = fme.moe_layer_nvfp4(xd, ld, bd, *nw, ncfg.e0, ncfg.top_k, 1.0, ncfg.limit)
+        uniq = len({int(e) for e in ids.reshape(-1).tolist() if ncfg.e0 <= e < ncfg.e0 + ncfg.L})
         ts = []
         for i in range(25):
             flush.amax()  # reads 512 MB: L2 holds none of the weights, and no dirty lines
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
-            fme.moe_routed_nvfp4(xd, idd, wd, *nw, ncfg.e0, ncfg.limit)
+            fme.moe_layer_nvfp4(xd, ld, bd, *nw, ncfg.e0, ncfg.top_k, 1.0, ncfg.limit)
             b.record()
             torch.cuda.synchronize()
             if i >= 5:
@@ -519,8 +521,9 @@ def side_measurements(fme, dev, args):
 
 
 def nvfp4_launches(args):
-    """Two NVFP4 slot-MoE calls at each of M = 1, 8, 64 on the 48-expert workload, nothing
-    else: the command the profiler launch lists of this kernel are taken on."""
+    """Two NVFP4 slot-MoE calls (routing fused in) at each of M = 1, 8, 64 on the
+    48-expert workload, nothing else: the command the profiler launch lists of this
+    kernel are taken on."""
     import torch
     import fp4_moe_expert_gb300 as fme
     from synth import workloads as W
@@ -528,12 +531,11 @@ def nvfp4_launches(args):
     ncfg = W.NVFP4
     nw = W.nvfp4_weights_device(ncfg, args.seed, dev)
     for M in (1, 8, 64):
-        x = W.nvfp4_activations(ncfg, M, args.seed, 5)[0]
-        ids, wts = W.nvfp4_routes(ncfg, M, args.seed, 5)
+        x, logits, rbias = W.nvfp4_activations(ncfg, M, args.seed, 5)
         xd = torch.from_numpy(x).to(dev).to(torch.bfloat16)
-        idd, wd = torch.from_numpy(ids).to(dev), torch.from_numpy(wts).to(dev)
+        ld, bd = torch.from_numpy(logits).to(dev), torch.from_numpy(rbias).to(dev)
         for _ in range(2):
-            fme.moe_routed_nvfp4(xd, idd, wd, *nw, ncfg.e0, ncfg.limit)
+            fme.moe_layer_nvfp4(xd, ld, bd, *nw, ncfg.e0, ncfg.top_k, 1.0, ncfg.limit)
         torch.cuda.synchronize()
     print(json.dumps({"nvfp4_launches": 6}))
 

@@ -41,6 +41,8 @@ SIGNATURES = {
                                       _c_int, _c_float, _vp, _vp, _c_size, _vp]),
     "fme_moe_routed_nvfp4_workspace": (_c_size, [_c_int] * 5),
     "fme_moe_finalize": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp]),
+    "fme_moe_layer_nvfp4": (_c_int, [_vp, _vp, _c_int, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                     _c_int, _c_int, _c_int, _c_float, _c_float, _vp, _vp, _vp, _vp, _c_size, _vp]),
     "fme_workspace_clear": (_c_int, [_vp, _c_size, _vp]),
     "fme_selftest_wait_timeout": (_c_int, [_vp, _c_size, _c_int, _vp]),
     "fme_workspace_error": (_c_int, [_vp, ctypes.POINTER(_c_int), _vp]),
@@ -305,6 +307,41 @@ def moe_routed_nvfp4(x, topk_ids, topk_weights, w13, s13, w2, s2, e0, limit=floa
                                     _ptr(s2), M, H, N, L, int(e0), top_k, float(limit), _ptr(y), ws.ptr(),
                                     ws.nbytes, _stream(dev)))
     return y
+
+
+def moe_layer_nvfp4(x, logits, bias, w13, s13, w2, s2, e0, top_k, scale=1.0, limit=float("inf"), y=None,
+                    workspace=None):
+    """NVFP4 slot MoE with the routing fused in (fme_moe_layer_nvfp4): logits [M, E]
+    FP32 or BF16 and bias [E] FP32 pick top_k of E experts per token; the slots of the
+    local experts [e0, e0 + L) run as in moe_routed_nvfp4. Returns (y, ids, weights)."""
+    M, H = x.shape
+    E = logits.shape[1]
+    L, n2, _ = w13.shape
+    N = n2 // 2
+    dev = x.device
+    _need(x, torch.bfloat16, (M, H), "x")
+    if logits.dtype == torch.float32:
+        dt = FME_F32
+    elif logits.dtype == torch.bfloat16:
+        dt = FME_BF16
+    else:
+        raise ValueError("logits must be float32 or bfloat16")
+    _need(logits, logits.dtype, (M, E), "logits")
+    _need(bias, torch.float32, (E,), "bias")
+    _need(w13, torch.uint8, (L, 2 * N, H // 2), "w13")
+    _need(s13, torch.uint8, (L, 2 * N, H // 16), "s13")
+    _need(w2, torch.uint8, (L, H, N // 2), "w2")
+    _need(s2, torch.uint8, (L, H, N // 16), "s2")
+    if y is None:
+        y = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    ids = torch.empty(M, top_k, dtype=torch.int32, device=dev)
+    weights = torch.empty(M, top_k, dtype=torch.float32, device=dev)
+    need = moe_routed_nvfp4_workspace(M, H, N, L, top_k)
+    ws = _workspace(need, dev, workspace)
+    _check(lib.fme_moe_layer_nvfp4(_ptr(x), _ptr(logits), dt, _ptr(bias), _ptr(w13), _ptr(s13), _ptr(w2), _ptr(s2),
+                                   M, H, N, L, E, int(e0), int(top_k), float(scale), float(limit), _ptr(y),
+                                   _ptr(ids), _ptr(weights), ws.ptr(), ws.nbytes, _stream(dev)))
+    return y, ids, weights
 
 
 def sm_count():

@@ -287,6 +287,39 @@ int fme_moe_finalize(const void* out, const float* weights, const void* shared_o
   return finalize(out, weights, shared_out, M, H, top_k, y, static_cast<cudaStream_t>(stream));
 }
 
+int fme_moe_layer_nvfp4(const void* x, const void* logits, int logits_dtype, const float* bias, const uint8_t* w13,
+                        const uint8_t* s13, const uint8_t* w2, const uint8_t* s2, int M, int H, int N, int L, int E,
+                        int e0, int top_k, float scale, float limit, void* y, int32_t* ids, float* weights,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  FME_REQUIRE(x && logits && bias && w13 && s13 && w2 && s2 && y && ids && weights, FME_EINVAL,
+              "null pointer argument");
+  FME_REQUIRE(M >= 1 && M <= kMaxTokens, FME_EUNSUPPORTED, "M=%d outside [1, %d]", M, kMaxTokens);
+  FME_REQUIRE(H >= 128 && H % 128 == 0 && N >= 128 && N % 128 == 0, FME_EINVAL,
+              "H=%d and N=%d must be positive multiples of 128", H, N);
+  FME_REQUIRE(H <= 8192 && N <= 8192, FME_EUNSUPPORTED, "H=%d or N=%d above 8192", H, N);
+  FME_REQUIRE(E >= 1 && E <= kMaxExperts, FME_EUNSUPPORTED, "E=%d outside [1, %d]", E, kMaxExperts);
+  FME_REQUIRE(L >= 1 && e0 >= 0 && e0 + L <= E, FME_EINVAL, "local range [%d, %d) outside [0, %d)", e0, e0 + L, E);
+  FME_REQUIRE(top_k >= 1 && top_k <= kMaxTopK && top_k <= E, FME_EINVAL, "top_k=%d outside [1, min(%d, E)]", top_k,
+              kMaxTopK);
+  FME_REQUIRE(logits_dtype == FME_F32 || logits_dtype == FME_BF16, FME_EINVAL, "logits_dtype=%d", logits_dtype);
+  FME_REQUIRE(std::isfinite(scale), FME_EINVAL, "scale must be finite");
+  FME_REQUIRE(limit > 0.0f, FME_EINVAL, "limit must be > 0");
+  FME_REQUIRE(!misaligned(x) && !misaligned(logits) && !misaligned(bias) && !misaligned(w13) && !misaligned(s13) &&
+                  !misaligned(w2) && !misaligned(s2) && !misaligned(y) && !misaligned(ids) && !misaligned(weights) &&
+                  !misaligned(workspace),
+              FME_EALIGN, "every pointer must be 16-byte aligned");
+  Nvfp4Routing r;
+  r.logits = logits;
+  r.logits_dtype = logits_dtype;
+  r.bias = bias;
+  r.E = E;
+  r.scale = scale;
+  r.ids = ids;
+  r.weights = weights;
+  return routed_nvfp4(x, nullptr, nullptr, w13, s13, w2, s2, M, H, N, L, e0, top_k, limit, y, workspace,
+                      workspace_bytes, static_cast<cudaStream_t>(stream), &r);
+}
+
 size_t fme_moe_routed_nvfp4_workspace(int M, int H, int N, int L, int top_k) {
   if (M < 1 || M > kMaxTokens || H < 128 || H % 128 || N < 128 || N % 128 || L < 1 || L > kMaxExperts ||
       top_k < 1 || top_k > kMaxTopK || H > 8192 || N > 8192)

@@ -58,4 +58,78 @@ __device__ __forceinline__ float warp_transpose_sum(float (&v)[V], int lane) {
   return s;
 }
 
+// ---------------------------------------------------------------- routing
+// One warp routes token t ("mega_moe" _MegaKernel.top_k_pick): sigmoid scores
+// (accurate expf, IEEE divide), keys score + bias as monotone uint32, top_k
+// rounds of warp max key then lowest expert among equals, weights
+// score / (float sum in pick order) * scale. Lane l holds experts l + 32 j in
+// registers; every load is issued before any sigmoid. Lane r < top_k gets
+// rank r's expert and weight.
+template <int J>
+__device__ void route_topk(const void* logits, bool logits_f32, const float* bias, int E, int top_k, float scale,
+                           int t, int lane, int& my_e, float& my_w) {
+  float lg[J], bs[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int e = lane + 32 * j;
+    lg[j] = 0.0f;
+    bs[j] = 0.0f;
+    if (e < E) {
+      if (logits_f32)
+        lg[j] = __ldg(static_cast<const float*>(logits) + static_cast<size_t>(t) * E + e);
+      else
+        lg[j] = __bfloat162float(static_cast<const __nv_bfloat16*>(logits)[static_cast<size_t>(t) * E + e]);
+      bs[j] = __ldg(bias + e);
+    }
+  }
+  uint32_t ky[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const float sgm = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-lg[j])));
+    lg[j] = sgm;  // score
+    ky[j] = (lane + 32 * j < E) ? ordered_key(__fadd_rn(sgm, bs[j])) : 0u;
+  }
+  float total = 0.0f, mine = 0.0f;
+  int mine_e = 0;
+  for (int r = 0; r < top_k; ++r) {
+    uint32_t best = 0u;
+#pragma unroll
+    for (int j = 0; j < J; ++j) best = max(best, ky[j]);
+    const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, best);
+    uint32_t cand = 0xFFFFFFFFu;
+#pragma unroll
+    for (int j = J - 1; j >= 0; --j)
+      if (ky[j] == top) cand = static_cast<uint32_t>(lane + 32 * j);
+    const int win = static_cast<int>(__reduce_min_sync(0xFFFFFFFFu, cand));
+    float sv = 0.0f;
+#pragma unroll
+    for (int j = 0; j < J; ++j)
+      if (lane + 32 * j == win) {
+        sv = lg[j];
+        ky[j] = 0u;
+      }
+    const float s = __shfl_sync(0xFFFFFFFFu, sv, win & 31);
+    total = __fadd_rn(total, s);
+    if (lane == r) {
+      mine = s;
+      mine_e = win;
+    }
+  }
+  my_e = mine_e;
+  my_w = __fmul_rn(__fdiv_rn(mine, total), scale);
+}
+
+// route_topk for any E <= kMaxExperts: the register loops sized to E.
+__device__ __forceinline__ void route_token_any(const void* logits, bool logits_f32, const float* bias, int E,
+                                                int top_k, float scale, int t, int lane, int& my_e, float& my_w) {
+  if (E <= 64)
+    route_topk<2>(logits, logits_f32, bias, E, top_k, scale, t, lane, my_e, my_w);
+  else if (E <= 256)
+    route_topk<8>(logits, logits_f32, bias, E, top_k, scale, t, lane, my_e, my_w);
+  else if (E <= 512)
+    route_topk<16>(logits, logits_f32, bias, E, top_k, scale, t, lane, my_e, my_w);
+  else
+    route_topk<kMaxExperts / 32>(logits, logits_f32, bias, E, top_k, scale, t, lane, my_e, my_w);
+}
+
 }  // namespace fme

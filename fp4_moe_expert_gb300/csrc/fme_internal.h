@@ -69,9 +69,23 @@ size_t layer_fp8_zero_bytes(int M, int H, int I, int E, int top_k, bool shared);
 int finalize(const void* out, const float* weights, const void* shared_out, int M, int H, int top_k, void* y,
              cudaStream_t st);
 
+// Routing fused into the NVFP4 call: picks from logits + bias over E experts
+// (the routed FP8 rule), written to ids / weights [M, top_k].
+struct Nvfp4Routing {
+  const void* logits = nullptr;
+  int logits_dtype = 0;
+  const float* bias = nullptr;
+  int E = 0;
+  float scale = 1.0f;
+  int32_t* ids = nullptr;
+  float* weights = nullptr;
+};
+
+// ids / weights: the caller's picks, or nullptr with `route` given.
 int routed_nvfp4(const void* x, const int32_t* ids, const float* weights, const uint8_t* w13, const uint8_t* s13,
                  const uint8_t* w2, const uint8_t* s2, int M, int H, int N, int L, int e0, int top_k, float limit,
-                 void* y, void* workspace, size_t workspace_bytes, cudaStream_t st);
+                 void* y, void* workspace, size_t workspace_bytes, cudaStream_t st,
+                 const Nvfp4Routing* route = nullptr);
 
 int ue8m0_unpack(const int32_t* packed, int n, int k, float* dst, int check, int* mismatch, cudaStream_t st);
 

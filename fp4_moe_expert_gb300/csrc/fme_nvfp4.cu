@@ -74,8 +74,16 @@ struct NvArgs {
   CUtensorMap maph;   // h image [nb2 * Rp rows, 128 bytes], box TOK rows, 128-byte swizzle
   CUtensorMap maphs;  // h image scales [nb2 * Rp rows, 16 bytes], box TOK rows
   const __nv_bfloat16* x;
-  const int32_t* ids;
+  const int32_t* ids;  // [M, top_k] caller's picks (route == 0)
   const float* tw;
+  // Fused routing (route != 0): picks from logits [M, E] + bias [E] by the
+  // routed FP8 kernel's rule, written to ids_out / tw_out by CTA 0.
+  const void* logits;
+  const float* bias;
+  int32_t* ids_out;
+  float* tw_out;
+  int route, E, logits_f32;
+  float scale;
   const uint8_t* s13;
   const uint8_t* s2;
   __nv_bfloat16* y;
@@ -112,6 +120,8 @@ struct NvSmem {
   int16_t uoff[kMaxExperts + 1];  // first compact slot row of each unit
   int16_t stok[kMaxTokens * kMaxTopK];
   int16_t sroute[kMaxTokens * kMaxTopK];
+  int32_t sid[kMaxTokens * kMaxTopK];  // every route's expert id and weight
+  float sw[kMaxTokens * kMaxTopK];
   uint32_t tmem_base;
   int U;
   volatile int abort;
@@ -473,6 +483,29 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
   __syncthreads();
   tc_fence_after();
 
+  // ---- the routes: the caller's picks, or this CTA's own routing of every
+  // token (one warp per token; CTA 0 writes them out)
+  if (a.route) {
+    for (int t = warp; t < a.M; t += kNvThreads / 32) {
+      int e;
+      float w;
+      route_token_any(a.logits, a.logits_f32 != 0, a.bias, a.E, a.top_k, a.scale, t, lane, e, w);
+      if (lane < a.top_k) {
+        S.sid[t * a.top_k + lane] = e;
+        S.sw[t * a.top_k + lane] = w;
+        if (c == 0) {
+          a.ids_out[t * a.top_k + lane] = e;
+          a.tw_out[t * a.top_k + lane] = w;
+        }
+      }
+    }
+  } else {
+    for (int i = tid; i < a.M * a.top_k; i += kNvThreads) {
+      S.sid[i] = __ldg(a.ids + i);
+      S.sw[i] = __ldg(a.tw + i);
+    }
+  }
+  __syncthreads();
   // ---- x image: token t, group g of 16 -> 8 packed bytes and a scale byte,
   // all CTAs share the work. Groups past H (an odd number of 128-value
   // halves) get zero data and zero scales, and so do the h image's scales of
@@ -515,7 +548,7 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
   }
   // ---- local slots and the unit list
   for (int i = tid; i < a.M * a.top_k; i += kNvThreads) {
-    const int le = __ldg(a.ids + i) - a.e0;
+    const int le = S.sid[i] - a.e0;
     if (le >= 0 && le < a.L) atomicOr(&S.tokmask[le], 1ull << (i / a.top_k));
   }
   __syncthreads();
@@ -552,7 +585,7 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
   }
   __syncthreads();
   for (int i = tid; i < a.M * a.top_k; i += kNvThreads) {
-    const int le = __ldg(a.ids + i) - a.e0;
+    const int le = S.sid[i] - a.e0;
     if (le >= 0 && le < a.L) {
       const int t = i / a.top_k;
       const int u = S.uidx[le];
@@ -829,9 +862,9 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
 #pragma unroll
       for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
       for (int r = 0; r < a.top_k; ++r) {
-        const int le = __ldg(a.ids + tt * a.top_k + r) - a.e0;
+        const int le = S.sid[tt * a.top_k + r] - a.e0;
         if (le < 0 || le >= a.L) continue;
-        const float wt = __ldg(a.tw + tt * a.top_k + r);
+        const float wt = S.sw[tt * a.top_k + r];
         const uint4 o =
             __ldcg(reinterpret_cast<const uint4*>(a.obuf + static_cast<size_t>(tt * a.top_k + r) * a.H + 8 * chn));
         const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
@@ -966,7 +999,7 @@ static int nv_launch(NvArgs& a, cudaStream_t st) {
 
 int routed_nvfp4(const void* x, const int32_t* ids, const float* weights, const uint8_t* w13, const uint8_t* s13,
                  const uint8_t* w2, const uint8_t* s2, int M, int H, int N, int L, int e0, int top_k, float limit,
-                 void* y, void* workspace, size_t workspace_bytes, cudaStream_t st) {
+                 void* y, void* workspace, size_t workspace_bytes, cudaStream_t st, const Nvfp4Routing* route) {
   const NvWorkspace w = nv_layout(workspace, M, H, N, L, top_k);
   if (workspace == nullptr || workspace_bytes < w.bytes)
     return set_last_error(FME_EWORKSPACE, "workspace of %zu bytes needed, %zu given", w.bytes, workspace_bytes);
@@ -975,6 +1008,16 @@ int routed_nvfp4(const void* x, const int32_t* ids, const float* weights, const 
   a.x = static_cast<const __nv_bfloat16*>(x);
   a.ids = ids;
   a.tw = weights;
+  if (route != nullptr) {
+    a.route = 1;
+    a.logits = route->logits;
+    a.logits_f32 = route->logits_dtype == FME_F32 ? 1 : 0;
+    a.bias = route->bias;
+    a.E = route->E;
+    a.scale = route->scale;
+    a.ids_out = route->ids;
+    a.tw_out = route->weights;
+  }
   a.s13 = s13;
   a.s2 = s2;
   a.y = static_cast<__nv_bfloat16*>(y);

@@ -169,68 +169,19 @@ __device__ __forceinline__ void epi_bar() { named_bar_sync(1, 128); }
 __device__ __forceinline__ void fill_bar() { named_bar_sync(2, kFillThreads); }
 
 // ---------------------------------------------------------------- routing
-// One warp routes token t ("mega_moe" _MegaKernel.top_k_pick): sigmoid scores
-// (accurate expf, IEEE divide), keys score + bias as monotone uint32, top_k
-// rounds of warp max key then lowest expert among equals, weights
-// score / (float sum in pick order) * scale. Lane l holds experts l + 32 j in
-// registers; every load is issued before any sigmoid.
+// One warp routes token t (route_topk) and records its picks.
 template <int J>
 __device__ void route_token(const TcArgs& a, TcSmem& S, int t, int lane, bool write_out) {
-  const int E = a.E;
-  float lg[J], bs[J];
-#pragma unroll
-  for (int j = 0; j < J; ++j) {
-    const int e = lane + 32 * j;
-    lg[j] = 0.0f;
-    bs[j] = 0.0f;
-    if (e < E) {
-      if (a.logits_f32)
-        lg[j] = __ldg(static_cast<const float*>(a.logits) + static_cast<size_t>(t) * E + e);
-      else
-        lg[j] = __bfloat162float(static_cast<const __nv_bfloat16*>(a.logits)[static_cast<size_t>(t) * E + e]);
-      bs[j] = __ldg(a.bias + e);
-    }
-  }
-  uint32_t ky[J];
-#pragma unroll
-  for (int j = 0; j < J; ++j) {
-    const float sgm = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-lg[j])));
-    lg[j] = sgm;  // score
-    ky[j] = (lane + 32 * j < E) ? ordered_key(__fadd_rn(sgm, bs[j])) : 0u;
-  }
-  float total = 0.0f, mine = 0.0f;
-  int mine_e = 0;
-  for (int r = 0; r < a.top_k; ++r) {
-    uint32_t best = 0u;
-#pragma unroll
-    for (int j = 0; j < J; ++j) best = max(best, ky[j]);
-    const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, best);
-    uint32_t cand = 0xFFFFFFFFu;
-#pragma unroll
-    for (int j = J - 1; j >= 0; --j)
-      if (ky[j] == top) cand = static_cast<uint32_t>(lane + 32 * j);
-    const int win = static_cast<int>(__reduce_min_sync(0xFFFFFFFFu, cand));
-    float sv = 0.0f;
-#pragma unroll
-    for (int j = 0; j < J; ++j)
-      if (lane + 32 * j == win) {
-        sv = lg[j];
-        ky[j] = 0u;
-      }
-    const float s = __shfl_sync(0xFFFFFFFFu, sv, win & 31);
-    total = __fadd_rn(total, s);
-    if (lane == r) {
-      mine = s;
-      mine_e = win;
-    }
-  }
+  int e;
+  float w;
+  route_topk<J>(a.logits, a.logits_f32 != 0, a.bias, a.E, a.top_k, a.scale, t, lane, e, w);
   if (lane < a.top_k) {
     const int route = t * a.top_k + lane;
-    S.rid[route] = static_cast<int16_t>(mine_e);
-    atomicOr(&S.tokmask[mine_e], 1ull << t);
+    S.rid[route] = static_cast<int16_t>(e);
+    atomicOr(&S.tokmask[e], 1ull << t);
     if (write_out) {
-      a.ids[route] = mine_e;
-      a.weights[route] = __fmul_rn(__fdiv_rn(mine, total), a.scale);
+      a.ids[route] = e;
+      a.weights[route] = w;
     }
   }
 }

@@ -261,6 +261,31 @@ int fme_moe_routed_nvfp4(const void* x, const int32_t* topk_ids, const float* to
 
 size_t fme_moe_routed_nvfp4_workspace(int M, int H, int N, int L, int top_k);
 
+/*
+ * NVFP4 slot MoE with the routing fused in: fme_moe_routed_nvfp4 whose picks
+ * come from router logits instead of the caller.
+ *
+ * Sources: the slot MoE as fme_moe_routed_nvfp4 ("nvfp4-megamoe-kernel
+ * README.md"); the routing is the routed FP8 kernel's ("mega_moe"
+ * _MegaKernel.top_k_pick): sigmoid scores, score + bias selects the top_k
+ * experts (ties to the lower id) in descending order, weights = score / (FP32
+ * sum of the picked scores in pick order) * scale. The page's NVFP4 pipeline
+ * receives its picks from elsewhere; this entry computes them in the same
+ * launch, every CTA for all tokens.
+ *
+ * Arguments: those of fme_moe_routed_nvfp4 without topk_ids / topk_weights,
+ * plus logits [M, E] (logits_dtype FME_F32 or FME_BF16), bias [E] FP32, the
+ * router's expert count E (1 .. 1024, with 0 <= e0 and e0 + L <= E), scale,
+ * and the outputs ids [M, top_k] int32 and weights [M, top_k] FP32 (every
+ * pick, local or not). top_k <= min(32, E). y, workspace, errors: as
+ * fme_moe_routed_nvfp4 (same workspace size function; the two entries may
+ * share a workspace).
+ */
+int fme_moe_layer_nvfp4(const void* x, const void* logits, int logits_dtype, const float* bias, const uint8_t* w13,
+                        const uint8_t* s13, const uint8_t* w2, const uint8_t* s2, int M, int H, int N, int L, int E,
+                        int e0, int top_k, float scale, float limit, void* y, int32_t* ids, float* weights,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
 /* Zero a workspace (cudaMemsetAsync on stream). */
 int fme_workspace_clear(void* workspace, size_t workspace_bytes, void* stream);
 

@@ -173,25 +173,10 @@ def nvfp4_weights_device(cfg: Nvfp4Config, seed: int, device):
     return tuple(out)
 
 
-def nvfp4_routes(cfg: Nvfp4Config, M: int, seed: int, step: int = 0):
-    """Top-k ids and weights handed to the NVFP4 layer (an input of it): each
-    token's top_k experts are those with the largest synthetic scores
-    (logit + bias of nvfp4_activations); the weights are seeded uniform draws
-    normalised per token. A plain selection over random scores, not the FP8
-    router's formula."""
-    _, logits, bias = nvfp4_activations(cfg, M, seed, step)
-    score = logits + bias[None, :]
-    ids = np.argsort(-score, axis=1, kind="stable")[:, :cfg.top_k].astype(np.int32)
-    rng = np.random.default_rng([seed, 77, step, M])
-    w = rng.uniform(0.1, 1.0, size=(M, cfg.top_k)).astype(np.float32)
-    w = (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
-    return ids, w
-
-
 def nvfp4_activations(cfg: Nvfp4Config, M: int, seed: int, step: int = 0):
     """x [M, H] BF16 values and router logits [M, E] / bias [E] (the tests derive
-    topk ids and weights from these with the oracle's routing; the bench uses
-    nvfp4_routes)."""
+    topk ids and weights from these with the oracle's routing; the bench lets
+    the fused-routing entry pick them)."""
     x = to_bf16_values(normal_f32(seed, S_X * 1000003 + step, (M, cfg.H)))
     logits = normal_f32(seed, S_LOGITS * 1000003 + step, (M, cfg.E))
     bias = normal_f32(seed, S_BIAS, (cfg.E,), 0.05)

@@ -91,10 +91,30 @@ def test_finalize_validation(fme):
     assert fin(vp(16), vp(16), vp(8), 2, 7168, 8, vp(16), None) == -3    # shared_out misaligned
 
 
+def test_fused_nvfp4_validation(fme):
+    vp = ctypes.c_void_p
+
+    def call(**kw):
+        a = dict(x=vp(16), lg=vp(16), dt=0, bias=vp(16), w13=vp(16), s13=vp(16), w2=vp(16), s2=vp(16), M=4,
+                 H=7168, N=3072, L=48, E=384, e0=0, k=6, scale=1.0, limit=float("inf"), y=vp(16), ids=vp(16),
+                 w=vp(16), ws=vp(16), wsb=1 << 30, st=None)
+        a.update(kw)
+        return fme.lib.fme_moe_layer_nvfp4(*a.values())
+
+    assert call(lg=None) == -1
+    assert call(e0=340) == -1          # local range past E
+    assert call(E=1025) == -2
+    assert call(k=33) == -1
+    assert call(dt=7) == -1
+    assert call(scale=float("nan")) == -1
+    assert call(M=65) == -2
+    assert call(ids=vp(20)) == -3
+
+
 def test_binding_exposes_a_wrapper_per_entry_point(fme):
     for name in ("moe_routed_fp8", "moe_routed_fp8_workspace", "moe_layer_fp8", "moe_layer_fp8_workspace",
                  "shared_expert_fp8", "shared_expert_fp8_workspace", "moe_routed_nvfp4",
-                 "moe_routed_nvfp4_workspace", "ue8m0_unpack", "moe_finalize"):
+                 "moe_routed_nvfp4_workspace", "ue8m0_unpack", "moe_finalize", "moe_layer_nvfp4"):
         assert callable(getattr(fme, name)), name
 
 

@@ -103,3 +103,37 @@ def test_ue8m0_unpack_matches_oracle_and_detects_mismatch(fme):
     packed[300, 1] ^= np.uint32(1 << 8)
     with pytest.raises(ValueError):
         fme.ue8m0_unpack(torch.from_numpy(packed.view(np.int32)).to(DEV), n, k)
+
+
+# ---------------------------------------------------------------- fused routing
+@pytest.mark.parametrize("cfg,M,logits_bf16", [(SMALL, 5, False), (RAGGED, 7, True), (ODD, 33, False)])
+def test_nvfp4_fused_routing_matches_oracle_and_unfused_call(fme, cfg, M, logits_bf16):
+    from tests.parity import assert_routing
+    w13h, s13h, w2h, s2h = _host_weights(cfg, 51)
+    w13, s13, w2, s2 = (torch.from_numpy(h.full()).to(DEV) for h in (w13h, s13h, w2h, s2h))
+    x, logits, bias = W.nvfp4_activations(cfg, M, 51)
+    if logits_bf16:
+        logits = codecs_bf16(logits)
+    scale = 1.5
+    xd = torch.from_numpy(x).to(DEV).to(torch.bfloat16)
+    ld = torch.from_numpy(logits).to(DEV)
+    ld = ld.to(torch.bfloat16) if logits_bf16 else ld
+    y, ids, wts = fme.moe_layer_nvfp4(xd, ld, torch.from_numpy(bias).to(DEV), w13, s13, w2, s2, cfg.e0, cfg.top_k,
+                                      scale, cfg.limit)
+    rids, rw, keys = routing.route(logits, bias, cfg.top_k, scale)
+    assert_routing(ids.cpu().numpy(), wts.cpu().numpy(), rids, rw, routing.selection_gap(keys, rids))
+    # the slot MoE on the kernel's own picks: the oracle, and the unfused entry bit for bit
+    gi, gw = ids.cpu().numpy(), wts.cpu().numpy()
+    ref = moe_nvfp4.routed_nvfp4(x, gi, gw, w13h, s13h, w2h, s2h, cfg.e0, cfg.L, cfg.limit)
+    local = ((gi >= cfg.e0) & (gi < cfg.e0 + cfg.L)).any(axis=1)
+    got = y.float().cpu().numpy()
+    assert (got[~local] == 0).all()
+    if local.any():
+        assert_outputs(got[local], ref[local])
+    y2 = fme.moe_routed_nvfp4(xd, ids, wts, w13, s13, w2, s2, cfg.e0, cfg.limit)
+    assert torch.equal(y, y2)
+
+
+def codecs_bf16(a):
+    from oracle import codecs
+    return codecs.bf16_round(np.asarray(a, dtype=np.float32))
