@@ -119,17 +119,70 @@ __device__ void route_topk(const void* logits, bool logits_f32, const float* bia
   my_w = __fmul_rn(__fdiv_rn(mine, total), scale);
 }
 
-// route_topk for any E <= kMaxExperts: the register loops sized to E.
-__device__ __forceinline__ void route_token_any(const void* logits, bool logits_f32, const float* bias, int E,
-                                                int top_k, float scale, int t, int lane, int& my_e, float& my_w) {
-  if (E <= 64)
-    route_topk<2>(logits, logits_f32, bias, E, top_k, scale, t, lane, my_e, my_w);
-  else if (E <= 256)
-    route_topk<8>(logits, logits_f32, bias, E, top_k, scale, t, lane, my_e, my_w);
-  else if (E <= 512)
-    route_topk<16>(logits, logits_f32, bias, E, top_k, scale, t, lane, my_e, my_w);
-  else
-    route_topk<kMaxExperts / 32>(logits, logits_f32, bias, E, top_k, scale, t, lane, my_e, my_w);
+// The same picks and weights as route_topk, bit for bit, with the keys and
+// scores of one token in shared memory (2 * E words at `scratch`) instead of
+// registers: short code for any E <= kMaxExperts, for kernels where one warp
+// routes one token and the code size of the register version costs more
+// than its speed saves.
+inline __device__ void route_topk_smem(const void* logits, bool logits_f32, const float* bias, int E, int top_k,
+                                float scale, int t, int lane, uint32_t* scratch, int& my_e, float& my_w) {
+  uint32_t* key = scratch;
+  float* score = reinterpret_cast<float*>(scratch + E);
+  // Eight experts per lane per pass, every load of a pass issued first.
+#pragma unroll 1
+  for (int e0 = lane; e0 < E; e0 += 256) {
+    float l[8], b[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int e = e0 + 32 * q;
+      l[q] = 0.0f;
+      b[q] = 0.0f;
+      if (e < E) {
+        l[q] = logits_f32 ? __ldg(static_cast<const float*>(logits) + static_cast<size_t>(t) * E + e)
+                          : __bfloat162float(static_cast<const __nv_bfloat16*>(logits)[static_cast<size_t>(t) * E + e]);
+        b[q] = __ldg(bias + e);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int e = e0 + 32 * q;
+      if (e < E) {
+        const float sgm = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l[q])));
+        score[e] = sgm;
+        key[e] = ordered_key(__fadd_rn(sgm, b[q]));
+      }
+    }
+  }
+  __syncwarp();
+  float total = 0.0f, mine = 0.0f;
+  int mine_e = 0;
+#pragma unroll 1
+  for (int r = 0; r < top_k; ++r) {
+    uint32_t best = 0u;
+    int bi = -1;
+#pragma unroll 4
+    for (int e = lane; e < E; e += 32) {
+      const uint32_t k = key[e];
+      if (k > best) {
+        best = k;
+        bi = e;
+      }
+    }
+    const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, best);
+    const uint32_t cand = (best == top && bi >= 0) ? static_cast<uint32_t>(bi) : 0xFFFFFFFFu;
+    const int win = static_cast<int>(__reduce_min_sync(0xFFFFFFFFu, cand));
+    const float sv = score[win];
+    __syncwarp();
+    if (lane == (win & 31)) key[win] = 0u;
+    __syncwarp();
+    total = __fadd_rn(total, sv);
+    if (lane == r) {
+      mine = sv;
+      mine_e = win;
+    }
+  }
+  my_e = mine_e;
+  my_w = __fmul_rn(__fdiv_rn(mine, total), scale);
 }
 
 }  // namespace fme

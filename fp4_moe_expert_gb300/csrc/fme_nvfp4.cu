@@ -88,7 +88,8 @@ struct NvArgs {
   const uint8_t* s2;
   __nv_bfloat16* y;
   uint32_t* err;
-  uint32_t* sync;     // [4]: x image shares written, CTAs past that wait, GEMM2 tiles done, CTAs past the scatter wait
+  uint32_t* sync;     // [6]: x image shares written, CTAs past that wait, GEMM2 tiles done, CTAs past the scatter
+                      // wait, CTAs whose tokens are routed, CTAs past that wait
   uint32_t* done;     // [L] GEMM1 tiles finished per local expert
   uint32_t* hpassed;  // [L] CTAs past the expert's hidden wait
   uint32_t* cnt1;     // [L * N/64] contributors per GEMM1 tile
@@ -120,8 +121,7 @@ struct NvSmem {
   int16_t uoff[kMaxExperts + 1];  // first compact slot row of each unit
   int16_t stok[kMaxTokens * kMaxTopK];
   int16_t sroute[kMaxTokens * kMaxTopK];
-  int32_t sid[kMaxTokens * kMaxTopK];  // every route's expert id and weight
-  float sw[kMaxTokens * kMaxTopK];
+  int16_t sid[kMaxTokens * kMaxTopK];  // every route's local expert, -1 when not local
   uint32_t tmem_base;
   int U;
   volatile int abort;
@@ -483,29 +483,24 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
   __syncthreads();
   tc_fence_after();
 
-  // ---- the routes: the caller's picks, or this CTA's own routing of every
-  // token (one warp per token; CTA 0 writes them out)
+  // ---- fused routing: token t is routed by warp 0 of CTA t % G (keys in
+  // the epilogue's staging buffer, unused until then) into the ids / weights
+  // outputs; every CTA reads all of them back after a grid-wide count
+  // (below), so the routing overlaps the x image.
   if (a.route) {
-    for (int t = warp; t < a.M; t += kNvThreads / 32) {
+    for (int t = c; warp == 0 && t < a.M; t += G) {
       int e;
       float w;
-      route_token_any(a.logits, a.logits_f32 != 0, a.bias, a.E, a.top_k, a.scale, t, lane, e, w);
+      route_topk_smem(a.logits, a.logits_f32 != 0, a.bias, a.E, a.top_k, a.scale, t, lane,
+                      reinterpret_cast<uint32_t*>(&S.ysm[0][0]), e, w);
       if (lane < a.top_k) {
-        S.sid[t * a.top_k + lane] = e;
-        S.sw[t * a.top_k + lane] = w;
-        if (c == 0) {
-          a.ids_out[t * a.top_k + lane] = e;
-          a.tw_out[t * a.top_k + lane] = w;
-        }
+        a.ids_out[t * a.top_k + lane] = e;
+        a.tw_out[t * a.top_k + lane] = w;
       }
     }
-  } else {
-    for (int i = tid; i < a.M * a.top_k; i += kNvThreads) {
-      S.sid[i] = __ldg(a.ids + i);
-      S.sw[i] = __ldg(a.tw + i);
-    }
+    __syncthreads();
+    if (tid == 0) red_release_gpu_add(a.sync + 4, 1u);  // this CTA's tokens are routed
   }
-  __syncthreads();
   // ---- x image: token t, group g of 16 -> 8 packed bytes and a scale byte,
   // all CTAs share the work. Groups past H (an odd number of 128-value
   // halves) get zero data and zero scales, and so do the h image's scales of
@@ -546,10 +541,32 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
         *reinterpret_cast<uint2*>(a.hsc + (static_cast<size_t>(nb2 - 1) * a.Rp + r) * 16 + 8) = make_uint2(0u, 0u);
     }
   }
+  // ---- every route's expert and weight into shared memory
+  if (a.route) {
+    if (tid == 0) {
+      nv_wait_ge(a, S.abort, a.sync + 4, static_cast<uint32_t>(G));
+      // The last CTA past the routing wait re-arms both counters.
+      if (atomicAdd(a.sync + 5, 1u) + 1u == static_cast<uint32_t>(G)) {
+        atomicExch(a.sync + 4, 0u);
+        atomicExch(a.sync + 5, 0u);
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < a.M * a.top_k; i += kNvThreads) {
+      const long long le = static_cast<long long>(__ldcg(a.ids_out + i)) - a.e0;
+      S.sid[i] = static_cast<int16_t>(le >= 0 && le < a.L ? le : -1);
+    }
+  } else {
+    for (int i = tid; i < a.M * a.top_k; i += kNvThreads) {
+      const long long le = static_cast<long long>(__ldg(a.ids + i)) - a.e0;
+      S.sid[i] = static_cast<int16_t>(le >= 0 && le < a.L ? le : -1);
+    }
+  }
+  __syncthreads();
   // ---- local slots and the unit list
   for (int i = tid; i < a.M * a.top_k; i += kNvThreads) {
-    const int le = S.sid[i] - a.e0;
-    if (le >= 0 && le < a.L) atomicOr(&S.tokmask[le], 1ull << (i / a.top_k));
+    const int le = S.sid[i];
+    if (le >= 0) atomicOr(&S.tokmask[le], 1ull << (i / a.top_k));
   }
   __syncthreads();
   if (tid == 0) red_release_gpu_add(a.sync, 1u);  // this CTA's share of the x image is written
@@ -585,7 +602,7 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
   }
   __syncthreads();
   for (int i = tid; i < a.M * a.top_k; i += kNvThreads) {
-    const int le = S.sid[i] - a.e0;
+    const int le = S.sid[i];
     if (le >= 0 && le < a.L) {
       const int t = i / a.top_k;
       const int u = S.uidx[le];
@@ -862,9 +879,9 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
 #pragma unroll
       for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
       for (int r = 0; r < a.top_k; ++r) {
-        const int le = S.sid[tt * a.top_k + r] - a.e0;
+        const int le = S.sid[tt * a.top_k + r];
         if (le < 0 || le >= a.L) continue;
-        const float wt = S.sw[tt * a.top_k + r];
+        const float wt = a.route ? __ldcg(a.tw_out + tt * a.top_k + r) : __ldg(a.tw + tt * a.top_k + r);
         const uint4 o =
             __ldcg(reinterpret_cast<const uint4*>(a.obuf + static_cast<size_t>(tt * a.top_k + r) * a.H + 8 * chn));
         const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
@@ -943,7 +960,7 @@ static NvWorkspace nv_layout(void* base, int M, int H, int N, int L, int top_k) 
   w.tok = M <= 16 ? 16 : kMaxTokens;
   w.Rp = M * top_k > w.tok ? M * top_k : w.tok;  // at least one box of rows
   w.err = reinterpret_cast<uint32_t*>(p + off);
-  w.sync = w.err + 1;  // words 1..4 of the first 256 bytes
+  w.sync = w.err + 1;  // words 1..6 of the first 256 bytes
   off += 256;
   w.done = reinterpret_cast<uint32_t*>(p + off);
   off += a256(4 * static_cast<size_t>(L));
