@@ -20,7 +20,8 @@ Sources (cited by page title and section in every function):
   sections 1, 2, 6 and 7 (slot pipeline, E2M1 staging, routing weights once).
 * "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.ep.comm" —
   ``EpCombine`` (the routing-weighted sum, FP32 in a fixed order, one BF16
-  rounding): the local finalize.
+  rounding): the local finalize; ``EpDispatch`` (MXFP8 quantiser) and the
+  combine's rank-order reduction with RMSNorm, in their single-GPU forms.
 
 Pins: every function here is checked in ``tests/test_oracle_*.py`` against
 something other than itself (closed forms, exhaustive code tables, library
@@ -28,4 +29,4 @@ casts, brute force on tiny inputs, algebraic identities, invariants). No
 function is "parity unpinned".
 """
 
-from . import codecs, routing, quant, moe_fp8, moe_nvfp4, finalize  # noqa: F401
+from . import codecs, routing, quant, moe_fp8, moe_nvfp4, finalize, ep_local  # noqa: F401
