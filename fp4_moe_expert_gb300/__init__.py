@@ -41,6 +41,8 @@ SIGNATURES = {
                                       _c_int, _c_float, _vp, _vp, _c_size, _vp]),
     "fme_moe_routed_nvfp4_workspace": (_c_size, [_c_int] * 5),
     "fme_moe_finalize": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp]),
+    "fme_mxfp8_quantize": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _vp]),
+    "fme_combine_rmsnorm": (_c_int, [_vp, _c_int, _c_int, _c_int, _vp, _c_float, _vp, _vp, _vp]),
     "fme_moe_layer_nvfp4": (_c_int, [_vp, _vp, _c_int, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                      _c_int, _c_int, _c_int, _c_float, _c_float, _vp, _vp, _vp, _vp, _c_size, _vp]),
     "fme_workspace_clear": (_c_int, [_vp, _c_size, _vp]),
@@ -262,6 +264,31 @@ def moe_finalize(out, weights, shared_out=None, y=None):
     _need(y, torch.bfloat16, (M, H), "y")
     _check(lib.fme_moe_finalize(_ptr(out), _ptr(weights), _ptr(shared_out), M, H, top_k, _ptr(y), _stream(dev)))
     return y
+
+
+def mxfp8_quantize(x):
+    """(q [T, H] uint8 E4M3, scales [T, H/32] uint8 E8M0) of x [T, H] BF16 (fme_mxfp8_quantize)."""
+    T, H = x.shape
+    dev = x.device
+    _need(x, torch.bfloat16, (T, H), "x")
+    q = torch.empty(T, H, dtype=torch.uint8, device=dev)
+    sc = torch.empty(T, H // 32, dtype=torch.uint8, device=dev)
+    _check(lib.fme_mxfp8_quantize(_ptr(x), T, H, _ptr(q), _ptr(sc), _stream(dev)))
+    return q, sc
+
+
+def combine_rmsnorm(partials, gamma, eps=1e-5):
+    """(latent [T, H], normed [T, H]) BF16 of partials [T, N, H] BF16 and gamma [H] BF16
+    (fme_combine_rmsnorm)."""
+    T, N, H = partials.shape
+    dev = partials.device
+    _need(partials, torch.bfloat16, (T, N, H), "partials")
+    _need(gamma, torch.bfloat16, (H,), "gamma")
+    latent = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    normed = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    _check(lib.fme_combine_rmsnorm(_ptr(partials), T, N, H, _ptr(gamma), float(eps), _ptr(latent), _ptr(normed),
+                                   _stream(dev)))
+    return latent, normed
 
 
 def ue8m0_unpack(packed, n, k, check=True):

@@ -320,6 +320,26 @@ int fme_moe_layer_nvfp4(const void* x, const void* logits, int logits_dtype, con
                       workspace_bytes, static_cast<cudaStream_t>(stream), &r);
 }
 
+int fme_mxfp8_quantize(const void* x, int T, int H, uint8_t* q, uint8_t* scales, void* stream) {
+  FME_REQUIRE(x && q && scales, FME_EINVAL, "null pointer argument");
+  FME_REQUIRE(T >= 1 && T <= (1 << 20), FME_EINVAL, "T=%d outside [1, 2^20]", T);
+  FME_REQUIRE(H >= 32 && H % 32 == 0 && H <= (1 << 20), FME_EINVAL, "H=%d must be a positive multiple of 32", H);
+  FME_REQUIRE(!misaligned(x) && !misaligned(q), FME_EALIGN, "x and q must be 16-byte aligned");
+  return mxfp8_quantize(x, T, H, q, scales, static_cast<cudaStream_t>(stream));
+}
+
+int fme_combine_rmsnorm(const void* partials, int T, int N, int H, const void* gamma, float eps, void* latent,
+                        void* normed, void* stream) {
+  FME_REQUIRE(partials && gamma && latent && normed, FME_EINVAL, "null pointer argument");
+  FME_REQUIRE(T >= 1 && T <= (1 << 20), FME_EINVAL, "T=%d outside [1, 2^20]", T);
+  FME_REQUIRE(N >= 1 && N <= 1024, FME_EINVAL, "N=%d outside [1, 1024]", N);
+  FME_REQUIRE(H >= 8 && H % 8 == 0 && H <= 8192, FME_EINVAL, "H=%d must be a multiple of 8 in [8, 8192]", H);
+  FME_REQUIRE(eps >= 0.0f && std::isfinite(eps), FME_EINVAL, "eps must be finite and >= 0");
+  FME_REQUIRE(!misaligned(partials) && !misaligned(gamma) && !misaligned(latent) && !misaligned(normed), FME_EALIGN,
+              "every pointer must be 16-byte aligned");
+  return combine_rmsnorm(partials, T, N, H, gamma, eps, latent, normed, static_cast<cudaStream_t>(stream));
+}
+
 size_t fme_moe_routed_nvfp4_workspace(int M, int H, int N, int L, int top_k) {
   if (M < 1 || M > kMaxTokens || H < 128 || H % 128 || N < 128 || N % 128 || L < 1 || L > kMaxExperts ||
       top_k < 1 || top_k > kMaxTopK || H > 8192 || N > 8192)

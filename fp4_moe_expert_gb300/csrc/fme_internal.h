@@ -69,6 +69,12 @@ size_t layer_fp8_zero_bytes(int M, int H, int I, int E, int top_k, bool shared);
 int finalize(const void* out, const float* weights, const void* shared_out, int M, int H, int top_k, void* y,
              cudaStream_t st);
 
+// MXFP8 of x [T, H] BF16 -> q [T, H] E4M3 and scales [T, H/32] E8M0 (arguments validated).
+int mxfp8_quantize(const void* x, int T, int H, uint8_t* q, uint8_t* scales, cudaStream_t st);
+// partials [T, N, H] BF16 -> latent [T, H] = bf16(rank-order FP32 sum), normed [T, H] = RMSNorm(latent) * gamma.
+int combine_rmsnorm(const void* partials, int T, int N, int H, const void* gamma, float eps, void* latent,
+                    void* normed, cudaStream_t st);
+
 // Routing fused into the NVFP4 call: picks from logits + bias over E experts
 // (the routed FP8 rule), written to ids / weights [M, top_k].
 struct Nvfp4Routing {

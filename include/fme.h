@@ -217,6 +217,44 @@ int fme_moe_finalize(const void* out, const float* weights, const void* shared_o
                      void* y, void* stream);
 
 /*
+ * MXFP8 quantisation of BF16 rows (the expert-parallel dispatch's quantiser,
+ * single-GPU form).
+ *
+ * Source: "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.ep.comm"
+ * (EpDispatch: BF16 latent -> MXFP8, two threads per 32-value block, one E8M0
+ * scale per 32 values in row order). The page does not print its exponent
+ * rule; this follows the OCP MX rule: shared exponent floor(log2(amax)) - 8
+ * (8 = the largest E4M3 exponent), clamped to [-127, 127], -127 for a zero
+ * (or subnormal) amax; each value times 2^-exponent, E4M3 round-to-nearest-
+ * even saturating at +-448; scale byte = exponent + 127.
+ *
+ * Arguments: x [T, H] BF16, q [T, H] E4M3 bytes, scales [T, H/32] bytes.
+ * 1 <= T <= 2^20, H a positive multiple of 32. x and q 16-byte aligned.
+ * Caller-owned buffers; asynchronous on `stream` (PDL launch).
+ * Returns FME_OK, FME_EINVAL, FME_EALIGN or FME_ECUDA.
+ */
+int fme_mxfp8_quantize(const void* x, int T, int H, uint8_t* q, uint8_t* scales, void* stream);
+
+/*
+ * The combine's reduction and RMSNorm, single-GPU form.
+ *
+ * Source: "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.ep.comm"
+ * (EpCombine, rms_rstd): per token, the FP32 sum of the N partial rows in rank
+ * order, rounded once to BF16 (the routed latent); then vLLM's RMSNorm of it:
+ * FP32 sum of squares, rstd = rsqrt(sum / H + eps) (IEEE divide, approximate
+ * reciprocal square root, as the page), out = bf16((x * rstd) * gamma).
+ *
+ * Arguments: partials [T, N, H] BF16 (row t * N + d = rank d's partial of
+ * token t), gamma [H] BF16, eps >= 0 (the page: 1e-5), latent [T, H] BF16 and
+ * normed [T, H] BF16 outputs. 1 <= N <= 1024, H a multiple of 8 up to 8192.
+ * Every pointer 16-byte aligned; outputs must not overlap inputs.
+ * Caller-owned buffers; asynchronous on `stream` (PDL launch).
+ * Returns FME_OK, FME_EINVAL, FME_EALIGN or FME_ECUDA.
+ */
+int fme_combine_rmsnorm(const void* partials, int T, int N, int H, const void* gamma, float eps, void* latent,
+                        void* normed, void* stream);
+
+/*
  * Packed UE8M0 block scales -> FP32 block scales.
  *
  * Source: "vllm.models.glm5next.nvidia.specialized_decode.shared_expert",

@@ -111,10 +111,22 @@ def test_fused_nvfp4_validation(fme):
     assert call(ids=vp(20)) == -3
 
 
+def test_ep_local_validation(fme):
+    vp = ctypes.c_void_p
+    assert fme.lib.fme_mxfp8_quantize(vp(16), 2, 48, vp(16), vp(16), None) == -1     # H % 32
+    assert fme.lib.fme_mxfp8_quantize(vp(16), 0, 64, vp(16), vp(16), None) == -1
+    assert fme.lib.fme_mxfp8_quantize(vp(8), 2, 64, vp(16), vp(16), None) == -3
+    comb = fme.lib.fme_combine_rmsnorm
+    assert comb(vp(16), 2, 4, 8200, vp(16), 1e-5, vp(16), vp(16), None) == -1       # H > 8192
+    assert comb(vp(16), 2, 0, 3584, vp(16), 1e-5, vp(16), vp(16), None) == -1
+    assert comb(vp(16), 2, 4, 3584, vp(16), -1.0, vp(16), vp(16), None) == -1
+    assert comb(vp(16), 2, 4, 3584, vp(24), 1e-5, vp(16), vp(16), None) == -3
+
+
 def test_binding_exposes_a_wrapper_per_entry_point(fme):
     for name in ("moe_routed_fp8", "moe_routed_fp8_workspace", "moe_layer_fp8", "moe_layer_fp8_workspace",
                  "shared_expert_fp8", "shared_expert_fp8_workspace", "moe_routed_nvfp4",
-                 "moe_routed_nvfp4_workspace", "ue8m0_unpack", "moe_finalize", "moe_layer_nvfp4"):
+                 "moe_routed_nvfp4_workspace", "ue8m0_unpack", "moe_finalize", "moe_layer_nvfp4", "mxfp8_quantize", "combine_rmsnorm"):
         assert callable(getattr(fme, name)), name
 
 
