@@ -516,6 +516,20 @@ def side_measurements(fme, dev, args):
         us = float(np.median(ts))
         res[f"nvfp4_slot_moe_M{M}"] = {"us_median": round(us, 2), "unique_local_experts": uniq,
                                        "GBps": round(uniq * per_expert / (us * 1e-6) / 1e9, 1) if uniq else 0.0}
+    # Single-GPU forms of the expert-parallel dispatch quantiser and the combine's
+    # reduction + RMSNorm on the latent shape (H 3584, 16 ranks), T = 8 and 64 tokens.
+    H = 3584
+    for T in (8, 64):
+        rng = np.random.default_rng(args.seed + T)
+        x = torch.from_numpy(rng.normal(size=(T, H)).astype(np.float32)).to(dev).to(torch.bfloat16)
+        parts = torch.from_numpy(rng.normal(size=(T, 16, H)).astype(np.float32)).to(dev).to(torch.bfloat16)
+        gam = torch.from_numpy(rng.uniform(0.5, 1.5, H).astype(np.float32)).to(dev).to(torch.bfloat16)
+        us_q = _event_us(lambda: fme.mxfp8_quantize(x), flush)
+        us_c = _event_us(lambda: fme.combine_rmsnorm(parts, gam, 1e-5), flush)
+        res[f"mxfp8_quantize_T{T}"] = {"us_median": round(us_q, 2),
+                                       "GBps": round(T * H * (2 + 1 + 1 / 32) / (us_q * 1e-6) / 1e9, 1)}
+        res[f"combine_rmsnorm_N16_T{T}"] = {"us_median": round(us_c, 2),
+                                            "GBps": round((T * 16 * H + 2 * T * H + H) * 2 / (us_c * 1e-6) / 1e9, 1)}
     del flush
     return res
 
