@@ -77,6 +77,8 @@ __global__ void __launch_bounds__(kCombThreads) combine_rmsnorm_kernel(const __n
       float acc[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
+      // Unrolled so that several ranks' loads are in flight; the sums stay in rank order.
+#pragma unroll 8
       for (int d = 0; d < N; ++d) {
         const uint4 p = __ldcg(reinterpret_cast<const uint4*>(partials + (static_cast<size_t>(t) * N + d) * H) + ch);
         const uint32_t w[4] = {p.x, p.y, p.z, p.w};
