@@ -138,8 +138,7 @@ static int check_fp8_shapes(int M, int H, int I, int E, int top_k, float limit) 
   FME_REQUIRE(M >= 1 && M <= kMaxTokens, FME_EUNSUPPORTED, "M=%d outside [1, %d]", M, kMaxTokens);
   FME_REQUIRE(H >= 128 && H % 128 == 0 && I >= 128 && I % 128 == 0, FME_EINVAL,
               "H=%d and I=%d must be positive multiples of 128", H, I);
-  FME_REQUIRE(H <= 16 * kComputeThreads * kMaxSlicesPerThread && I <= 16 * kComputeThreads * kMaxSlicesPerThread,
-              FME_EUNSUPPORTED, "H=%d or I=%d above %d", H, I, 16 * kComputeThreads * kMaxSlicesPerThread);
+  FME_REQUIRE(H <= kMaxHidden && I <= kMaxHidden, FME_EUNSUPPORTED, "H=%d or I=%d above %d", H, I, kMaxHidden);
   FME_REQUIRE(E >= 1 && E <= kMaxExperts, FME_EUNSUPPORTED, "E=%d outside [1, %d]", E, kMaxExperts);
   FME_REQUIRE(top_k >= 1 && top_k <= E && top_k <= kMaxTopK, FME_EINVAL, "top_k=%d outside [1, min(E=%d, %d)]",
               top_k, E, kMaxTopK);

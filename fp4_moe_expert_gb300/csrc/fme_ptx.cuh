@@ -69,16 +69,6 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
-// Contiguous global -> shared copy completing on an mbarrier (bytes: multiple
-// of 16; both addresses 16-byte aligned).
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                         uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
-      "%4;" ::"r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
 
 // ------------------------------------------------------------------ gpu-scope sync
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
@@ -101,12 +91,6 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint
       : "=r"(lo), "=r"(hi)
       : "r"(w));
 }
-// Two E2M1 nibbles (low nibble first) in the low byte of w -> one f16x2 word.
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t w) {
-  uint32_t d;
-  asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(d) : "r"(w));
-  return d;
-}
 // (lo, hi) -> E4M3 bytes, lo in the low byte: round to nearest even, finite
 // values beyond 448 saturate.
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
@@ -119,15 +103,6 @@ __device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float lo, float hi) {
   uint32_t r;
   asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
-}
-// c + a.lo * b.lo + a.hi * b.hi: each f16 product exact, each add rounded in f32.
-__device__ __forceinline__ float fma_f16x2_f32(uint32_t a, uint32_t b, float c) {
-  float d;
-  asm("{ .reg .b16 al, ah, bl, bh; .reg .f32 t; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2; "
-      "fma.rn.f32.f16 t, al, bl, %3; fma.rn.f32.f16 %0, ah, bh, t; }"
-      : "=f"(d)
-      : "r"(a), "r"(b), "f"(c));
-  return d;
 }
 // Float value of an E4M3 byte (exact).
 __device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
@@ -165,11 +140,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, 
       "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
       "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
-}
-// L2 prefetch of one tensor-map box (no shared memory, no completion signal).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap), "r"(x), "r"(y)
-               : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
@@ -250,12 +220,6 @@ __device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, uint32_t (&r)[16]) {
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
-}
-// Store eight 32-bit columns of this thread's TMEM lane (warp-wide, 32x32b shape).
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-               : "memory");
 }
 // Store sixteen 32-bit columns of this thread's TMEM lane (warp-wide, 32x32b shape).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
