@@ -137,3 +137,26 @@ def test_nvfp4_fused_routing_matches_oracle_and_unfused_call(fme, cfg, M, logits
 def codecs_bf16(a):
     from oracle import codecs
     return codecs.bf16_round(np.asarray(a, dtype=np.float32))
+
+
+def test_nvfp4_fused_routing_full_size_m64_sampled_tokens(fme):
+    # 384-expert router, 48 local experts, BF16 logits: picks against the oracle for
+    # every token, y against the oracle for two sampled tokens on the kernel's picks
+    from tests.parity import assert_routing
+    cfg = W.NVFP4
+    M, seed = 64, 46
+    w13h, s13h, w2h, s2h = _host_weights(cfg, seed)
+    w13, s13, w2, s2 = W.nvfp4_weights_device(cfg, seed, DEV)
+    x, logits, bias = W.nvfp4_activations(cfg, M, seed)
+    logits = codecs_bf16(logits)
+    y, ids, wts = fme.moe_layer_nvfp4(torch.from_numpy(x).to(DEV).to(torch.bfloat16),
+                                      torch.from_numpy(logits).to(DEV).to(torch.bfloat16),
+                                      torch.from_numpy(bias).to(DEV), w13, s13, w2, s2, cfg.e0, cfg.top_k, 1.0,
+                                      cfg.limit)
+    rids, rw, keys = routing.route(logits, bias, cfg.top_k, 1.0)
+    gi, gw = ids.cpu().numpy(), wts.cpu().numpy()
+    assert_routing(gi, gw, rids, rw, routing.selection_gap(keys, rids))
+    tokens = [t for t in range(M) if ((gi[t] >= cfg.e0) & (gi[t] < cfg.e0 + cfg.L)).any()][:2]
+    assert tokens
+    ref = moe_nvfp4.routed_nvfp4(x[tokens], gi[tokens], gw[tokens], w13h, s13h, w2h, s2h, cfg.e0, cfg.L, cfg.limit)
+    assert_outputs(y.float().cpu().numpy()[tokens], ref)
