@@ -56,10 +56,11 @@ __device__ __forceinline__ uint32_t nv_sfcol(int sf) { return 128u + 32u * stati
 
 template <int TOK>
 struct NvCfg {
-  // Packed-weight ring: about 100 KB in flight keeps the weight stream at
-  // the copy rate (deeper rings measured slower); the activation operand
+  // Packed-weight ring: 64-80 KB in flight per SM. Deeper rings measured
+  // slower (more weight rows open at once in DRAM: 10 stages took M = 8 from
+  // 56 to 62 us, 8 stages M = 64 from 177 to 205 us); the activation operand
   // comes from L2 and needs only a short ring of its own.
-  static constexpr int kStages = 7;
+  static constexpr int kStages = TOK == 16 ? 4 : 5;
   static constexpr int kBStages = 4;
   static constexpr int kSfBuf = 4;                // scale-vector buffers in tensor memory
   static constexpr int kBBytes = TOK * 128;       // TOK rows of 128 packed bytes (256 values)
