@@ -42,6 +42,33 @@ def block_scaled_gemv(w_codes, w_scales, a_codes, a_scales, row_idx=None):
     return (P * S.astype(np.float64)).sum(axis=1)
 
 
+def mx_block_scaled_gemv(w_codes, w_scales, a_codes, a_e8m0):
+    """y[n] = sum over K blocks b and their 32-value blocks s of
+    P[n, b, s] * float32(w_scale[n/128, b] * 2^(a_e8m0[b, s] - 127)).
+
+    The GEMV of MXFP8 activations (E4M3 values, one E8M0 scale per 32 values,
+    "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.ep.comm"
+    EpDispatch's format) with the routed weights' FP32 block-128 scales
+    ("mega_moe"). Reading: the pages do not print this product; each 32-value
+    block's exact partial sum takes its own scale product, as the MX format
+    defines, and the sums are exact (float64 here).
+
+    Args: w_codes [N, K] uint8 E4M3, w_scales [N/128, K/128] float32,
+        a_codes [K] uint8 E4M3, a_e8m0 [K/32] uint8.
+    Returns: [N] float64.
+    """
+    w_codes = np.asarray(w_codes)
+    N, K = w_codes.shape
+    nb = K // GROUP
+    W = e4m3_decode(w_codes).reshape(N, nb, 4, GROUP // 4)
+    a = e4m3_decode(a_codes).reshape(nb, 4, GROUP // 4)
+    P = np.einsum("nbsk,bsk->nbs", W, a)
+    ws = np.asarray(w_scales, dtype=np.float32)[np.arange(N) // GROUP, :]
+    ax = np.exp2(np.asarray(a_e8m0, dtype=np.float64).reshape(nb, 4) - 127.0)
+    S = (ws[:, :, None].astype(np.float64) * ax[None, :, :]).astype(np.float32)
+    return (P * S.astype(np.float64)).sum(axis=(1, 2))
+
+
 def clamped_swiglu(gate, up, limit):
     """silu(min(gate, limit)) * clamp(up, -limit, limit) in float64.
 
@@ -56,7 +83,7 @@ def clamped_swiglu(gate, up, limit):
 
 
 def routed_fp8(x, logits, bias, w13, s13, w2, s2, top_k, limit, scale, ue8m0,
-               hidden_ue8m0=None, routes=None, rows=None):
+               hidden_ue8m0=None, routes=None, rows=None, x_mx=None):
     """Routed experts of a few decode tokens ("mega_moe" ``MegaExperts.__call__``).
 
     Args:
@@ -69,6 +96,9 @@ def routed_fp8(x, logits, bias, w13, s13, w2, s2, top_k, limit, scale, ue8m0,
         hidden_ue8m0: rounding of the hidden scale (default: ``ue8m0``).
         routes: optional iterable of route indices t*top_k + r to evaluate.
         rows: optional array of output rows m to evaluate (sampling).
+        x_mx: optional MXFP8 activations (codes [M, H] uint8 E4M3, scales
+            [M, H/32] uint8 E8M0) used by GEMM1 instead of quantising x
+            (x then only gives M and H).
 
     Returns:
         out [M*top_k, H] float32 holding BF16 values (NaN where not evaluated),
@@ -89,7 +119,10 @@ def routed_fp8(x, logits, bias, w13, s13, w2, s2, top_k, limit, scale, ue8m0,
         e = int(ids[t, r])
         W1 = np.asarray(w13[e])
         inter = W1.shape[0] // 2
-        y = block_scaled_gemv(W1, s13[e], xq[t], sx[t]).astype(np.float32)
+        if x_mx is None:
+            y = block_scaled_gemv(W1, s13[e], xq[t], sx[t]).astype(np.float32)
+        else:
+            y = mx_block_scaled_gemv(W1, s13[e], x_mx[0][t], x_mx[1][t]).astype(np.float32)
         # W31 row order: up rows, then gate rows ("mega_moe" module docstring).
         up, gate = y[:inter], y[inter:]
         h = clamped_swiglu(gate, up, limit).astype(np.float32)

@@ -305,3 +305,25 @@ def test_nvfp4_per_slot_silu_brute_force():
             o = codecs.bf16_round(W2d @ hd)
             acc = (acc + (weights[t, r] * o).astype(np.float32)).astype(np.float32)
         assert np.array_equal(y[t], codecs.bf16_round(acc))
+
+
+def test_mx_gemv_reduces_to_block_gemv_and_matches_dense_dequant():
+    from oracle import codecs
+    from oracle.moe_fp8 import block_scaled_gemv, mx_block_scaled_gemv
+    rng = np.random.default_rng(11)
+    N, K = 256, 512
+    w = rng.integers(0, 0x7E, size=(N, K), dtype=np.uint8) | (rng.integers(0, 2, size=(N, K), dtype=np.uint8) << 7)
+    w[(w & 0x7F) == 0x7F] = 0
+    ws = np.exp2(rng.uniform(-12, -6, size=(N // 128, K // 128))).astype(np.float32)
+    a = rng.integers(0, 0x7E, size=K, dtype=np.uint8)
+    # equal exponents inside each 128-block: the per-128 GEMV with scale 2^(e-127)
+    e128 = rng.integers(110, 140, size=K // 128).astype(np.uint8)
+    e32 = np.repeat(e128, 4)
+    got = mx_block_scaled_gemv(w, ws, a, e32)
+    ref = block_scaled_gemv(w, ws, a, np.exp2(e128.astype(np.float64) - 127).astype(np.float32))
+    assert np.allclose(got, ref, rtol=1e-12, atol=0)
+    # any exponents: the dense dequantised product (power-of-two scales: exact scale products)
+    e = rng.integers(100, 150, size=K // 32).astype(np.uint8)
+    W = codecs.e4m3_decode(w) * np.repeat(np.repeat(ws.astype(np.float64), 128, 0), 128, 1)
+    av = codecs.e4m3_decode(a) * np.repeat(np.exp2(e.astype(np.float64) - 127), 32)
+    assert np.allclose(mx_block_scaled_gemv(w, ws, a, e), W @ av, rtol=1e-12, atol=1e-300)
