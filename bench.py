@@ -437,6 +437,10 @@ def layer_measurements(fme, dev, args, shared_w, shared_bytes, flush):
         us_sep = _event_us(separate, flush)
         us_fused = _event_us(fused, flush)
         us_shared = _event_us(lambda: fme.shared_expert_fp8(xd, *shared, workspace=ws_s), flush)
+        # routed experts alone, BF16 tokens against MXFP8 tokens (E4M3 + per-32 E8M0)
+        xq, xsc = fme.mxfp8_quantize(xd)
+        us_routed = _event_us(lambda: fme.moe_routed_fp8(*routed, workspace=ws_r), flush)
+        us_mx = _event_us(lambda: fme.moe_routed_fp8_mx(xq, xsc, *routed[1:], workspace=ws_r), flush)
         # local finalize of the layer's outputs: y = bf16(sum_r w * out + shared_out)
         lo, _, lw, lso = outs["l"]
         ybuf = torch.empty(M, cfg.H, dtype=torch.bfloat16, device=dev)
@@ -458,6 +462,9 @@ def layer_measurements(fme, dev, args, shared_w, shared_bytes, flush):
             "one_launch_layer_us": round(us_fused, 2),
             "one_launch_layer_GBps": round(nbytes / (us_fused * 1e-6) / 1e9, 1),
             "shared_then_routed_GBps": round(nbytes / (us_sep * 1e-6) / 1e9, 1),
+            "routed_bf16_input_us": round(us_routed, 2),
+            "routed_mxfp8_input_us": round(us_mx, 2),
+            "routed_mxfp8_input_GBps": round(uniq * EXPERT_BYTES / (us_mx * 1e-6) / 1e9, 1),
             "finalize_us": round(us_fin, 2),
             "finalize_GBps": round(fin_bytes / (us_fin * 1e-6) / 1e9, 1),
             "layer_plus_finalize_us": round(us_layer_y, 2),

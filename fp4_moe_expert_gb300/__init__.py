@@ -27,6 +27,8 @@ SIGNATURES = {
     "fme_moe_routed_fp8": (_c_int, [_vp, _vp, _c_int, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                     _c_int, _c_float, _c_float, _c_int, _vp, _vp, _vp, _vp, _c_size, _vp]),
     "fme_moe_routed_fp8_workspace": (_c_size, [_c_int] * 5),
+    "fme_moe_routed_fp8_mx": (_c_int, [_vp, _vp, _vp, _c_int, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                       _c_int, _c_float, _c_float, _c_int, _vp, _vp, _vp, _vp, _c_size, _vp]),
     "fme_moe_routed_fp8_noalloc": (_c_int, [_vp, _vp, _c_int, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                             _c_int, _c_int, _c_float, _c_float, _c_int, _vp, _vp, _vp, _vp]),
     "fme_shared_expert_fp8": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_float, _c_int, _vp,
@@ -167,6 +169,43 @@ def moe_routed_fp8(x, logits, bias, w13, s13, w2, s2, top_k, limit, scale, ue8m0
     _check(lib.fme_moe_routed_fp8(_ptr(x), _ptr(logits), ldt, _ptr(bias), _ptr(w13), _ptr(s13), _ptr(w2),
                                   _ptr(s2), M, H, I, E, top_k, float(limit), float(scale), int(bool(ue8m0)),
                                   _ptr(out), _ptr(ids), _ptr(weights), ws.ptr(), ws.nbytes, _stream(dev)))
+    return out, ids, weights
+
+
+def moe_routed_fp8_mx(xq, xscales, logits, bias, w13, s13, w2, s2, top_k, limit, scale, ue8m0,
+                      out=None, ids=None, weights=None, workspace=None):
+    """moe_routed_fp8 with MXFP8 activations (fme_moe_routed_fp8_mx): xq [M, H] uint8
+    E4M3 and xscales [M, H/32] uint8 E8M0 (as mxfp8_quantize returns). Returns
+    (out [M*top_k, H] bf16, ids [M, top_k] int32, weights [M, top_k] float32)."""
+    M, H = xq.shape
+    E = logits.shape[1]
+    I = w2.shape[2]
+    dev = xq.device
+    _need(xq, torch.uint8, (M, H), "xq")
+    _need(xscales, torch.uint8, (M, H // 32), "xscales")
+    if logits.dtype == torch.float32:
+        dt = FME_F32
+    elif logits.dtype == torch.bfloat16:
+        dt = FME_BF16
+    else:
+        raise ValueError("logits must be float32 or bfloat16")
+    _need(logits, logits.dtype, (M, E), "logits")
+    _need(bias, torch.float32, (E,), "bias")
+    _need(w13, torch.uint8, (E, 2 * I, H), "w13")
+    _need(s13, torch.float32, (E, 2 * I // 128, H // 128), "s13")
+    _need(w2, torch.uint8, (E, H, I), "w2")
+    _need(s2, torch.float32, (E, H // 128, I // 128), "s2")
+    if out is None:
+        out = torch.empty(M * top_k, H, dtype=torch.bfloat16, device=dev)
+    if ids is None:
+        ids = torch.empty(M, top_k, dtype=torch.int32, device=dev)
+    if weights is None:
+        weights = torch.empty(M, top_k, dtype=torch.float32, device=dev)
+    need = moe_routed_fp8_workspace(M, H, I, E, top_k)
+    ws = _workspace(need, dev, workspace)
+    _check(lib.fme_moe_routed_fp8_mx(_ptr(xq), _ptr(xscales), _ptr(logits), dt, _ptr(bias), _ptr(w13), _ptr(s13),
+                                     _ptr(w2), _ptr(s2), M, H, I, E, top_k, float(limit), float(scale), int(ue8m0),
+                                     _ptr(out), _ptr(ids), _ptr(weights), ws.ptr(), ws.nbytes, _stream(dev)))
     return out, ids, weights
 
 

@@ -185,6 +185,42 @@ int fme_moe_routed_fp8(const void* x, const void* logits, int logits_dtype, cons
   return layer_fp8(r, SharedFp8(), M, H, I, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
+
+int fme_moe_routed_fp8_mx(const uint8_t* xq, const uint8_t* xscales, const void* logits, int logits_dtype,
+                          const float* bias, const uint8_t* w13, const float* s13, const uint8_t* w2, const float* s2,
+                          int M, int H, int I, int E, int top_k, float limit, float scale, int ue8m0, void* out,
+                          int32_t* ids, float* weights, void* workspace, size_t workspace_bytes, void* stream) {
+  FME_REQUIRE(xq && xscales && logits && bias && w13 && s13 && w2 && s2 && out && ids && weights, FME_EINVAL,
+              "null pointer argument");
+  const int st = check_fp8_shapes(M, H, I, E, top_k, limit);
+  if (st != FME_OK) return st;
+  FME_REQUIRE(logits_dtype == FME_F32 || logits_dtype == FME_BF16, FME_EINVAL, "logits_dtype=%d", logits_dtype);
+  FME_REQUIRE(std::isfinite(scale), FME_EINVAL, "scale must be finite");
+  FME_REQUIRE(!misaligned(xq) && !misaligned(logits) && !misaligned(bias) && !misaligned(w13) && !misaligned(s13) &&
+                  !misaligned(w2) && !misaligned(s2) && !misaligned(out) && !misaligned(ids) &&
+                  !misaligned(weights) && !misaligned(workspace),
+              FME_EALIGN, "every pointer except xscales must be 16-byte aligned");
+  RoutedFp8 r;
+  r.xq = xq;
+  r.xsc = xscales;
+  r.logits = logits;
+  r.logits_dtype = logits_dtype;
+  r.bias = bias;
+  r.w13 = w13;
+  r.s13 = s13;
+  r.w2 = w2;
+  r.s2 = s2;
+  r.E = E;
+  r.top_k = top_k;
+  r.limit = limit;
+  r.scale = scale;
+  r.ue8m0 = ue8m0;
+  r.out = out;
+  r.ids = ids;
+  r.weights = weights;
+  return layer_fp8(r, SharedFp8(), M, H, I, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
 size_t fme_shared_expert_fp8_workspace(int M, int H, int I) {
   if (check_fp8_shapes(M, H, I, 1, 1, 1.0f) != FME_OK) return 0;
   return layer_fp8_workspace_bytes(M, H, I, 0, 0, true);

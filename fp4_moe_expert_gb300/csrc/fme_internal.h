@@ -27,6 +27,8 @@ size_t nvfp4_workspace_bytes(int M, int H, int N, int L, int top_k);
 // The routed experts of one FP8 layer call (E == 0: none).
 struct RoutedFp8 {
   const void* x = nullptr;
+  const uint8_t* xq = nullptr;   // MXFP8 input instead of x: E4M3 [M, H] and E8M0 [M, H/32]
+  const uint8_t* xsc = nullptr;
   const void* logits = nullptr;
   int logits_dtype = 0;
   const float* bias = nullptr;

@@ -67,6 +67,8 @@ struct TcArgs {
   CUtensorMap smap13;  // shared-expert gate_up as [2I rows, H bytes]
   CUtensorMap smap2;   // shared-expert down as [H rows, I bytes]
   const __nv_bfloat16* x;
+  const uint8_t* xq;   // MXFP8 input (the MX kernel): x as E4M3 [M, H] and E8M0 [M, H/32]
+  const uint8_t* xsc;
   const void* logits;
   const float* bias;
   const float* s13;
@@ -209,6 +211,7 @@ struct PhasePlan {
 
 struct Plan {
   int U, N, kcmax, c, G, W;
+  int kcmax1;  // K blocks per GEMM1 chunk (the MX kernel: four accumulator groups per K block)
   int tiles[2], nb[2];  // per unit: GEMM1 64-row tiles x H/128 K blocks; GEMM2 128-row tiles x I/128
   __device__ int wave_lo(int w) const { return U * w / W; }
   // Stage q of 2W: GEMM1 of wave 0, then GEMM1(w + 1) / GEMM2(w) pairs, then
@@ -269,7 +272,7 @@ struct Cursor {
         ch.T = tile - uw * pp.tiles;
         ch.t0 = t0;
         ch.kb0 = pos - t0;
-        ch.kc = min(P.kcmax, seg1 - pos);
+        ch.kc = min(phase == 1 ? P.kcmax1 : P.kcmax, seg1 - pos);
         ch.last_of_seg = pos + ch.kc == seg1;
         ch.pp = pp;
         pos += ch.kc;
@@ -316,6 +319,53 @@ __device__ void fill_context(const TcArgs& a, TcSmem& S, int u, int fid) {
   fill_bar();
 }
 
+// MXFP8 input, GEMM1 chunk: the tokens' E4M3 rows go into B buffer b as they
+// are, and each 32-value block's E8M0 scale, as 2^(e - 127), into
+// S.xs[b][t][4 j + s] (K block j, its block s): the MMA puts each 32-value
+// block in its own accumulator group and the accumulate warps apply the
+// scale to it. Routed experts only (the MX entry has no shared expert).
+__device__ bool fill_b_mx(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& ch, int b, int ci, int fid) {
+  const int r = S.ctx_n[2];
+  const int N = P.N;
+  uint8_t* B = S.B[b];
+  const XInfo xi = xinfo(a, S, ch.u);
+  float wsv = 0.0f;
+  if (fid < 2 * kMaxKc) {
+    const int half = fid / kMaxKc, j = fid % kMaxKc;
+    if (j < ch.kc) {
+      const int rb = (half == 0 ? 0 : a.I / 128) + ch.T / 2;
+      wsv = __ldg(xi.s13 + (static_cast<size_t>(xi.row_e) * (2 * a.I / 128) + rb) * (a.H / 128) + ch.kb0 + j);
+    }
+  }
+  if (ci >= 2) {
+    if (!mbar_wait(&S.mfree[b], ((ci >> 1) - 1) & 1, a.timeout_ns, &S.abort)) {
+      if (!S.abort) tc_error(a, S, kErrRingWait);
+    }
+    fill_bar();
+    if (S.abort) return false;
+  }
+  for (int t = fid; t < r; t += kFillThreads) S.ctx_route[b][t] = S.ctx_route[2][t];
+  if (fid == 0) S.ctx_n[b] = r;
+  const int items = ch.kc * r * 8;  // (K block, token, 16-byte chunk)
+  for (int w = fid; w < items; w += kFillThreads) {
+    const int p = w >> 3, sub = w & 7;
+    const int t = p % r, j = p / r;
+    const int tok = S.ctx_route[2][t] / a.top_k;
+    const int col = (ch.kb0 + j) * 128 + sub * 16;
+    const uint4 q = __ldg(reinterpret_cast<const uint4*>(a.xq + static_cast<size_t>(tok) * a.H + col));
+    *reinterpret_cast<uint4*>(B + j * N * 128 + t * 128 + ((sub ^ (t & 7)) << 4)) = q;
+    if ((sub & 1) == 0) {
+      const uint32_t e = __ldg(a.xsc + static_cast<size_t>(tok) * (a.H / 32) + col / 32);
+      S.xs[b][t][4 * j + (sub >> 1)] = __uint_as_float(e == 0 ? 0x00400000u : e << 23);
+    }
+  }
+  if (fid < 2 * kMaxKc) S.wsc[b][fid / kMaxKc][fid % kMaxKc] = wsv;
+  fence_proxy_async_smem();
+  fill_bar();
+  if (fid == 0) mbar_arrive(&S.bfull[b]);
+  return true;
+}
+
 // Quantise the activations of chunk `ch` into B buffer b: for each token row
 // t < r and K block j of the chunk, 128 values -> E4M3 by the pages' rule.
 // Phase 1 reads x (BF16): sx = max(amax, 1e-10) / 448 [UE8M0], q = e4m3(x * (1/sx)).
@@ -327,7 +377,11 @@ __device__ void fill_context(const TcArgs& a, TcSmem& S, int u, int fid) {
 // The scales and the first batch of activations are loaded before waiting
 // for buffer b (chunk ci - 2's accumulators read), hiding their latency.
 // Returns false when the wait gave up.
+template <bool MX>
 __device__ bool fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& ch, int b, int ci, int fid) {
+  if constexpr (MX) {
+    if (ch.phase == 1) return fill_b_mx(a, S, P, ch, b, ci, fid);
+  }
   const int r = S.ctx_n[2];
   const int N = P.N;
   uint8_t* B = S.B[b];
@@ -695,7 +749,7 @@ __device__ __forceinline__ void accumulate(uint32_t tbase, int N, int kc, int r,
 // TOK: token capacity of the accumulators (16 when M <= 16, else 64): the
 // per-token loops are unrolled to it, so the small case keeps its code small
 // enough to stay in the instruction caches.
-template <int TOK>
+template <int TOK, bool MX>
 __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_constant__ TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   TcSmem& S = *reinterpret_cast<TcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -774,6 +828,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
   P.U = S.U;
   P.N = 16 * ((S.rmax + 15) / 16);
   P.kcmax = min(kMaxKc, kTmemBuf / P.N);
+  P.kcmax1 = MX ? max(1, min(kMaxKc / 4, kTmemBuf / (4 * P.N))) : P.kcmax;
   P.c = blockIdx.x;
   P.G = gridDim.x;
   P.W = min(P.U, a.has_shared ? layer_waves(a.ptok) : max_waves(a.ptok));
@@ -862,11 +917,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
           }
           tc_fence_after();
           const uint32_t abase = smem_u32(S.A[s]);
-          const uint32_t d = tmem + b * kTmemBuf + j * P.N;
+          if (MX && ch.phase == 1) {
+            // One accumulator group per 32-value block: its activation scale differs.
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc_mma_f8(d, sw128_desc(abase + 32 * kk), sw128_desc(bbase + j * P.N * 128 + 32 * kk), idesc,
-                      kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_f8(tmem + b * kTmemBuf + (4 * j + kk) * P.N, sw128_desc(abase + 32 * kk),
+                        sw128_desc(bbase + j * P.N * 128 + 32 * kk), idesc, 0u);
+          } else {
+            const uint32_t d = tmem + b * kTmemBuf + j * P.N;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_f8(d, sw128_desc(abase + 32 * kk), sw128_desc(bbase + j * P.N * 128 + 32 * kk), idesc,
+                        kk > 0 ? 1u : 0u);
+          }
           tc_commit(&S.empty[s]);
         }
         if (!ok) break;
@@ -900,17 +963,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
       tc_fence_after();
       const int r = S.ctx_n[b];
       float ws[kMaxKc];
+      // MX GEMM1 chunks: four groups per K block, each with the K block's weight scale.
+      const int gsh = (MX && ch.phase == 1) ? 2 : 0;
 #pragma unroll
-      for (int j = 0; j < kMaxKc; ++j) ws[j] = S.wsc[b][ch.phase == 1 ? half : 0][j];
+      for (int j = 0; j < kMaxKc; ++j) ws[j] = S.wsc[b][ch.phase == 1 ? half : 0][j >> gsh];
+      const int groups = ch.kc << gsh;
       const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16) + b * kTmemBuf;
       if (r == 1)
-        accumulate<1, 1, 16>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
+        accumulate<1, 1, 16>(tbase, P.N, groups, r, ws, S.xs[b], y);
       else if (r <= 4)
-        accumulate<4, 1, 8>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
+        accumulate<4, 1, 8>(tbase, P.N, groups, r, ws, S.xs[b], y);
       else if (TOK == 16 || r <= 16)
-        accumulate<16, 1, 2>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
+        accumulate<16, 1, 2>(tbase, P.N, groups, r, ws, S.xs[b], y);
       else if constexpr (TOK > 16)
-        accumulate<16, TOK / 16, 1>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
+        accumulate<16, TOK / 16, 1>(tbase, P.N, groups, r, ws, S.xs[b], y);
       tc_fence_before();
       if (seg_first) {
         // First chunk of a segment: keep its routes for the segment's end.
@@ -947,7 +1013,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
       if (first2 && !wait_hidden(a, S, P, ch, fid)) break;
       ctx_u = ch.u;
       ctx_phase = ch.phase;
-      if (!fill_b(a, S, P, ch, b, ci, fid)) break;
+      if (!fill_b<MX>(a, S, P, ch, b, ci, fid)) break;
       if (first2 && fid == 0) pass_hidden(a, S, ch);
       ++ci;
     }
@@ -1053,7 +1119,8 @@ static int launch_tc(TcArgs& a, const uint8_t* w13, const uint8_t* w2, const uin
   const int sms = device_sm_count(dev);
   if (sms <= 0) return set_last_error(FME_ECUDA, "cannot query the SM count");
   // M <= 16 tokens: the 16-token variant (every expert then has <= 16 rows).
-  auto kernel = a.M <= 16 ? fp8_moe_tc_kernel<16> : fp8_moe_tc_kernel<kMaxTokens>;
+  auto kernel = a.xq != nullptr ? (a.M <= 16 ? fp8_moe_tc_kernel<16, true> : fp8_moe_tc_kernel<kMaxTokens, true>)
+                                 : (a.M <= 16 ? fp8_moe_tc_kernel<16, false> : fp8_moe_tc_kernel<kMaxTokens, false>);
   if (!ensure_smem_attr(dev, reinterpret_cast<const void*>(kernel), kTcSmemBytes)) return FME_ECUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sms < kFp8MaxCtas ? sms : kFp8MaxCtas);
@@ -1075,6 +1142,9 @@ static int layer_launch(const RoutedFp8& r, const SharedFp8& sh, int M, int H, i
 
 int layer_fp8(const RoutedFp8& r, const SharedFp8& sh, int M, int H, int I, void* workspace, size_t workspace_bytes,
               cudaStream_t st) {
+  // The MXFP8-input kernel reads its tokens from xq only: no shared expert beside it.
+  if (r.xq != nullptr && sh.w13 != nullptr)
+    return set_last_error(FME_EINVAL, "MXFP8 input with a shared expert is not supported");
   // Above 4 tokens the shared expert as the last unit of the routed schedule
   // costs more than it saves (M = 8: 490 us in one launch against 418 us for
   // the two calls): run it alone, then the routed experts, on the stream.
@@ -1100,6 +1170,8 @@ static int layer_launch(const RoutedFp8& r, const SharedFp8& sh, int M, int H, i
   a.scale = 1.0f;
   if (r.E > 0) {
     a.x = static_cast<const __nv_bfloat16*>(r.x);
+    a.xq = r.xq;
+    a.xsc = r.xsc;
     a.logits = r.logits;
     a.bias = r.bias;
     a.s13 = r.s13;

@@ -101,6 +101,29 @@ int fme_moe_routed_fp8(const void* x, const void* logits, int logits_dtype, cons
 size_t fme_moe_routed_fp8_workspace(int M, int H, int I, int E, int top_k);
 
 /*
+ * fme_moe_routed_fp8 with MXFP8 activations: x arrives as E4M3 values with one
+ * E8M0 scale per 32 values (the format of the expert-parallel dispatch,
+ * fme_mxfp8_quantize), so GEMM1 skips the per-128 quantisation of x.
+ *
+ * Sources: the routed layer as fme_moe_routed_fp8 ("mega_moe"); the
+ * activation format from "vllm.models.kimi_k3.nvidia.specialized_decode.
+ * cutedsl.moe.ep.comm" (EpDispatch). The pages do not print this product; it
+ * is y[n] = sum over K blocks b and their 32-value blocks s of
+ * P[n, b, s] * (w_scale[n/128, b] * 2^(e[b, s] - 127)), each P an exact
+ * FP32 partial (one accumulator per 32-value block). GEMM2 and everything
+ * after it as fme_moe_routed_fp8.
+ *
+ * Arguments: xq [M, H] E4M3 bytes and xscales [M, H/32] E8M0 bytes in place
+ * of x; the rest as fme_moe_routed_fp8 (same workspace size function; the two
+ * entries may share a workspace). Every pointer 16-byte aligned except
+ * xscales. Errors as fme_moe_routed_fp8.
+ */
+int fme_moe_routed_fp8_mx(const uint8_t* xq, const uint8_t* xscales, const void* logits, int logits_dtype,
+                          const float* bias, const uint8_t* w13, const float* s13, const uint8_t* w2, const float* s2,
+                          int M, int H, int I, int E, int top_k, float limit, float scale, int ue8m0, void* out,
+                          int32_t* ids, float* weights, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * fme_moe_routed_fp8 for callers that cannot allocate device memory.
  *
  * No counterpart in the pages: this is a library convenience. Some callers

@@ -70,6 +70,24 @@ def test_host_validation_rejects_bad_calls(fme):
     assert "aligned" in msg
 
 
+def _routed_mx(fme, **kw):
+    vp = ctypes.c_void_p
+    args = dict(xq=vp(16), xs=vp(3), logits=vp(16), dt=0, bias=vp(16), w13=vp(16), s13=vp(16), w2=vp(16),
+                s2=vp(16), M=1, H=512, I=256, E=8, k=2, limit=7.0, scale=1.0, ue=0, out=vp(16), ids=vp(16),
+                weights=vp(16), ws=vp(16), wsb=1 << 20, st=None)
+    args.update(kw)
+    return fme.lib.fme_moe_routed_fp8_mx(*args.values())
+
+
+def test_mx_input_validation(fme):
+    assert _routed_mx(fme, xq=None) == -1
+    assert _routed_mx(fme, xs=None) == -1
+    assert _routed_mx(fme, M=65) == -2
+    assert _routed_mx(fme, H=480) == -1
+    assert _routed_mx(fme, dt=3) == -1
+    assert _routed_mx(fme, xq=ctypes.c_void_p(8)) == -3
+
+
 def test_nvfp4_and_unpack_validation(fme):
     vp = ctypes.c_void_p
     rc = fme.lib.fme_moe_routed_nvfp4(vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), 1, 7168, 3000,
@@ -126,7 +144,7 @@ def test_ep_local_validation(fme):
 def test_binding_exposes_a_wrapper_per_entry_point(fme):
     for name in ("moe_routed_fp8", "moe_routed_fp8_workspace", "moe_layer_fp8", "moe_layer_fp8_workspace",
                  "shared_expert_fp8", "shared_expert_fp8_workspace", "moe_routed_nvfp4",
-                 "moe_routed_nvfp4_workspace", "ue8m0_unpack", "moe_finalize", "moe_layer_nvfp4", "mxfp8_quantize", "combine_rmsnorm"):
+                 "moe_routed_nvfp4_workspace", "ue8m0_unpack", "moe_finalize", "moe_layer_nvfp4", "mxfp8_quantize", "combine_rmsnorm", "moe_routed_fp8_mx"):
         assert callable(getattr(fme, name)), name
 
 
