@@ -83,7 +83,7 @@ def clamped_swiglu(gate, up, limit):
 
 
 def routed_fp8(x, logits, bias, w13, s13, w2, s2, top_k, limit, scale, ue8m0,
-               hidden_ue8m0=None, routes=None, rows=None, x_mx=None):
+               hidden_ue8m0=None, routes=None, rows=None, x_mx=None, exact=False):
     """Routed experts of a few decode tokens ("mega_moe" ``MegaExperts.__call__``).
 
     Args:
@@ -99,10 +99,14 @@ def routed_fp8(x, logits, bias, w13, s13, w2, s2, top_k, limit, scale, ue8m0,
         x_mx: optional MXFP8 activations (codes [M, H] uint8 E4M3, scales
             [M, H/32] uint8 E8M0) used by GEMM1 instead of quantising x
             (x then only gives M and H).
+        exact: also return the float64 GEMM2 results before their BF16
+            rounding (where a BF16 rounding decision sits on a tie, which of
+            the two neighbours a summation in another order picks is open).
 
     Returns:
         out [M*top_k, H] float32 holding BF16 values (NaN where not evaluated),
-        ids [M, top_k] int32, weights [M, top_k] float32, keys [M, E] float32.
+        ids [M, top_k] int32, weights [M, top_k] float32, keys [M, E] float32
+        (and with ``exact`` the unrounded out [M*top_k, H] float64).
     """
     x = np.asarray(x, dtype=np.float32)
     M, H = x.shape
@@ -112,6 +116,7 @@ def routed_fp8(x, logits, bias, w13, s13, w2, s2, top_k, limit, scale, ue8m0,
     # x-quant: "mega_moe" epilogue head, per 128-K block, values * inverse.
     xq, sx = fp8_quant_mul(x, ue8m0)
     out = np.full((M * top_k, H), np.nan, dtype=np.float32)
+    unrounded = np.full((M * top_k, H), np.nan, dtype=np.float64)
     routes = range(M * top_k) if routes is None else routes
     row_idx = np.arange(H) if rows is None else np.asarray(rows)
     for route_i in routes:
@@ -131,6 +136,9 @@ def routed_fp8(x, logits, bias, w13, s13, w2, s2, top_k, limit, scale, ue8m0,
         S2 = np.asarray(s2[e])
         y2 = block_scaled_gemv(W2, S2, qh, sh, row_idx=row_idx)
         out[route_i, row_idx] = bf16_round(y2)
+        unrounded[route_i, row_idx] = y2
+    if exact:
+        return out, ids, weights, keys, unrounded
     return out, ids, weights, keys
 
 

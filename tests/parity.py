@@ -5,6 +5,15 @@ relative; per route row max-abs error <= 0.02 x the oracle row's RMS; at least
 99.9% of elements within 2 BF16 ulp of the oracle value (ulp taken at the
 oracle value). The same output criteria are applied to the shared expert and
 the NVFP4 layer.
+
+Rounding ties. The outputs are BF16 roundings of FP32 sums. Where the exact
+value sits within FP32 summation noise of the midpoint between two BF16
+values, a kernel that sums in another order may round to the other neighbour:
+one BF16 ulp, which for an element above about 2.6 x the row RMS exceeds
+0.02 x RMS although both sides are correct. Given the oracle's unrounded
+values, such one-ulp tie flips (exact value within TIE_REL x max(|exact|, row
+RMS) of the midpoint) are left out of the row max; they still count in the
+2-ulp fraction.
 """
 
 import numpy as np
@@ -13,6 +22,7 @@ ROW_RMS_FRAC = 0.02
 ULP_FRAC = 0.999
 ULPS = 2.0
 WEIGHT_RTOL = 1e-6
+TIE_REL = 2.0**-18
 
 
 def bf16_ulp(v):
@@ -22,19 +32,30 @@ def bf16_ulp(v):
     return np.exp2(e - 7)
 
 
-def output_report(got, ref):
+def tie_flips(got, ref, exact, rms):
+    """Elements where got and ref are neighbouring BF16 values and the exact
+    value lies within TIE_REL x max(|exact|, rms) of their midpoint."""
+    got, ref, exact = (np.asarray(v, dtype=np.float64) for v in (got, ref, exact))
+    lo, hi = np.minimum(got, ref), np.maximum(got, ref)
+    neighbours = (hi > lo) & (hi - lo <= np.minimum(bf16_ulp(lo), bf16_ulp(hi)) * 1.0000001)
+    near = np.abs(exact - 0.5 * (lo + hi)) <= TIE_REL * np.maximum(np.abs(exact), rms[..., None])
+    return neighbours & near
+
+
+def output_report(got, ref, exact=None):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     err = np.abs(got - ref)
     within = err <= ULPS * bf16_ulp(ref)
     rms = np.sqrt(np.mean(ref**2, axis=-1))
-    row_ratio = err.max(axis=-1) / np.maximum(rms, 1e-30)
+    ties = np.zeros(err.shape, dtype=bool) if exact is None else tie_flips(got, ref, exact, rms)
+    row_ratio = np.where(ties, 0.0, err).max(axis=-1) / np.maximum(rms, 1e-30)
     return {"frac_within_2ulp": float(within.mean()), "worst_row_maxerr_over_rms": float(row_ratio.max()),
-            "max_abs_err": float(err.max()), "n": int(err.size)}
+            "max_abs_err": float(err.max()), "n": int(err.size), "tie_flips": int(ties.sum())}
 
 
-def assert_outputs(got, ref, what="out"):
-    r = output_report(got, ref)
+def assert_outputs(got, ref, what="out", exact=None):
+    r = output_report(got, ref, exact)
     assert np.isfinite(np.asarray(got, dtype=np.float64)).all(), f"{what}: non-finite values"
     assert r["frac_within_2ulp"] >= ULP_FRAC, f"{what}: {r}"
     assert r["worst_row_maxerr_over_rms"] <= ROW_RMS_FRAC, f"{what}: {r}"

@@ -40,15 +40,16 @@ def _run(fme, cfg, M, seed, w13h, w2h, s13, s2, dev_weights=None, routes=None, r
     out, ids, wts = fme.moe_routed_fp8_mx(_dev(codes), _dev(scales), _logits(cfg, logits), _dev(bias), w13, s13d, w2,
                                           s2d, cfg.top_k, cfg.limit, cfg.scale, cfg.ue8m0, workspace=workspace)
     torch.cuda.synchronize()
-    ref, rids, rw, keys = moe_fp8.routed_fp8(x, logits, bias, w13h, s13, w2h, s2, cfg.top_k, cfg.limit, cfg.scale,
-                                             cfg.ue8m0, routes=routes, rows=rows, x_mx=(codes, scales))
+    ref, rids, rw, keys, exact = moe_fp8.routed_fp8(x, logits, bias, w13h, s13, w2h, s2, cfg.top_k, cfg.limit,
+                                                    cfg.scale, cfg.ue8m0, routes=routes, rows=rows,
+                                                    x_mx=(codes, scales), exact=True)
     assert_routing(ids.cpu().numpy(), wts.cpu().numpy(), rids, rw, routing.selection_gap(keys, rids))
     got = out.float().cpu().numpy()
     if routes is not None:
-        got, ref = got[routes], ref[routes]
+        got, ref, exact = got[routes], ref[routes], exact[routes]
     if rows is not None:
-        got, ref = got[:, rows], ref[:, rows]
-    assert_outputs(got, ref, "routed mx")
+        got, ref, exact = got[:, rows], ref[:, rows], exact[:, rows]
+    assert_outputs(got, ref, "routed mx", exact)
     return out, ids
 
 
@@ -96,9 +97,9 @@ def test_mx_device_quantiser_feeds_the_gemm(fme):
     torch.cuda.synchronize()
     codes, scales = ep_local.mxfp8_quantize(x)
     assert np.array_equal(q.cpu().numpy(), codes) and np.array_equal(sc.cpu().numpy(), scales)
-    ref, *_ = moe_fp8.routed_fp8(x, logits, bias, w13h, s13, w2h, s2, cfg.top_k, cfg.limit, cfg.scale, cfg.ue8m0,
-                                 x_mx=(codes, scales))
-    assert_outputs(out.float().cpu().numpy(), ref, "routed mx")
+    ref, _, _, _, exact = moe_fp8.routed_fp8(x, logits, bias, w13h, s13, w2h, s2, cfg.top_k, cfg.limit, cfg.scale,
+                                             cfg.ue8m0, x_mx=(codes, scales), exact=True)
+    assert_outputs(out.float().cpu().numpy(), ref, "routed mx", exact)
     out_bf16, ids2, _ = fme.moe_routed_fp8(xd, _logits(cfg, logits), _dev(bias), *dw, cfg.top_k, cfg.limit, cfg.scale,
                                            cfg.ue8m0)
     torch.cuda.synchronize()
