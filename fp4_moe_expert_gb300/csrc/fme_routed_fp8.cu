@@ -260,6 +260,7 @@ struct Chunk {
 struct Cursor {
   int q = -1, pos = 0, phase = 1;
   PhasePlan pp;
+  template <bool MX>
   __device__ bool next(const Plan& P, Chunk& ch) {
     while (true) {
       if (q >= 0 && pos < pp.hi) {
@@ -272,7 +273,7 @@ struct Cursor {
         ch.T = tile - uw * pp.tiles;
         ch.t0 = t0;
         ch.kb0 = pos - t0;
-        ch.kc = min(phase == 1 ? P.kcmax1 : P.kcmax, seg1 - pos);
+        ch.kc = min(MX && phase == 1 ? P.kcmax1 : P.kcmax, seg1 - pos);
         ch.last_of_seg = pos + ch.kc == seg1;
         ch.pp = pp;
         pos += ch.kc;
@@ -828,7 +829,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
   P.U = S.U;
   P.N = 16 * ((S.rmax + 15) / 16);
   P.kcmax = min(kMaxKc, kTmemBuf / P.N);
-  P.kcmax1 = MX ? max(1, min(kMaxKc / 4, kTmemBuf / (4 * P.N))) : P.kcmax;
+  P.kcmax1 = MX ? max(1, min(kMaxKc / 4, kTmemBuf / (4 * P.N))) : 0;
   P.c = blockIdx.x;
   P.G = gridDim.x;
   P.W = min(P.U, a.has_shared ? layer_waves(a.ptok) : max_waves(a.ptok));
@@ -860,7 +861,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
       Chunk ch;
       int k = 0;
       bool ok = true;
-      while (ok && cur.next(P, ch)) {
+      while (ok && cur.next<MX>(P, ch)) {
         int ra, rb;
         const void* map;
         coords(ch, ra, rb, map);
@@ -899,7 +900,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
       Chunk ch;
       int k = 0, ci = 0;
       bool ok = true;
-      while (ok && cur.next(P, ch)) {
+      while (ok && cur.next<MX>(P, ch)) {
         const int b = ci & 1;
         if (!mbar_wait(&S.bfull[b], (ci >> 1) & 1, a.timeout_ns, &S.abort) ||
             (ci >= 2 && !mbar_wait(&S.tmemfree[b], ((ci >> 1) - 1) & 1, a.timeout_ns, &S.abort))) {
@@ -953,7 +954,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
     float y[TOK];
 #pragma unroll
     for (int t = 0; t < TOK; ++t) y[t] = 0.0f;
-    while (cur.next(P, ch)) {
+    while (cur.next<MX>(P, ch)) {
       const int b = ci & 1;
       if (!mbar_wait(&S.accfull[b], (ci >> 1) & 1, a.timeout_ns, &S.abort)) {
         if (!S.abort) tc_error(a, S, kErrRingWait);
@@ -1006,7 +1007,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
     Cursor cur;
     Chunk ch;
     int ci = 0, ctx_u = -1, ctx_phase = 0;
-    while (cur.next(P, ch)) {
+    while (cur.next<MX>(P, ch)) {
       const int b = ci & 1;
       if (ch.u != ctx_u) fill_context(a, S, ch.u, fid);
       const bool first2 = ch.phase == 2 && (ch.u != ctx_u || ctx_phase != 2);
