@@ -211,7 +211,7 @@ struct PhasePlan {
 
 struct Plan {
   int U, N, kcmax, c, G, W;
-  int kcmax1;  // K blocks per GEMM1 chunk (the MX kernel: four accumulator groups per K block)
+  int N1, kcmax1;  // the MX kernel's GEMM1 B rows (four per token) and K blocks per chunk
   int tiles[2], nb[2];  // per unit: GEMM1 64-row tiles x H/128 K blocks; GEMM2 128-row tiles x I/128
   __device__ int wave_lo(int w) const { return U * w / W; }
   // Stage q of 2W: GEMM1 of wave 0, then GEMM1(w + 1) / GEMM2(w) pairs, then
@@ -320,14 +320,16 @@ __device__ void fill_context(const TcArgs& a, TcSmem& S, int u, int fid) {
   fill_bar();
 }
 
-// MXFP8 input, GEMM1 chunk: the tokens' E4M3 rows go into B buffer b as they
-// are, and each 32-value block's E8M0 scale, as 2^(e - 127), into
-// S.xs[b][t][4 j + s] (K block j, its block s): the MMA puts each 32-value
-// block in its own accumulator group and the accumulate warps apply the
-// scale to it. Routed experts only (the MX entry has no shared expert).
+// MXFP8 input, GEMM1 chunk: token t takes four B rows, 4 t + s holding the
+// E4M3 codes of its 32-value block s of each K block (zeros elsewhere), so one
+// accumulator column per (token, 32-value block) comes out of the usual four
+// K = 32 MMAs of a K block. The four E8M0 bytes of (t, K block j) go to
+// S.xs[b][t][j] as they are (byte s = block s); the accumulate warps apply
+// w_scale x 2^(e - 127) per column. Routed experts only (the MX entry has no
+// shared expert).
 __device__ bool fill_b_mx(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& ch, int b, int ci, int fid) {
   const int r = S.ctx_n[2];
-  const int N = P.N;
+  const int N1 = P.N1;
   uint8_t* B = S.B[b];
   const XInfo xi = xinfo(a, S, ch.u);
   float wsv = 0.0f;
@@ -347,17 +349,22 @@ __device__ bool fill_b_mx(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk
   }
   for (int t = fid; t < r; t += kFillThreads) S.ctx_route[b][t] = S.ctx_route[2][t];
   if (fid == 0) S.ctx_n[b] = r;
-  const int items = ch.kc * r * 8;  // (K block, token, 16-byte chunk)
+  const int items = ch.kc * r * 32;  // (K block, token, block s, 16-byte chunk of the row)
   for (int w = fid; w < items; w += kFillThreads) {
-    const int p = w >> 3, sub = w & 7;
+    const int p = w >> 5, sub = w & 31;
     const int t = p % r, j = p / r;
+    const int sblk = sub >> 3, c16 = sub & 7;
+    const int row = 4 * t + sblk;
     const int tok = S.ctx_route[2][t] / a.top_k;
-    const int col = (ch.kb0 + j) * 128 + sub * 16;
-    const uint4 q = __ldg(reinterpret_cast<const uint4*>(a.xq + static_cast<size_t>(tok) * a.H + col));
-    *reinterpret_cast<uint4*>(B + j * N * 128 + t * 128 + ((sub ^ (t & 7)) << 4)) = q;
-    if ((sub & 1) == 0) {
-      const uint32_t e = __ldg(a.xsc + static_cast<size_t>(tok) * (a.H / 32) + col / 32);
-      S.xs[b][t][4 * j + (sub >> 1)] = __uint_as_float(e == 0 ? 0x00400000u : e << 23);
+    uint4 q = make_uint4(0u, 0u, 0u, 0u);
+    if ((c16 >> 1) == sblk)
+      q = __ldg(reinterpret_cast<const uint4*>(a.xq + static_cast<size_t>(tok) * a.H + (ch.kb0 + j) * 128 + c16 * 16));
+    *reinterpret_cast<uint4*>(B + j * N1 * 128 + row * 128 + ((c16 ^ (row & 7)) << 4)) = q;
+    if (sub == 0) {
+      const uint8_t* e = a.xsc + static_cast<size_t>(tok) * (a.H / 32) + (ch.kb0 + j) * 4;
+      const uint32_t packed = static_cast<uint32_t>(__ldg(e)) | (static_cast<uint32_t>(__ldg(e + 1)) << 8) |
+                              (static_cast<uint32_t>(__ldg(e + 2)) << 16) | (static_cast<uint32_t>(__ldg(e + 3)) << 24);
+      reinterpret_cast<uint32_t*>(S.xs[b][t])[j] = packed;
     }
   }
   if (fid < 2 * kMaxKc) S.wsc[b][fid / kMaxKc][fid % kMaxKc] = wsv;
@@ -746,6 +753,49 @@ __device__ __forceinline__ void accumulate(uint32_t tbase, int N, int kc, int r,
   }
 }
 
+// The MX kernel's GEMM1 chunk: column 4 t + s of K block j holds token t's
+// partial over 32-value block s; y[t] += D * (w_scale[j] * 2^(e - 127)) for
+// s = 0..3 in turn, e = byte s of xs[t][j]. LDT tokens (4 LDT columns) per
+// tcgen05.ld, GROUPS groups of them, KB K blocks per wait.
+template <int LDT, int GROUPS, int KB, int TOK>
+__device__ __forceinline__ void accumulate_mx(uint32_t tbase, int N1, int kc, int r, const float* ws,
+                                              const float (&xs)[kMaxTokens][kMaxKc], float (&y)[TOK]) {
+  constexpr int LD = 4 * LDT;
+#pragma unroll
+  for (int j0 = 0; j0 < kMaxKc; j0 += KB) {
+    if (j0 < kc) {
+#pragma unroll
+      for (int g = 0; g < GROUPS; ++g) {
+        if (g * LDT < r) {
+          uint32_t v[KB][LD];
+#pragma unroll
+          for (int jb = 0; jb < KB; ++jb)
+            if (j0 + jb < kc) tmem_ld<LD>(tbase + (j0 + jb) * N1 + g * LD, v[jb]);
+          tc_wait_ld();
+#pragma unroll
+          for (int jb = 0; jb < KB; ++jb) {
+            if (j0 + jb < kc) {
+#pragma unroll
+              for (int tt = 0; tt < LDT; ++tt) {
+                const int t = g * LDT + tt;
+                if (t < r) {
+                  const uint32_t e4 = __float_as_uint(xs[t][j0 + jb]);
+#pragma unroll
+                  for (int sb = 0; sb < 4; ++sb) {
+                    const uint32_t e = (e4 >> (8 * sb)) & 0xFFu;
+                    const float c = __fmul_rn(ws[j0 + jb], __uint_as_float(e == 0 ? 0x00400000u : e << 23));
+                    y[t] = fmaf(__uint_as_float(v[jb][4 * tt + sb]), c, y[t]);
+                  }
+                }
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- kernel
 // TOK: token capacity of the accumulators (16 when M <= 16, else 64): the
 // per-token loops are unrolled to it, so the small case keeps its code small
@@ -829,7 +879,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
   P.U = S.U;
   P.N = 16 * ((S.rmax + 15) / 16);
   P.kcmax = min(kMaxKc, kTmemBuf / P.N);
-  P.kcmax1 = MX ? max(1, min(kMaxKc / 4, kTmemBuf / (4 * P.N))) : 0;
+  P.N1 = MX ? 16 * ((4 * S.rmax + 15) / 16) : P.N;
+  P.kcmax1 = MX ? min(kMaxKc, kTmemBuf / P.N1) : 0;
   P.c = blockIdx.x;
   P.G = gridDim.x;
   P.W = min(P.U, a.has_shared ? layer_waves(a.ptok) : max_waves(a.ptok));
@@ -896,6 +947,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = f8_idesc(128, P.N);
+      const uint32_t idesc1 = MX ? f8_idesc(128, P.N1) : idesc;
       Cursor cur;
       Chunk ch;
       int k = 0, ci = 0;
@@ -918,19 +970,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
           }
           tc_fence_after();
           const uint32_t abase = smem_u32(S.A[s]);
-          if (MX && ch.phase == 1) {
-            // One accumulator group per 32-value block: its activation scale differs.
+          // MX GEMM1: N1 rows of B (four per token), one column per (token, 32-value block).
+          const bool mx1 = MX && ch.phase == 1;
+          const int nc = mx1 ? P.N1 : P.N;
+          const uint32_t d = tmem + b * kTmemBuf + j * nc;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc_mma_f8(tmem + b * kTmemBuf + (4 * j + kk) * P.N, sw128_desc(abase + 32 * kk),
-                        sw128_desc(bbase + j * P.N * 128 + 32 * kk), idesc, 0u);
-          } else {
-            const uint32_t d = tmem + b * kTmemBuf + j * P.N;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc_mma_f8(d, sw128_desc(abase + 32 * kk), sw128_desc(bbase + j * P.N * 128 + 32 * kk), idesc,
-                        kk > 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_f8(d, sw128_desc(abase + 32 * kk), sw128_desc(bbase + j * nc * 128 + 32 * kk),
+                      mx1 ? idesc1 : idesc, kk > 0 ? 1u : 0u);
           tc_commit(&S.empty[s]);
         }
         if (!ok) break;
@@ -963,21 +1010,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
       if (S.abort) break;
       tc_fence_after();
       const int r = S.ctx_n[b];
-      float ws[kMaxKc];
-      // MX GEMM1 chunks: four groups per K block, each with the K block's weight scale.
-      const int gsh = (MX && ch.phase == 1) ? 2 : 0;
-#pragma unroll
-      for (int j = 0; j < kMaxKc; ++j) ws[j] = S.wsc[b][ch.phase == 1 ? half : 0][j >> gsh];
-      const int groups = ch.kc << gsh;
       const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16) + b * kTmemBuf;
-      if (r == 1)
-        accumulate<1, 1, 16>(tbase, P.N, groups, r, ws, S.xs[b], y);
-      else if (r <= 4)
-        accumulate<4, 1, 8>(tbase, P.N, groups, r, ws, S.xs[b], y);
-      else if (TOK == 16 || r <= 16)
-        accumulate<16, 1, 2>(tbase, P.N, groups, r, ws, S.xs[b], y);
-      else if constexpr (TOK > 16)
-        accumulate<16, TOK / 16, 1>(tbase, P.N, groups, r, ws, S.xs[b], y);
+      if (MX && ch.phase == 1) {
+        const float* wsp = S.wsc[b][half];
+        if (r == 1)
+          accumulate_mx<1, 1, 8>(tbase, P.N1, ch.kc, r, wsp, S.xs[b], y);
+        else if (r <= 4)
+          accumulate_mx<4, 1, 2>(tbase, P.N1, ch.kc, r, wsp, S.xs[b], y);
+        else if (TOK == 16 || r <= 16)
+          accumulate_mx<4, 4, 1>(tbase, P.N1, ch.kc, r, wsp, S.xs[b], y);
+        else if constexpr (TOK > 16)
+          accumulate_mx<4, TOK / 4, 1>(tbase, P.N1, ch.kc, r, wsp, S.xs[b], y);
+      } else {
+        float ws[kMaxKc];
+#pragma unroll
+        for (int j = 0; j < kMaxKc; ++j) ws[j] = S.wsc[b][ch.phase == 1 ? half : 0][j];
+        if (r == 1)
+          accumulate<1, 1, 16>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
+        else if (r <= 4)
+          accumulate<4, 1, 8>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
+        else if (TOK == 16 || r <= 16)
+          accumulate<16, 1, 2>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
+        else if constexpr (TOK > 16)
+          accumulate<16, TOK / 16, 1>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
+      }
       tc_fence_before();
       if (seg_first) {
         // First chunk of a segment: keep its routes for the segment's end.
