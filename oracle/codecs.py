@@ -97,7 +97,7 @@ def e2m1_encode(values) -> np.ndarray:
 def fp4_unpack(packed, k: int) -> np.ndarray:
     """Nibbles [..., k] from packed E2M1 bytes [..., k/2]: element 2i in the low
     nibble, 2i+1 in the high nibble ("Data Formats": 2 FP4 values per byte,
-    K-major; the nibble order is this build's stated reading)."""
+    K-major; the page does not fix the nibble order, so this one is a reading)."""
     p = np.asarray(packed, dtype=np.uint8)
     out = np.empty(p.shape[:-1] + (k,), dtype=np.uint8)
     out[..., 0::2] = p & 0xF

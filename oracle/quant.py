@@ -49,8 +49,8 @@ def fp8_quant_div(values, ue8m0: bool):
     """Per-128 FP8 quantisation by dividing by the scale.
 
     "mega_moe" ``_MegaKernel.hidden_block``: scale = max(amax, 1e-10) / 448 and
-    codes of ``act / scale``. The page does not round this scale; this build
-    rounds it up to a power of two when ue8m0 (the workload states that every
+    codes of ``act / scale``. The page does not round this scale; here it is
+    rounded up to a power of two when ue8m0 (the workload states that every
     activation scale is rounded), where division and inverse-multiply agree.
     """
     v = np.asarray(values, dtype=np.float32)
