@@ -55,6 +55,8 @@ def parse_args():
                     help="experts resident on the device (smaller for profiler captures; 32 x 44 MB = 1.4 GB)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--mx-launches", action="store_true",
+                    help="only BF16- and MXFP8-token routed FP8 calls at M = 1, 2, 4, 8 (profiling)")
     ap.add_argument("--nvfp4-launches", action="store_true",
                     help="only launch the NVFP4 slot MoE twice at each of M = 1, 8, 64 (for profiler launch lists)")
     return ap.parse_args()
@@ -564,8 +566,36 @@ def nvfp4_launches(args):
     print(json.dumps({"nvfp4_launches": 6}))
 
 
+def mx_launches(args):
+    """Per M = 1, 2, 4, 8: one BF16-token and one MXFP8-token routed FP8 call on the
+    DeepSeek-V3 shape (``--experts`` resident), nothing else: the command the
+    profiles comparing the two instantiations are taken on."""
+    import dataclasses
+
+    import torch
+    import fp4_moe_expert_gb300 as fme
+    from synth import workloads as W
+    dev = torch.device("cuda", 0)
+    cfg = dataclasses.replace(W.DSV3_UE8M0, E=args.experts)
+    w13, s13, w2, s2 = W.fp8_weights_device(cfg, args.seed, dev)
+    for M in MS:
+        x, logits, bias = W.fp8_activations(cfg, M, args.seed, 7)
+        xd = torch.from_numpy(x).to(dev).to(torch.bfloat16)
+        ld = torch.from_numpy(logits).to(dev).to(torch.bfloat16)
+        bd = torch.from_numpy(bias).to(dev)
+        xq, xsc = fme.mxfp8_quantize(xd)
+        rest = (ld, bd, w13, s13, w2, s2, cfg.top_k, cfg.limit, cfg.scale, cfg.ue8m0)
+        fme.moe_routed_fp8(xd, *rest)
+        fme.moe_routed_fp8_mx(xq, xsc, *rest)
+        torch.cuda.synchronize()
+    print(json.dumps({"mx_launches": 2 * len(MS)}))
+
+
 def main():
     args = parse_args()
+    if args.mx_launches:
+        mx_launches(args)
+        return
     if args.nvfp4_launches:
         nvfp4_launches(args)
         return
