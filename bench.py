@@ -322,19 +322,27 @@ def gpu_arm(args, rank, world, local_rank):
         dist.destroy_process_group()
 
 
+def kernel_code_sha256(path):
+    """sha256 of a CUDA source without its whole-line comments and blank lines:
+    changes to the code change it, comment-only edits do not."""
+    import hashlib
+    with open(path) as f:
+        lines = [ln.rstrip() for ln in f]
+    code = [ln for ln in lines if ln.strip() and not ln.strip().startswith("//")]
+    return hashlib.sha256("\n".join(code).encode()).hexdigest()
+
+
 def load_traffic():
     """Mean DRAM bytes (read + write) per launch of the dominant kernel from the
     committed ncu launch list (profiles/traffic.json); None when the kernel
-    source has changed since those counters were taken."""
-    import hashlib
+    code has changed since those counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     src = os.path.join(ROOT, "fp4_moe_expert_gb300", "csrc", "fme_routed_fp8.cu")
     try:
         with open(path) as f:
             d = json.load(f)
-        with open(src, "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != d.get("kernel_source_sha256"):
-                return None
+        if kernel_code_sha256(src) != d.get("kernel_code_sha256"):
+            return None
         return d.get("fp8_moe_kernel_dsv3_bytes_per_launch")
     except Exception:
         return None

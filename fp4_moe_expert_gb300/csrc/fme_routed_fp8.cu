@@ -5,13 +5,13 @@
 // _GateUpKernel, _DownKernel, _group_scale) define. The design is this
 // library's own:
 //
-// * One persistent CTA per SM, six warps: warp 0 streams weight tiles with
-//   TMA (128-byte swizzle, 8 x 16 KB ring, L2 evict-first); warp 1 owns the
-//   tensor memory and issues tcgen05.mma kind::f8f6f4 (M = 128 weight rows,
-//   N = 16 * ceil(tokens / 16), K = 32); warps 2-5 quantise the activations
-//   into the B operand and run the epilogue. Every warp first redoes the
-//   routing of all tokens, so each CTA derives the same list of the unique
-//   experts touched and each expert's weights stream from HBM once.
+// * One persistent CTA per SM, eight warps: warp 0 streams weight tiles with
+//   TMA (128-byte swizzle, 8 x 16 KB ring, L2 evict-first); warp 1 owns TMEM
+//   and issues tcgen05.mma kind::f8f6f4 (M = 128 weight rows, N = 16 *
+//   ceil(tokens / 16), K = 32); warps 2-5 read the accumulators and run the
+//   epilogue; warps 6-7 quantise the activations into the B operand. Every
+//   CTA redoes the routing of all tokens, so each derives the same list of
+//   the unique experts touched and each expert's weights stream once.
 // * The block scales are FP32 and not powers of two, so the MMA cannot apply
 //   them: each 128-wide K block accumulates into its own group of TMEM
 //   columns, and the epilogue multiplies every block's partial by
@@ -21,7 +21,7 @@
 //   rows + the 64 matching second-half rows, K block) slots, GEMM2 is
 //   (expert, tile of 128 rows, K block) slots; every CTA owns an equal
 //   contiguous slice of each phase. A tile cut by slice boundaries is summed
-//   by its last contributor, in CTA order, from partials in the workspace.
+//   by its first contributor, in CTA order, from partials in the workspace.
 // * A finished GEMM1 tile writes its SwiGLU output (f32) to the workspace and
 //   releases a per-expert counter; GEMM2 work of that expert waits for all of
 //   its GEMM1 tiles (bounded wait), then quantises the hidden per 128 itself.
