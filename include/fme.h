@@ -109,9 +109,10 @@ size_t fme_moe_routed_fp8_workspace(int M, int H, int I, int E, int top_k);
  * activation format from "vllm.models.kimi_k3.nvidia.specialized_decode.
  * cutedsl.moe.ep.comm" (EpDispatch). The pages do not print this product; it
  * is y[n] = sum over K blocks b and their 32-value blocks s of
- * P[n, b, s] * (w_scale[n/128, b] * 2^(e[b, s] - 127)), each P an exact
- * FP32 partial (one accumulator per 32-value block). GEMM2 and everything
- * after it as fme_moe_routed_fp8.
+ * P[n, b, s] * (w_scale[n/128, b] * 2^(e[b, s] - 127)), each P the FP32
+ * partial sum of one 32-value block (its own accumulator column), the
+ * scaled partials summed in FP32. GEMM2 and everything after it as
+ * fme_moe_routed_fp8.
  *
  * Arguments: xq [M, H] E4M3 bytes and xscales [M, H/32] E8M0 bytes in place
  * of x; the rest as fme_moe_routed_fp8 (same workspace size function; the two
