@@ -116,11 +116,14 @@ def run_oracle_subprocess(seconds):
     return json.loads(out.stdout.strip().splitlines()[-1])
 
 
-def host_cores():
+def host_cores(cap=32):
+    """Cores this process may run on (at most `cap`: each oracle process holds
+    one expert, about 0.1 GB, in memory)."""
     try:
-        return len(os.sched_getaffinity(0))
+        n = len(os.sched_getaffinity(0))
     except AttributeError:  # pragma: no cover
-        return os.cpu_count() or 1
+        n = os.cpu_count() or 1
+    return max(1, min(n, cap))
 
 
 def run_oracle_parallel(seconds, workers, steps=1):
