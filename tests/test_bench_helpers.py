@@ -30,3 +30,11 @@ def test_committed_traffic_record_matches_the_kernel():
     assert d["kernel_code_sha256"] == bench.kernel_code_sha256(SRC)
     assert bench.load_traffic() == d["fp8_moe_kernel_dsv3_bytes_per_launch"]
     assert 1.0 <= d["fp8_moe_kernel_dsv3_bytes_per_launch"] / d["algorithmic_bytes_per_launch"] < 1.05
+
+
+def test_parallel_oracle_leg_runs_every_process_over_one_window():
+    out = bench.run_oracle_parallel(0.2, 2, steps=2)
+    assert len(out) == 2
+    for step in out:
+        assert step["workers"] == 2 and step["routes"] >= 2 and step["seconds"] > 0
+        assert abs(step["gbs"] - step["routes"] * bench.EXPERT_BYTES / step["seconds"] / 1e9) < 1e-9
