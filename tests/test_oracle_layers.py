@@ -327,3 +327,48 @@ def test_mx_gemv_reduces_to_block_gemv_and_matches_dense_dequant():
     W = codecs.e4m3_decode(w) * np.repeat(np.repeat(ws.astype(np.float64), 128, 0), 128, 1)
     av = codecs.e4m3_decode(a) * np.repeat(np.exp2(e.astype(np.float64) - 127), 32)
     assert np.allclose(mx_block_scaled_gemv(w, ws, a, e), W @ av, rtol=1e-12, atol=1e-300)
+
+
+def test_shared_gate_up_row_order():
+    """"shared_expert" ``_DownKernel`` reads gates at the row base and ups at
+    base + inter, so gate_up rows [0, I) are the gate. Gate rows forced very
+    negative make silu(gate) = 0 and the output vanishes; an oracle that took
+    gate from the second half would give large outputs."""
+    rng = np.random.default_rng(35)
+    M, H, I = 2, 256, 128
+    x = codecs.bf16_round(np.abs(rng.standard_normal((M, H))) + 0.1)
+    w13 = np.empty((2 * I, H), np.uint8)
+    w13[:I] = codecs.e4m3_encode(np.full((I, H), -4.0, np.float32))  # gate: very negative
+    w13[I:] = codecs.e4m3_encode(np.full((I, H), 0.5, np.float32))  # up: positive
+    s13 = np.ones((2, 2), np.float32)
+    w2 = _normalish_codes(rng, (H, I))
+    s2 = np.ones((2, 1), np.float32)
+    out, gu = moe_fp8.shared_fp8(x, w13, s13, w2, s2, 7.0, False)
+    assert (gu[:, :I] < -100).all() and (gu[:, I:] > 10).all()
+    assert (out == 0).all()
+    # the mirror image: gate rows positive, up rows negative -> clamped, non-zero
+    out2, _ = moe_fp8.shared_fp8(x, w13[np.r_[I:2 * I, 0:I]], s13, w2, s2, 7.0, False)
+    assert np.abs(out2).max() > 1.0
+
+
+def test_nvfp4_gate_up_row_order():
+    """"nvfp4-megamoe-kernel README.md", Bugs Found & Fixed §4: L1 rows are the
+    plain concatenation [gate; up]. Gate rows forced very negative make every
+    slot's SiLU zero, so y vanishes; reading gate from the second half would
+    not."""
+    rng = np.random.default_rng(36)
+    M, k, H, N, L = 2, 2, 64, 32, 4
+    x = codecs.bf16_round(np.abs(rng.standard_normal((M, H))) + 0.5)
+    neg4, half = 0xE, 0x1  # E2M1 nibbles of -4.0 and +0.5
+    w13 = np.empty((L, 2 * N, H // 2), np.uint8)
+    w13[:, :N] = neg4 | (neg4 << 4)
+    w13[:, N:] = half | (half << 4)
+    s13 = np.full((L, 2 * N, H // 16), 0x38, np.uint8)  # UE4M3 1.0
+    w2, s2 = _nvfp4_weights(rng, L, H, N)
+    ids = np.array([[0, 1], [2, 3]], np.int32)
+    weights = np.full((M, k), 0.5, np.float32)
+    y = moe_nvfp4.routed_nvfp4(x, ids, weights, w13, s13, w2, s2, 0, L)
+    assert (y == 0).all()
+    swapped = w13[:, np.r_[N:2 * N, 0:N]]
+    y2 = moe_nvfp4.routed_nvfp4(x, ids, weights, swapped, s13, w2, s2, 0, L)
+    assert np.abs(y2).max() > 1.0

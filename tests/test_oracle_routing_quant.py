@@ -169,3 +169,80 @@ def test_nvfp4_stored_scale_is_divisor_and_zero_groups():
     assert (nib[1, 16:32] == 0).all() and d[1, 1] == 0
     deq = codecs.e2m1_decode(nib).reshape(2, 4, 16) * d[..., None]
     assert np.all(np.abs(deq).max(-1) <= 6 * d + 1e-12)
+
+
+# ------------------------------------------------------------------- exact divide quantiser
+def _f32_round(q):
+    """Nearest float32 to the rational q, ties to the even significand
+    (subnormals included, no overflow handling needed here)."""
+    from fractions import Fraction
+    q = Fraction(q)
+    if q == 0:
+        return Fraction(0)
+    a = abs(q)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    ulp = Fraction(2) ** max(e - 23, -149)
+    n = round(a / ulp)  # Fraction.__round__: half to even
+    v = n * ulp
+    return v if q > 0 else -v
+
+
+def _e4m3_code_exact(q):
+    """E4M3 byte of the rational q: nearest finite magnitude by brute force over
+    the 127 non-negative codes, ties to the even code, saturating at 448."""
+    from fractions import Fraction
+    mags = [Fraction(codecs.e4m3_value(c)) for c in range(0x7F)]
+    a = abs(Fraction(q))
+    if a >= mags[-1]:
+        c = 0x7E
+    else:
+        best = None
+        for c0 in range(0x7F):
+            d = abs(mags[c0] - a)
+            if best is None or d < best[0] or (d == best[0] and c0 % 2 == 0):
+                best = (d, c0)
+        c = best[1]
+    return c | 0x80 if q < 0 else c
+
+
+def test_quant_div_is_an_ieee_divide_not_an_inverse_multiply():
+    """"mega_moe" ``hidden_block`` quantises the routed hidden by dividing by its
+    scale (``act / scale``). With a non-power-of-two scale (ue8m0 False) the
+    float32 quotient h / sh can differ from h * float32(1 / sh); the values below
+    are picked where the two land on different sides of an E4M3 rounding
+    midpoint, so an oracle quantising by the inverse fails this exact check."""
+    from fractions import Fraction
+    amax = np.float32(300.0)
+    sh = _f32_round(Fraction(float(amax)) / 448)  # float32(max(amax, 1e-10) / 448)
+    inv = np.float32(1.0) / np.float32(float(sh))
+    mags = [Fraction(codecs.e4m3_value(c)) for c in range(0x7F)]
+    mids = [(mags[i] + mags[i + 1]) / 2 for i in range(40, 120)]
+    picked = []
+    for m in mids:
+        centre = np.float32(float(m * sh))
+        h = centre
+        for _ in range(6):  # a few float32 steps either side of m * sh
+            h = np.nextafter(h, np.float32(-np.inf), dtype=np.float32)
+        for _ in range(13):
+            div = _e4m3_code_exact(_f32_round(Fraction(float(h)) / sh))
+            mul = _e4m3_code_exact(Fraction(float(np.float32(h * inv))))
+            if div != mul:
+                picked.append(float(h))
+                break
+            h = np.nextafter(h, np.float32(np.inf), dtype=np.float32)
+        if len(picked) >= 8:
+            break
+    assert len(picked) >= 4, "no discriminating values found"
+    block = np.zeros(128, np.float32)
+    block[0] = amax
+    block[1:1 + len(picked)] = picked
+    block[64:64 + len(picked)] = -np.asarray(picked, np.float32)
+    codes, scale = quant.fp8_quant_div(block[None, :], False)
+    assert Fraction(float(scale[0, 0])) == sh
+    want = [_e4m3_code_exact(_f32_round(Fraction(float(v)) / sh)) for v in block]
+    assert codes[0].tolist() == want
+    # and the same block quantised by the inverse differs (the check can fail)
+    codes_mul, _ = quant.fp8_quant_mul(block[None, :], False)
+    assert (codes_mul[0] != codes[0]).sum() >= len(picked)
