@@ -21,6 +21,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -55,8 +56,11 @@ def parse_args():
                     help="experts resident on the device (smaller for profiler captures; 32 x 44 MB = 1.4 GB)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-flushed", action="store_true", help="skip the L2-flushed per-M calls")
     ap.add_argument("--mx-launches", action="store_true",
                     help="only BF16- and MXFP8-token routed FP8 calls at M = 1, 2, 4, 8 (profiling)")
+    ap.add_argument("--shared-launches", action="store_true",
+                    help="only launch the FP8 shared expert alone twice at each of M = 1, 8 (for profiles)")
     ap.add_argument("--nvfp4-launches", action="store_true",
                     help="only launch the NVFP4 slot MoE twice at each of M = 1, 8, 64 (for profiler launch lists)")
     return ap.parse_args()
@@ -212,11 +216,10 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"fme_clocks_rank{index}_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
@@ -343,6 +346,10 @@ def gpu_arm(args, rank, world, local_rank):
                          "GBps_median": round(float(np.median(bytes_call[sel] / (launch_ms[sel] * 1e-3) / 1e9)), 1)}
     peak, peak_kind = peaks()
     achieved = float(bytes_call.sum() / (launch_ms.sum() * 1e-3) / 1e9)
+    for M in MS:
+        per_m[str(M)]["pct_of_peak_median"] = round(100.0 * per_m[str(M)]["GBps_median"] / peak, 1)
+    if not args.no_flushed:
+        flushed_per_m(fme, torch, cfg, xs, logits_pool, bias, w13, s13, w2, s2, outs, ws, dev, per_m, peak)
     traffic = load_traffic()
 
     e2e = None if args.no_e2e else e2e_leg(fme, cfg, w13, s13, w2, s2, bias, dev, args)
@@ -371,7 +378,8 @@ def gpu_arm(args, rank, world, local_rank):
         "config": {"workload": "dsv3_routed_fp8: H 7168, I 2048, E 256, top_k 8, M in {1,2,4,8} per step, "
                    "BF16 logits, non-pow2 FP32 block scales", "global_batch": sum(MS) * world, "seq_len": 1,
                    "parallelism": "replicas" if world > 1 else "single-gpu",
-                   "l2": "no flush: each call streams >= 352 MB of weights (> 129 MB L2) and fresh routing",
+                   "l2": "timed region: no flush, each call streams >= 352 MB of weights (> 129 MB L2) with "
+                         "fresh routing; per_m also gives 50 calls per M with L2 flushed (512 MB read) before each",
                    "per_m": per_m, "unique_experts_per_step": round(float(uniq.sum() / args.steps), 2)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
@@ -386,6 +394,39 @@ def gpu_arm(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def flushed_per_m(fme, torch, cfg, xs, logits_pool, bias, w13, s13, w2, s2, outs, ws, dev, per_m, peak, calls=50):
+    """Per M, `calls` more calls with L2 flushed before each (a 512 MB read,
+    outside the events) and fresh logits each time: median microseconds and
+    GB/s of the unique experts each call touched, beside the back-to-back
+    figures of the timed region."""
+    flush = torch.ones(128 * 1024 * 1024, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for M in MS:
+        out, ids, wts = outs[M]
+        us, gbs = [], []
+        for i in range(calls + 3):
+            flush.amax()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fme.moe_routed_fp8(xs[M], logits_pool[(7 * i + M) % len(logits_pool)][:M], bias, w13, s13, w2, s2,
+                               cfg.top_k, cfg.limit, cfg.scale, cfg.ue8m0, out=out, ids=ids, weights=wts,
+                               workspace=ws)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                t = a.elapsed_time(b) * 1e3
+                u = len(set(ids.reshape(-1).tolist()))
+                us.append(t)
+                gbs.append(u * EXPERT_BYTES / (t * 1e-6) / 1e9)
+        if ws.error():
+            raise SystemExit("device error word set in the flushed per-M calls")
+        d = per_m[str(M)]
+        d["us_median_l2_flushed"] = round(float(np.median(us)), 2)
+        d["GBps_median_l2_flushed"] = round(float(np.median(gbs)), 1)
+        d["pct_of_peak_median_l2_flushed"] = round(100.0 * float(np.median(gbs)) / peak, 1)
+    del flush
 
 
 def kernel_code_sha256(path):
@@ -549,6 +590,48 @@ def layer_measurements(fme, dev, args, shared_w, shared_bytes, flush):
     return res
 
 
+def latent_measurements(fme, dev, args, flush, calls=20):
+    """Latent-MoE shape (H 3584, I 2048, 896 experts, top_k 16, FP32 logits, skewed
+    bias N(0, 0.5)) at M = 1, 5, 16, 32: median microseconds of `calls` calls,
+    L2 flushed before each, fresh logits each call; GB/s = unique experts x
+    22,025,472 B over the call's time."""
+    import torch
+    from synth import workloads as W
+
+    cfg = W.LATENT
+    per_expert = 4096 * 3584 + 3584 * 2048 + 4 * (32 * 28 + 28 * 16)
+    w13, s13, w2, s2 = W.fp8_weights_device(cfg, args.seed, dev)
+    ws = fme.Workspace(fme.moe_routed_fp8_workspace(max(cfg.Ms), cfg.H, cfg.I, cfg.E, cfg.top_k), dev)
+    res = {}
+    for M in cfg.Ms:
+        x, _, bias = W.fp8_activations(cfg, M, args.seed, 0)
+        xd = torch.from_numpy(x).to(dev).to(torch.bfloat16)
+        bd = torch.from_numpy(bias).to(dev)
+        lgs = [torch.from_numpy(W.fp8_activations(cfg, M, args.seed, 100 + i)[1]).to(dev) for i in range(calls + 3)]
+        us, gbs, uq = [], [], []
+        for i, ld in enumerate(lgs):
+            flush.amax()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            _, ids, _ = fme.moe_routed_fp8(xd, ld, bd, w13, s13, w2, s2, cfg.top_k, cfg.limit, cfg.scale, cfg.ue8m0,
+                                           workspace=ws)
+            b.record()
+            torch.cuda.synchronize()
+            if i >= 3:
+                t = a.elapsed_time(b) * 1e3
+                u = len(set(ids.reshape(-1).tolist()))
+                us.append(t)
+                uq.append(u)
+                gbs.append(u * per_expert / (t * 1e-6) / 1e9)
+        if ws.error():
+            raise RuntimeError("device wait timed out in the latent measurement")
+        res[f"latent_routed_fp8_M{M}"] = {"us_median": round(float(np.median(us)), 2),
+                                         "unique_experts_mean": round(float(np.mean(uq)), 2),
+                                         "GBps_median": round(float(np.median(gbs)), 1)}
+    del w13, w2
+    return res
+
+
 def side_measurements(fme, dev, args):
     """Shared expert (UE8M0, H 7168 / I 2048) and NVFP4 slot MoE latencies."""
     import torch
@@ -561,6 +644,7 @@ def side_measurements(fme, dev, args):
     shared_bytes = w13.numel() + w2.numel() + 4 * (s13.numel() + s2.numel())
     flush = torch.ones(128 * 1024 * 1024, dtype=torch.int32, device=dev)
     res.update(layer_measurements(fme, dev, args, (w13, s13, w2, s2), shared_bytes, flush))
+    res.update(latent_measurements(fme, dev, args, flush))
     for M in (1, 8):
         x = torch.from_numpy(W.fp8_activations(W.DSV3, M, args.seed, 3)[0]).to(dev).to(torch.bfloat16)
         ts = []
@@ -640,6 +724,23 @@ def nvfp4_launches(args):
     print(json.dumps({"nvfp4_launches": 6}))
 
 
+def shared_launches(args):
+    """The FP8 shared expert alone (UE8M0, H 7168 / I 2048), two calls at each of
+    M = 1 and 8, nothing else: the command the profiles of that launch are taken on."""
+    import torch
+    import fp4_moe_expert_gb300 as fme
+    from synth import workloads as W
+    dev = torch.device("cuda", 0)
+    cfg = W.SHARED
+    w13, s13, w2, s2 = (torch.from_numpy(v).to(dev) for v in W.shared_weights_host(cfg, args.seed))
+    for M in (1, 8):
+        x = torch.from_numpy(W.fp8_activations(W.DSV3, M, args.seed, 3)[0]).to(dev).to(torch.bfloat16)
+        for _ in range(2):
+            fme.shared_expert_fp8(x, w13, s13, w2, s2, cfg.limit, cfg.ue8m0)
+        torch.cuda.synchronize()
+    print(json.dumps({"shared_launches": 4}))
+
+
 def mx_launches(args):
     """Per M = 1, 2, 4, 8: one BF16-token and one MXFP8-token routed FP8 call on the
     DeepSeek-V3 shape (``--experts`` resident), nothing else: the command the
@@ -672,6 +773,9 @@ def main():
         return
     if args.nvfp4_launches:
         nvfp4_launches(args)
+        return
+    if args.shared_launches:
+        shared_launches(args)
         return
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))

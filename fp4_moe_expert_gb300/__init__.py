@@ -31,6 +31,7 @@ SIGNATURES = {
                                        _c_int, _c_float, _c_float, _c_int, _vp, _vp, _vp, _vp, _c_size, _vp]),
     "fme_moe_routed_fp8_noalloc": (_c_int, [_vp, _vp, _c_int, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                             _c_int, _c_int, _c_float, _c_float, _c_int, _vp, _vp, _vp, _vp]),
+    "fme_moe_routed_fp8_noalloc_error": (_c_int, [_vp, _vp]),
     "fme_shared_expert_fp8": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_float, _c_int, _vp,
                                        _vp, _vp, _c_size, _vp]),
     "fme_shared_expert_fp8_workspace": (_c_size, [_c_int] * 3),

@@ -122,18 +122,6 @@ static bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) &
     if (!(cond)) return set_last_error(status, __VA_ARGS__); \
   } while (0)
 
-extern "C" {
-
-const char* fme_last_error(void) { return g_last_error; }
-
-int fme_version(void) { return 100; }
-
-int fme_sm_count(void) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-  return device_sm_count(dev);
-}
-
 static int check_fp8_shapes(int M, int H, int I, int E, int top_k, float limit) {
   FME_REQUIRE(M >= 1 && M <= kMaxTokens, FME_EUNSUPPORTED, "M=%d outside [1, %d]", M, kMaxTokens);
   FME_REQUIRE(H >= 128 && H % 128 == 0 && I >= 128 && I % 128 == 0, FME_EINVAL,
@@ -146,15 +134,11 @@ static int check_fp8_shapes(int M, int H, int I, int E, int top_k, float limit) 
   return FME_OK;
 }
 
-size_t fme_moe_routed_fp8_workspace(int M, int H, int I, int E, int top_k) {
-  if (check_fp8_shapes(M, H, I, E, top_k, 1.0f) != FME_OK) return 0;
-  return layer_fp8_workspace_bytes(M, H, I, E, top_k, false);
-}
-
-int fme_moe_routed_fp8(const void* x, const void* logits, int logits_dtype, const float* bias, const uint8_t* w13,
-                       const float* s13, const uint8_t* w2, const float* s2, int M, int H, int I, int E, int top_k,
-                       float limit, float scale, int ue8m0, void* out, int32_t* ids, float* weights,
-                       void* workspace, size_t workspace_bytes, void* stream) {
+namespace fme {
+int check_routed_fp8_args(const void* x, const void* logits, int logits_dtype, const float* bias, const uint8_t* w13,
+                          const float* s13, const uint8_t* w2, const float* s2, int M, int H, int I, int E, int top_k,
+                          float limit, float scale, const void* out, const int32_t* ids, const float* weights,
+                          const void* workspace) {
   FME_REQUIRE(x && logits && bias && w13 && s13 && w2 && s2 && out && ids && weights, FME_EINVAL,
               "null pointer argument");
   const int st = check_fp8_shapes(M, H, I, E, top_k, limit);
@@ -165,6 +149,35 @@ int fme_moe_routed_fp8(const void* x, const void* logits, int logits_dtype, cons
                   !misaligned(w2) && !misaligned(s2) && !misaligned(out) && !misaligned(ids) &&
                   !misaligned(weights) && !misaligned(workspace),
               FME_EALIGN, "every pointer must be 16-byte aligned");
+  return FME_OK;
+}
+}  // namespace fme
+
+extern "C" {
+
+const char* fme_last_error(void) { return g_last_error; }
+
+int fme_version(void) { return 100; }
+
+int fme_sm_count(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return device_sm_count(dev);
+}
+
+size_t fme_moe_routed_fp8_workspace(int M, int H, int I, int E, int top_k) {
+  if (check_fp8_shapes(M, H, I, E, top_k, 1.0f) != FME_OK) return 0;
+  return layer_fp8_workspace_bytes(M, H, I, E, top_k, false);
+}
+
+
+int fme_moe_routed_fp8(const void* x, const void* logits, int logits_dtype, const float* bias, const uint8_t* w13,
+                       const float* s13, const uint8_t* w2, const float* s2, int M, int H, int I, int E, int top_k,
+                       float limit, float scale, int ue8m0, void* out, int32_t* ids, float* weights,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  const int st = check_routed_fp8_args(x, logits, logits_dtype, bias, w13, s13, w2, s2, M, H, I, E, top_k, limit,
+                                       scale, out, ids, weights, workspace);
+  if (st != FME_OK) return st;
   RoutedFp8 r;
   r.x = x;
   r.logits = logits;

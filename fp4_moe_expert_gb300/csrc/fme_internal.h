@@ -57,6 +57,13 @@ struct SharedFp8 {
   void* out = nullptr;
 };
 
+// Host-side checks of a routed FP8 call (pointers, shapes, dtype, scale,
+// 16-byte alignment): FME_OK or the status fme_moe_routed_fp8 returns.
+int check_routed_fp8_args(const void* x, const void* logits, int logits_dtype, const float* bias, const uint8_t* w13,
+                          const float* s13, const uint8_t* w2, const float* s2, int M, int H, int I, int E, int top_k,
+                          float limit, float scale, const void* out, const int32_t* ids, const float* weights,
+                          const void* workspace);
+
 // One launch of the tcgen05 kernel over the routed experts and/or the shared
 // expert of M tokens (arguments already validated).
 int layer_fp8(const RoutedFp8& r, const SharedFp8& sh, int M, int H, int I, void* workspace, size_t workspace_bytes,

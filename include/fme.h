@@ -141,17 +141,31 @@ int fme_moe_routed_fp8_mx(const uint8_t* xq, const uint8_t* xscales, const void*
  *   H = 7168, I = 2048, top_k = 8 up to M = 32 tokens). Larger requests
  *   return FME_EUNSUPPORTED.
  * - First call per device: it looks up the array's device address with that
- *   device current. Make that first call before any stream capture.
+ *   device current. Make that first call before any stream capture. The
+ *   address is cached per device and looked up again when the device's
+ *   context has changed (after cudaDeviceReset).
  * - Every call shares the one array and zeroes its counters first, so calls
  *   that overlap on the GPU (other streams, other host threads) race and
  *   corrupt each other: issue them in one stream order.
- * - The device error word lives in the shared array; it is not readable
- *   through fme_workspace_error.
+ * - Arguments are checked exactly as fme_moe_routed_fp8 checks them, before
+ *   the array is touched: a rejected call leaves it as it was.
+ * - The device error word lives in the shared array. Calls do not clear it:
+ *   a bit set by any call stays set until fme_moe_routed_fp8_noalloc_error
+ *   reads it.
  */
 int fme_moe_routed_fp8_noalloc(const void* x, const void* logits, int logits_dtype, const float* bias,
                                const uint8_t* w13, const float* s13, const uint8_t* w2, const float* s2,
                                int M, int H, int I, int E, int top_k, float limit, float scale, int ue8m0,
                                void* out, int32_t* ids, float* weights, void* stream);
+
+/*
+ * Read and clear the device error word of fme_moe_routed_fp8_noalloc on the
+ * current device (synchronises stream). No counterpart in the pages. The
+ * bits are those of fme_workspace_error and accumulate over every no-alloc
+ * call since the last read. Allocates nothing. *code receives the word;
+ * returns FME_ETIMEOUT when it is non-zero, FME_OK otherwise.
+ */
+int fme_moe_routed_fp8_noalloc_error(int* code, void* stream);
 
 /*
  * FP8 shared expert for M decode tokens.

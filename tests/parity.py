@@ -62,14 +62,45 @@ def assert_outputs(got, ref, what="out", exact=None):
     return r
 
 
-def assert_routing(ids, weights, ref_ids, ref_weights, gaps=None, min_gap=1e-6):
-    """ids must match exactly except for tokens whose decisive key gap (from the
-    oracle, in float32) is below `min_gap`: there a few-ulp sigmoid difference
-    may legitimately swap two picks, and only the set/weights are checked."""
+GAP_ULPS = 4  # near-tie excuse of the routing comparison, in float32 ulps of the keys
+
+
+def decisive_gap_ulps(keys, ids):
+    """Per token, the smallest gap that decides its picks or their order (between
+    consecutive picked keys, and between the k-th pick and the best unpicked
+    key), in float32 ulps at the larger key of each pair, from the oracle's
+    float32 keys [M, E] and ids [M, k]."""
+    keys = np.asarray(keys, dtype=np.float32)
+    ids = np.asarray(ids)
+    M, E = keys.shape
+    out = np.full(M, np.inf)
+    for t in range(M):
+        ordered = [keys[t, int(e)] for e in ids[t]]
+        picked = set(int(e) for e in ids[t])
+        rest = [keys[t, e] for e in range(E) if e not in picked]
+        pairs = list(zip(ordered, ordered[1:]))
+        if rest:
+            pairs.append((min(ordered), max(rest)))
+        for a, b in pairs:
+            ulp = float(np.spacing(np.float32(max(abs(a), abs(b)))))
+            out[t] = min(out[t], (float(a) - float(b)) / ulp)
+    return out
+
+
+def assert_routing(ids, weights, ref_ids, ref_weights, keys=None, max_ulps=GAP_ULPS):
+    """ids must match the oracle's exactly. The one excuse: a token whose
+    decisive key gap (decisive_gap_ulps, from the oracle's keys) is below
+    `max_ulps` float32 ulps, where the kernel's sigmoid (CUDA expf, IEEE add
+    and divide) and the oracle's correctly rounded one may order two keys
+    differently; such a token must still pick the same set up to the one
+    swapped boundary pick. Weights at matching picks are within 1e-6 relative.
+    Returns the number of excused tokens (also printed when non-zero)."""
     ids, ref_ids = np.asarray(ids), np.asarray(ref_ids)
+    gaps = None if keys is None else decisive_gap_ulps(keys, ref_ids)
+    excused = 0
     for t in range(ids.shape[0]):
-        if gaps is not None and gaps[t] < min_gap:
-            # a near-tie may swap at most the boundary pick
+        if gaps is not None and gaps[t] < max_ulps:
+            excused += 1
             assert len(set(ids[t].tolist()) ^ set(ref_ids[t].tolist())) <= 2, f"token {t}"
             continue
         assert (ids[t] == ref_ids[t]).all(), f"token {t}: {ids[t]} vs {ref_ids[t]}"
@@ -77,3 +108,6 @@ def assert_routing(ids, weights, ref_ids, ref_weights, gaps=None, min_gap=1e-6):
     same = ids == ref_ids
     assert np.all(np.abs(w - rw)[same] <= WEIGHT_RTOL * np.abs(rw)[same] + 1e-30), \
         f"weights: max rel err {np.max(np.abs(w - rw)[same] / np.abs(rw)[same])}"
+    if excused:
+        print(f"routing: {excused} of {ids.shape[0]} tokens excused (decisive key gap < {max_ulps} ulp)")
+    return excused

@@ -172,3 +172,20 @@ def test_layer_validation_and_workspace(fme):
     assert fme.moe_layer_fp8_workspace(0, 7168, 2048, 256, 8) == 0
     # a workspace too small for the call is refused before any launch
     assert _layer(fme, wsb=64) in (-6, -4)
+
+
+def test_noalloc_checks_arguments_before_touching_its_scratch(fme):
+    """The allocation-free variant runs fme_moe_routed_fp8's host checks before
+    any CUDA call, so these rejections need no GPU."""
+    vp = ctypes.c_void_p
+    null = vp(16)
+    rc = fme.lib.fme_moe_routed_fp8_noalloc(None, null, 0, null, null, null, null, null, 1, 256, 128, 8, 2, 7.0,
+                                            1.0, 0, null, null, null, None)
+    assert rc == -1 and "null" in fme.lib.fme_last_error().decode()
+    rc = fme.lib.fme_moe_routed_fp8_noalloc(null, null, 0, null, null, null, null, null, 1, 256, 100, 8, 2, 7.0,
+                                            1.0, 0, null, null, null, None)
+    assert rc == -1  # I not a multiple of 128
+    rc = fme.lib.fme_moe_routed_fp8_noalloc(vp(24), null, 0, null, null, null, null, null, 1, 256, 128, 8, 2, 7.0,
+                                            1.0, 0, null, null, null, None)
+    assert rc == -3  # misaligned x
+    assert fme.lib.fme_moe_routed_fp8_noalloc_error(None, None) == -1

@@ -46,8 +46,7 @@ def _run_small(fme, cfg, M, seed, top_k=None, **over):
     torch.cuda.synchronize()
     ref, rids, rw, keys = moe_fp8.routed_fp8(x, logits, bias, w13h, s13, w2h, s2, top_k, cfg.limit, cfg.scale,
                                              cfg.ue8m0)
-    gaps = routing.selection_gap(keys, rids)
-    assert_routing(ids.cpu().numpy(), wts.cpu().numpy(), rids, rw, gaps)
+    assert_routing(ids.cpu().numpy(), wts.cpu().numpy(), rids, rw, keys)
     got = out.float().cpu().numpy()
     return got, ref, ids.cpu().numpy(), rids
 
@@ -123,7 +122,7 @@ def test_routed_one_workspace_serves_every_token_count(fme):
         assert ws.error() == 0, (step, M)
         ref, rids, rw, keys = moe_fp8.routed_fp8(x, logits, bias, w13h, s13, w2h, s2, cfg.top_k, cfg.limit,
                                                  cfg.scale, cfg.ue8m0)
-        assert_routing(ids.cpu().numpy(), wts.cpu().numpy(), rids, rw, routing.selection_gap(keys, rids))
+        assert_routing(ids.cpu().numpy(), wts.cpu().numpy(), rids, rw, keys)
         assert_outputs(out.float().cpu().numpy(), ref)
 
 
@@ -137,7 +136,7 @@ def _full_size(fme, cfg, M, seed, routes, rows):
     torch.cuda.synchronize()
     ref, rids, rw, keys = moe_fp8.routed_fp8(x, logits, bias, w13h, s13h, w2h, s2h, cfg.top_k, cfg.limit,
                                              cfg.scale, cfg.ue8m0, routes=routes, rows=rows)
-    assert_routing(ids.cpu().numpy(), wts.cpu().numpy(), rids, rw, routing.selection_gap(keys, rids))
+    assert_routing(ids.cpu().numpy(), wts.cpu().numpy(), rids, rw, keys)
     # the device-filled weights are the generator's bytes
     e = int(rids.reshape(-1)[routes[0]])
     assert np.array_equal(w13[e, :64].cpu().numpy(), w13h[e][:64])
@@ -164,6 +163,29 @@ def test_latent_m32_sampled_routes(fme):
     rng = np.random.default_rng(2)
     routes = sorted(rng.choice(32 * 16, 5, replace=False).tolist())
     _full_size(fme, W.LATENT, 32, seed=14, routes=routes, rows=np.arange(3584))
+
+
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_latent_full_size(fme, M):
+    """Latent-MoE shape (H 3584, I 2048, 896 experts, top_k 16, FP32 logits, skewed
+    bias N(0, 0.5)) at full size: every route at M = 1; at M = 5 and 16 the
+    routes of the expert picked by the most tokens (expert sharing) plus
+    others, each compared on all 3584 rows."""
+    cfg = W.LATENT
+    x, logits, bias = W.fp8_activations(cfg, M, 15 + M)
+    ids, _, _ = routing.route(logits, bias, cfg.top_k, cfg.scale)
+    if M == 1:
+        routes = list(range(cfg.top_k))
+    else:
+        flat = ids.reshape(-1)
+        vals, counts = np.unique(flat, return_counts=True)
+        shared = int(vals[np.argmax(counts)])
+        assert counts.max() >= 2, "the skewed bias should make some expert shared"
+        routes = [int(r) for r in np.nonzero(flat == shared)[0][:3]]
+        rng = np.random.default_rng(M)
+        rest = [r for r in range(M * cfg.top_k) if r not in routes]
+        routes = sorted(routes + rng.choice(rest, 3, replace=False).tolist())
+    _full_size(fme, cfg, M, seed=15 + M, routes=routes, rows=np.arange(cfg.H))
 
 
 @pytest.mark.parametrize("M", [1, 3])

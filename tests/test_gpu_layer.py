@@ -56,7 +56,7 @@ def _check_layer(fme, cfg, scfg, M, seed, ws=None, shared_ws=None):
     assert ws.error() == 0
     ref, rids, rw, keys = moe_fp8.routed_fp8(x, logits, bias, w13h, s13, w2h, s2, cfg.top_k, cfg.limit, cfg.scale,
                                              cfg.ue8m0)
-    assert_routing(ids.cpu().numpy(), wts.cpu().numpy(), rids, rw, routing.selection_gap(keys, rids))
+    assert_routing(ids.cpu().numpy(), wts.cpu().numpy(), rids, rw, keys)
     assert_outputs(out.float().cpu().numpy(), ref, "routed")
     sref, _ = moe_fp8.shared_fp8(x, sw13, ss13, sw2, ss2, scfg.limit, scfg.ue8m0)
     assert_outputs(sout.float().cpu().numpy(), sref, "shared")
@@ -113,7 +113,7 @@ def test_layer_dsv3_full_size(fme):
     ref, rids, rw, keys = moe_fp8.routed_fp8(x, logits, bias, w13h, s13.cpu().numpy(), w2h, s2.cpu().numpy(),
                                              cfg.top_k, cfg.limit, cfg.scale, cfg.ue8m0, routes=routes,
                                              rows=np.arange(7168))
-    assert_routing(ids.cpu().numpy(), wts.cpu().numpy(), rids, rw, routing.selection_gap(keys, rids))
+    assert_routing(ids.cpu().numpy(), wts.cpu().numpy(), rids, rw, keys)
     assert_outputs(out.float().cpu().numpy()[routes], ref[routes], "routed")
     sref, _ = moe_fp8.shared_fp8(x, sw13, ss13, sw2, ss2, scfg.limit, scfg.ue8m0)
     assert_outputs(sout.float().cpu().numpy(), sref, "shared")

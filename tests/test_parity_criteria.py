@@ -59,3 +59,23 @@ def test_oracle_exact_output_rounds_to_its_output():
                                              cfg.ue8m0, exact=True)
     assert np.array_equal(bf16_round(exact), out)
     assert not np.array_equal(exact, out.astype(np.float64))
+
+
+def test_routing_excuse_is_a_few_ulps_of_the_keys():
+    """A swap of two picks is excused only where the oracle's deciding keys
+    are within GAP_ULPS float32 ulps of each other; the count is returned."""
+    import pytest
+    from tests.parity import GAP_ULPS, assert_routing, decisive_gap_ulps
+    one = np.float32(0.75)
+    ulp = float(np.spacing(one))
+    keys = np.array([[0.9, 0.75, 0.75 - 2 * ulp, 0.1],       # ranks 2/3 two ulps apart
+                     [0.9, 0.75, 0.75 - 10 * ulp, 0.1]], np.float32)
+    ref = np.array([[0, 1, 2], [0, 1, 2]], np.int32)
+    w = np.full((2, 3), 1 / 3, np.float32)
+    g = decisive_gap_ulps(keys, ref)
+    assert g[0] == pytest.approx(2.0) and g[1] == pytest.approx(10.0)
+    swapped = np.array([[0, 2, 1], [0, 1, 2]], np.int32)
+    assert assert_routing(swapped, w, ref, w, keys) == 1
+    with pytest.raises(AssertionError):
+        assert_routing(np.array([[0, 1, 2], [0, 2, 1]], np.int32), w, ref, w, keys)
+    assert GAP_ULPS <= 4

@@ -60,6 +60,11 @@ def test_noalloc_matches_workspace_entry_point_twice(fme):
         assert torch.equal(ids, ref_ids)
         assert np.allclose(wts.cpu().numpy(), ref_w.cpu().numpy(), rtol=1e-6, atol=0)
         assert_outputs(out.float().cpu().numpy(), ref_out.float().cpu().numpy(), f"call {step}")
+    # Both calls finished without a device-side error: the variant's own error
+    # word (in the static array, not in any workspace) reads zero.
+    code = ctypes.c_int(-1)
+    rc = fme.lib.fme_moe_routed_fp8_noalloc_error(ctypes.byref(code), stream)
+    assert rc == 0 and code.value == 0, fme.lib.fme_last_error().decode()
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch(fme):
