@@ -28,11 +28,13 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
 #include "fme_common.cuh"
 #include "fme_internal.h"
+#include "fme_plan.cuh"
 
 namespace fme {
 
@@ -44,23 +46,6 @@ constexpr int kBBufBytes = 256 * 128;    // K blocks x N token rows x 128 bytes 
 constexpr int kTmemCols = 512;
 constexpr int kTmemBuf = 256;            // two accumulator buffers
 constexpr int kMaxKc = 16;
-// Waves: the unit list is cut into W consecutive groups; every CTA takes a
-// share of every wave and runs GEMM1 of wave w + 1 before GEMM2 of wave w, so
-// one wave's GEMM1 -> GEMM2 hand-over (last tiles finishing, hidden rows
-// re-quantised) overlaps the next wave's weight stream, and each CTA's work
-// mixes experts hit by different token counts. Every wave adds split tiles,
-// each with a partial round trip. Measured on the DeepSeek-V3 shape: three
-// waves pay off at 5-8 tokens (M = 8: 414 -> 389 us); at 1-4 tokens two
-// waves were slower than one. With the shared expert as one more unit (the
-// one-launch layer, run as one launch up to 4 tokens) two waves pay off at
-// 3-4 tokens (M = 4: 269 -> 244 us).
-__host__ __device__ constexpr int max_waves(int ptok) { return ptok > 4 && ptok <= 8 ? 3 : 1; }
-__host__ __device__ constexpr int layer_waves(int ptok) { return ptok > 2 && ptok <= 4 ? 2 : 1; }
-// Waves the partial-sum region is sized for, any call.
-__host__ __device__ constexpr int waves_cap(int ptok) {
-  return max_waves(ptok) > layer_waves(ptok) ? max_waves(ptok) : layer_waves(ptok);
-}
-
 struct TcArgs {
   CUtensorMap map13;   // routed W13 as [E * 2I rows, H bytes], box 64 rows x 128 bytes
   CUtensorMap map2;    // routed W2 as [E * H rows, I bytes]
@@ -92,6 +77,11 @@ struct TcArgs {
   float limit, scale;
   float slimit;      // shared-expert SwiGLU clamp
   int ue8m0, logits_f32, has_shared;
+  // Phases this launch runs (1 = GEMM1 .. SwiGLU, 2 = hidden re-quant ..
+  // GEMM2): 1..2 for the one persistent launch; the two-kernel chain runs
+  // 1..1, then 2..2 as a programmatic dependent launch that streams its W2
+  // tiles before it waits for the first kernel.
+  int phase_lo, phase_hi;
   int sue8m0;        // shared-expert activation scales rounded up to powers of two
   unsigned long long timeout_ns;
 };
@@ -187,106 +177,6 @@ __device__ void route_token(const TcArgs& a, TcSmem& S, int t, int lane, bool wr
     }
   }
 }
-
-// ---------------------------------------------------------------- work plan
-// The units are cut into W waves of consecutive units. The slots of one
-// (wave, phase) -- units x tiles x K blocks, at most 1025 x 128 x 64 = 8.4M --
-// are split over Ge = min(G, n) CTAs: CTA c < Ge owns [n*c/Ge, n*(c+1)/Ge),
-// never empty; CTAs c >= Ge own nothing. The products stay below 8.4M x 161
-// < 2^32, so unsigned 32-bit arithmetic is exact.
-struct PhasePlan {
-  int n, lo, hi;
-  int Ge, tiles, nb;
-  int w, u0;  // wave and its first unit
-  __device__ int lo_of(int c) const {
-    return c >= Ge ? n : static_cast<int>(static_cast<uint32_t>(n) * static_cast<uint32_t>(c) /
-                                          static_cast<uint32_t>(Ge));
-  }
-  // The CTA whose slice holds slot x.
-  __device__ int cta_of(int x) const {
-    return static_cast<int>((static_cast<uint32_t>(x + 1) * static_cast<uint32_t>(Ge) + static_cast<uint32_t>(n) - 1u) /
-                            static_cast<uint32_t>(n)) - 1;
-  }
-};
-
-struct Plan {
-  int U, N, kcmax, c, G, W;
-  int N1, kcmax1;  // the MX kernel's GEMM1 B rows (four per token) and K blocks per chunk
-  int tiles[2], nb[2];  // per unit: GEMM1 64-row tiles x H/128 K blocks; GEMM2 128-row tiles x I/128
-  __device__ int wave_lo(int w) const { return U * w / W; }
-  // Stage q of 2W: GEMM1 of wave 0, then GEMM1(w + 1) / GEMM2(w) pairs, then
-  // the last GEMM2.
-  __device__ void stage(int q, int& w, int& phase) const {
-    if (q == 0) {
-      w = 0;
-      phase = 1;
-    } else if (q < 2 * W - 1) {
-      w = (q & 1) ? (q + 1) / 2 : q / 2 - 1;
-      phase = (q & 1) ? 1 : 2;
-    } else {
-      w = W - 1;
-      phase = 2;
-    }
-  }
-  __device__ PhasePlan plan(int w, int phase) const {
-    PhasePlan pp;
-    const int u0 = wave_lo(w), u1 = wave_lo(w + 1);
-    const int t = tiles[phase - 1], nbp = nb[phase - 1];
-    pp.n = (u1 - u0) * t * nbp;
-    pp.tiles = t;
-    pp.nb = nbp;
-    pp.w = w;
-    pp.u0 = u0;
-    pp.Ge = min(G, pp.n);
-    if (c >= pp.Ge) {
-      pp.lo = pp.hi = pp.n;
-    } else {
-      pp.lo = pp.lo_of(c);
-      pp.hi = pp.lo_of(c + 1);
-    }
-    return pp;
-  }
-};
-
-struct Chunk {
-  int phase, u, T, kb0, kc;
-  int t0;  // first slot of the tile within its (wave, phase)
-  bool last_of_seg;
-  PhasePlan pp;
-};
-
-// Walks this CTA's slots stage by stage in chunks of at most kcmax K blocks
-// that never cross a tile.
-struct Cursor {
-  int q = -1, pos = 0, phase = 1;
-  PhasePlan pp;
-  template <bool MX>
-  __device__ bool next(const Plan& P, Chunk& ch) {
-    while (true) {
-      if (q >= 0 && pos < pp.hi) {
-        const int tile = pos / pp.nb;
-        const int t0 = tile * pp.nb;
-        const int seg1 = min(pp.hi, t0 + pp.nb);
-        const int uw = tile / pp.tiles;
-        ch.phase = phase;
-        ch.u = pp.u0 + uw;
-        ch.T = tile - uw * pp.tiles;
-        ch.t0 = t0;
-        ch.kb0 = pos - t0;
-        ch.kc = min(MX && phase == 1 ? P.kcmax1 : P.kcmax, seg1 - pos);
-        ch.last_of_seg = pos + ch.kc == seg1;
-        ch.pp = pp;
-        pos += ch.kc;
-        return true;
-      }
-      if (++q >= 2 * P.W) return false;
-      int w;
-      P.stage(q, w, phase);
-      pp = P.plan(w, phase);
-      pos = pp.lo;
-    }
-  }
-};
 
 // ---------------------------------------------------------------- B operand fill
 // Routes of expert u (token order) into the fill warps' staging slot ctx_route[2].
@@ -684,6 +574,13 @@ __device__ void end_segment(const TcArgs& a, TcSmem& S, const Plan& P, const Chu
 // the CTA in afterwards, off the path to the first GEMM2 MMA.)
 __device__ bool wait_hidden(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& ch, int fid) {
   const int u = ch.u;
+  if (a.phase_lo == 2) {
+    // The chain's second kernel: the first kernel (every GEMM1 tile) has
+    // completed and its writes are visible once this returns.
+    griddep_wait();
+    fill_bar();
+    return true;
+  }
   if (fid == 0) {
     const int e = xinfo(a, S, u).id;
     const uint32_t target = static_cast<uint32_t>(P.tiles[0]);
@@ -834,7 +731,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
     tmem_relinquish();
   }
   for (int e = tid; e < a.E; e += kTcThreads) S.tokmask[e] = 0ull;
-  griddep_wait();
+  // The chain's second kernel reads only the inputs the first one read after
+  // its own wait (logits, bias, weights) until its fill waits for the hidden
+  // rows; every other launch waits for its predecessor here.
+  if (a.phase_lo == 1) griddep_wait();
+  if (a.phase_hi == 1) griddep_launch_dependents();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -844,13 +745,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
     for (int t = warp; t < a.M; t += kTcThreads / 32) {
       // Lane l holds experts l + 32 j, j < J: loops sized to the expert count.
       if (a.E <= 64)
-        route_token<2>(a, S, t, lane, blockIdx.x == 0);
+        route_token<2>(a, S, t, lane, blockIdx.x == 0 && a.phase_lo == 1);
       else if (a.E <= 256)
-        route_token<8>(a, S, t, lane, blockIdx.x == 0);
+        route_token<8>(a, S, t, lane, blockIdx.x == 0 && a.phase_lo == 1);
       else if (a.E <= 512)
-        route_token<16>(a, S, t, lane, blockIdx.x == 0);
+        route_token<16>(a, S, t, lane, blockIdx.x == 0 && a.phase_lo == 1);
       else
-        route_token<kMaxExperts / 32>(a, S, t, lane, blockIdx.x == 0);
+        route_token<kMaxExperts / 32>(a, S, t, lane, blockIdx.x == 0 && a.phase_lo == 1);
     }
     __syncthreads();
     if (warp == 0) {
@@ -883,7 +784,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
   P.kcmax1 = MX ? min(kMaxKc, kTmemBuf / P.N1) : 0;
   P.c = blockIdx.x;
   P.G = gridDim.x;
-  P.W = min(P.U, a.has_shared ? layer_waves(a.ptok) : max_waves(a.ptok));
+  P.W = a.phase_lo == a.phase_hi ? 1 : min(P.U, a.has_shared ? layer_waves(a.ptok) : max_waves(a.ptok));
+  P.phase_lo = a.phase_lo;
+  P.phase_hi = a.phase_hi;
   P.tiles[0] = a.I / 64;
   P.nb[0] = a.H / 128;
   P.tiles[1] = a.H / 128;
@@ -1197,6 +1100,13 @@ static int launch_tc(TcArgs& a, const uint8_t* w13, const uint8_t* w2, const uin
 static int layer_launch(const RoutedFp8& r, const SharedFp8& sh, int M, int H, int I, void* workspace,
                         size_t workspace_bytes, cudaStream_t st, int lay_routes, int lay_slots);
 
+// Routed calls as a two-kernel chain instead of one persistent launch
+// (FME_FP8_CHAIN=1): kept to compare the two schedules, off by default.
+static bool fp8_chain_enabled() {
+  const char* env = std::getenv("FME_FP8_CHAIN");
+  return env != nullptr && env[0] == '1';
+}
+
 int layer_fp8(const RoutedFp8& r, const SharedFp8& sh, int M, int H, int I, void* workspace, size_t workspace_bytes,
               cudaStream_t st) {
   // The MXFP8-input kernel reads its tokens from xq only: no shared expert beside it.
@@ -1221,6 +1131,8 @@ static int layer_launch(const RoutedFp8& r, const SharedFp8& sh, int M, int H, i
                         size_t workspace_bytes, cudaStream_t st, int lay_routes, int lay_slots) {
   TcArgs a;
   memset(&a, 0, sizeof(a));
+  a.phase_lo = 1;
+  a.phase_hi = 2;
   a.M = M;
   a.H = H;
   a.I = I;
@@ -1252,6 +1164,15 @@ static int layer_launch(const RoutedFp8& r, const SharedFp8& sh, int M, int H, i
     a.gate_up = static_cast<__nv_bfloat16*>(sh.gate_up);
     a.slimit = sh.limit;
     a.sue8m0 = sh.ue8m0 ? 1 : 0;
+  }
+  if (r.E > 0 && sh.w13 == nullptr && r.xq == nullptr && fp8_chain_enabled()) {
+    // The two-kernel chain: GEMM1 .. SwiGLU, then the re-quant and GEMM2 as a
+    // programmatic dependent launch (the same workspace layout; the second
+    // kernel re-arms the hidden counters the first one raised).
+    a.phase_hi = 1;
+    const int err = launch_tc(a, r.w13, r.w2, sh.w13, sh.w2, workspace, workspace_bytes, st, lay_routes, lay_slots);
+    if (err != FME_OK) return err;
+    a.phase_lo = a.phase_hi = 2;
   }
   return launch_tc(a, r.w13, r.w2, sh.w13, sh.w2, workspace, workspace_bytes, st, lay_routes, lay_slots);
 }

@@ -1,0 +1,106 @@
+// Host check of the routed FP8 kernel's work decomposition (fme_plan.cuh):
+// for many (units, tiles, K blocks, CTAs, waves, phase ranges, chunk sizes)
+// every CTA walks its chunks with the kernel's own Cursor, and the walk must
+// cover every (phase, unit, tile, K block) slot of the launched phases exactly
+// once, in chunks of 1..kcmax K blocks inside one tile, each slot on the CTA
+// cta_of names, a split tile's first K blocks at the end of its first
+// contributor's slice, and no slot of a phase the launch does not run.
+// Prints "OK <cases>" or the first failure; exit status 0 only on success.
+#include <cstdio>
+#include <vector>
+
+#include "fme_plan.cuh"
+
+using fme::Chunk;
+using fme::Cursor;
+using fme::Plan;
+
+static int fail(const char* what, int U, int G, int W, int lo, int hi, int c) {
+  std::printf("FAIL %s: U=%d G=%d W=%d phases %d..%d cta %d\n", what, U, G, W, lo, hi, c);
+  return 1;
+}
+
+template <bool MX>
+static int check(int U, int tiles1, int nb1, int tiles2, int nb2, int G, int W, int lo, int hi, int kcmax, int kcmax1) {
+  // seen[phase][unit][tile][kb]
+  std::vector<int> seen[2];
+  seen[0].assign(static_cast<size_t>(U) * tiles1 * nb1, 0);
+  seen[1].assign(static_cast<size_t>(U) * tiles2 * nb2, 0);
+  for (int c = 0; c < G; ++c) {
+    Plan P{};
+    P.U = U;
+    P.N = 16;
+    P.kcmax = kcmax;
+    P.N1 = 16;
+    P.kcmax1 = kcmax1;
+    P.c = c;
+    P.G = G;
+    P.W = W;
+    P.phase_lo = lo;
+    P.phase_hi = hi;
+    P.tiles[0] = tiles1;
+    P.nb[0] = nb1;
+    P.tiles[1] = tiles2;
+    P.nb[1] = nb2;
+    Cursor cur;
+    Chunk ch;
+    int guard = 0;
+    int last_phase = 0;
+    while (cur.next<MX>(P, ch)) {
+      if (++guard > 1 << 22) return fail("walk does not end", U, G, W, lo, hi, c);
+      if (ch.phase < lo || ch.phase > hi) return fail("phase outside the launch", U, G, W, lo, hi, c);
+      const int p = ch.phase - 1;
+      const int tl = p == 0 ? tiles1 : tiles2, nb = p == 0 ? nb1 : nb2;
+      const int cap = (MX && ch.phase == 1) ? kcmax1 : kcmax;
+      if (ch.u < 0 || ch.u >= U || ch.T < 0 || ch.T >= tl) return fail("unit or tile out of range", U, G, W, lo, hi, c);
+      if (ch.kc < 1 || ch.kc > cap || ch.kb0 < 0 || ch.kb0 + ch.kc > nb)
+        return fail("chunk size or K range", U, G, W, lo, hi, c);
+      const int tile_in_wave = (ch.u - ch.pp.u0) * tl + ch.T;
+      if (ch.t0 != tile_in_wave * nb) return fail("tile start slot", U, G, W, lo, hi, c);
+      for (int j = 0; j < ch.kc; ++j) {
+        const int slot = ch.t0 + ch.kb0 + j;
+        if (ch.pp.cta_of(slot) != c) return fail("cta_of disagrees with the walk", U, G, W, lo, hi, c);
+        int& s = seen[p][(static_cast<size_t>(ch.u) * tl + ch.T) * nb + ch.kb0 + j];
+        if (s++) return fail("slot walked twice", U, G, W, lo, hi, c);
+      }
+      // a split tile: its first contributor holds its first K blocks at the end of its slice
+      const int cf = ch.pp.cta_of(ch.t0), cl = ch.pp.cta_of(ch.t0 + nb - 1);
+      if (cf != cl && c == cf && ch.last_of_seg && ch.t0 + ch.kb0 + ch.kc != ch.pp.hi)
+        return fail("first contributor's part not at its slice end", U, G, W, lo, hi, c);
+      if (W == 1 && ch.phase < last_phase) return fail("phases out of order", U, G, W, lo, hi, c);
+      last_phase = ch.phase;
+    }
+  }
+  for (int p = 0; p < 2; ++p) {
+    const bool run = p + 1 >= lo && p + 1 <= hi;
+    for (int v : seen[p])
+      if (v != (run ? 1 : 0)) return fail(run ? "slot never walked" : "slot of a skipped phase walked", U, G, W, lo, hi, -1);
+  }
+  return 0;
+}
+
+int main() {
+  struct Shape { int tiles1, nb1, tiles2, nb2; };
+  const Shape shapes[] = {{32, 56, 56, 16},   // DeepSeek-V3: I 2048, H 7168
+                          {32, 28, 28, 16},   // latent: H 3584
+                          {4, 4, 4, 2},       // tiny: H 512, I 256
+                          {6, 8, 8, 3},       // ragged: H 1024, I 384
+                          {2, 1, 1, 1}};      // H = I = 128
+  const int units[] = {1, 2, 3, 8, 16, 31, 53, 257};
+  const int ctas[] = {1, 3, 148, 152, 160};
+  const int ranges[][2] = {{1, 2}, {1, 1}, {2, 2}};
+  int cases = 0;
+  for (const Shape& s : shapes)
+    for (int U : units)
+      for (int G : ctas)
+        for (int W = 1; W <= 3; ++W)
+          for (const auto& r : ranges)
+            for (int kc : {16, 8, 4, 1}) {
+              if (W > U || (r[0] == r[1] && W != 1)) continue;
+              if (check<false>(U, s.tiles1, s.nb1, s.tiles2, s.nb2, G, W, r[0], r[1], kc, kc)) return 1;
+              if (check<true>(U, s.tiles1, s.nb1, s.tiles2, s.nb2, G, W, r[0], r[1], kc, kc > 4 ? kc / 4 : 1)) return 1;
+              cases += 2;
+            }
+  std::printf("OK %d\n", cases);
+  return 0;
+}
