@@ -121,11 +121,11 @@ extern "C" int fme_moe_routed_fp8_noalloc(const void* x, const void* logits, int
   void* scratch = scratch_address(dev);
   if (scratch == nullptr) return FME_ECUDA;
   // The array keeps whatever the previous call left. The counters must start
-  // at zero (the rest is written before it is read); the error word (first
-  // 256-byte unit) is left alone, so a device-side error stays visible to
+  // at zero (the rest is written before it is read); the error word (its
+  // first 4 bytes) is left alone, so a device-side error stays visible to
   // fme_moe_routed_fp8_noalloc_error until read there, across later calls.
   const size_t zero = fme::layer_fp8_zero_bytes(M, H, I, E, top_k, false);
-  const cudaError_t err = cudaMemsetAsync(static_cast<uint8_t*>(scratch) + 256, 0, zero - 256,
+  const cudaError_t err = cudaMemsetAsync(static_cast<uint8_t*>(scratch) + 4, 0, zero - 4,
                                           static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return fme::set_last_error(FME_ECUDA, "cudaMemsetAsync: %s", cudaGetErrorString(err));
   return fme_moe_routed_fp8(x, logits, logits_dtype, bias, w13, s13, w2, s2, M, H, I, E, top_k, limit, scale,

@@ -55,6 +55,8 @@ struct PhasePlan {
 
 struct Plan {
   int U, N, kcmax, c, G, W;
+  bool ximage;  // GEMM1 B rows copied from a per-call quantised image of x
+  int kcmax2;  // K blocks per GEMM2 chunk, at most
   int phase_lo, phase_hi;  // phases this launch runs
   int N1, kcmax1;  // the MX kernel's GEMM1 B rows (four per token) and K blocks per chunk
   int tiles[2], nb[2];  // per unit: GEMM1 64-row tiles x H/128 K blocks; GEMM2 128-row tiles x I/128
@@ -118,7 +120,7 @@ struct Cursor {
         ch.T = tile - uw * pp.tiles;
         ch.t0 = t0;
         ch.kb0 = pos - t0;
-        ch.kc = plan_min(MX && phase == 1 ? P.kcmax1 : P.kcmax, seg1 - pos);
+        ch.kc = plan_min(phase == 2 ? P.kcmax2 : (MX ? P.kcmax1 : P.kcmax), seg1 - pos);
         ch.last_of_seg = pos + ch.kc == seg1;
         ch.pp = pp;
         pos += ch.kc;

@@ -39,6 +39,9 @@
 namespace fme {
 
 constexpr int kTcThreads = 256;  // TMA, MMA, 4 accumulate, 2 fill warps
+// Above this many routes on one expert the GEMM1 fills copy from a per-call
+// image of x instead of quantising per chunk.
+constexpr int kXImageRoutes = 4;
 constexpr int kFillThreads = 64;
 constexpr int kTcStages = 8;
 constexpr int kAStageBytes = 128 * 128;  // one 128-row x 128-byte K block of weights
@@ -71,6 +74,9 @@ struct TcArgs {
   uint32_t* cnt1;    // [(E + 1) * I/64] contributors arrived per GEMM1 tile (expert id, tile)
   uint32_t* cnt2;    // [(E + 1) * H/128] per GEMM2 tile
   float* hbuf;       // [M * top_k + M, I] SwiGLU output (routed routes, then shared tokens)
+  uint8_t* ximg;     // [M, H] x quantised per 128 (E4M3), built once per call when experts take many tokens
+  float* ximg_sc;    // [M, H/128] its scales
+  uint32_t* xsync;   // [2]: CTAs whose share of the image is written; CTAs past the wait for it
   float* part;       // [2 phases][kFp8MaxCtas][2 slots][tokens][128 rows] split-tile partials
   int M, H, I, E, top_k;  // E routed experts (0: shared expert only)
   int ptok;          // token rows of one partial slot (min(M, 64))
@@ -98,6 +104,7 @@ struct TcSmem {
   int16_t rid[kMaxTokens * kMaxTopK];
   int16_t ulist[kMaxExperts];
   int16_t ctx_route[3][kMaxTokens];  // routes of each B buffer's expert, in token order; [2]: the fill's next
+  int btag[2];                       // what each B buffer holds: a GEMM2 (unit, K range), or -1
   int ctx_n[3];
   int16_t seg_route[kMaxTokens];     // the accumulate warps' copy for the current segment
   int seg_n;
@@ -174,6 +181,137 @@ __device__ void route_token(const TcArgs& a, TcSmem& S, int t, int lane, bool wr
     if (write_out) {
       a.ids[route] = e;
       a.weights[route] = w;
+    }
+  }
+}
+
+// Up to 4 tokens and 256 experts: the 8 warps split each token's experts
+// (wpt = 8, 4 or 2 warps per token, expert blocks of 32 dealt round-robin),
+// each warp picks its top_k by the rule of route_topk (largest key, lowest
+// expert among equals) into shared memory, then warp t merges token t's
+// candidates by the same rule and forms the weights exactly as route_topk
+// (float sum of the picked scores in pick order, divide, times scale). The
+// picks and weights are those of route_topk bit for bit; the rounds of
+// warp reductions are shorter (one or two keys per lane instead of eight).
+struct RouteCand {
+  uint32_t key;
+  int e;
+  float score;
+};
+
+__device__ void route_split(const TcArgs& a, TcSmem& S, int warp, int lane, bool write_out) {
+  const int wpt = a.M == 1 ? 8 : (a.M == 2 ? 4 : 2);
+  const int t = warp / wpt, sl = warp % wpt;
+  const int k = a.top_k;
+  // candidates [token][slice][k] in the idle B buffer (no fill has started yet)
+  RouteCand* cand = reinterpret_cast<RouteCand*>(S.B[0]);
+  if (t < a.M) {
+    constexpr int J = 4;  // expert blocks per slice: 8 blocks (E <= 256) over 2+ warps
+    float sc[J], bs[J];
+    uint32_t ky[J];
+    int ex[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {  // every load issued before any sigmoid
+      ex[j] = lane + 32 * (sl + wpt * j);
+      sc[j] = 0.0f;
+      bs[j] = 0.0f;
+      if (ex[j] < a.E) {
+        sc[j] = a.logits_f32
+                    ? __ldg(static_cast<const float*>(a.logits) + static_cast<size_t>(t) * a.E + ex[j])
+                    : __bfloat162float(static_cast<const __nv_bfloat16*>(a.logits)[static_cast<size_t>(t) * a.E + ex[j]]);
+        bs[j] = __ldg(a.bias + ex[j]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const float sgm = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-sc[j])));
+      sc[j] = sgm;
+      ky[j] = ex[j] < a.E ? ordered_key(__fadd_rn(sgm, bs[j])) : 0u;
+    }
+    RouteCand* mine = cand + (t * 8 + sl) * k;
+    for (int r = 0; r < k; ++r) {
+      uint32_t best = 0u;
+#pragma unroll
+      for (int j = 0; j < J; ++j) best = max(best, ky[j]);
+      const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, best);
+      uint32_t c = 0xFFFFFFFFu;
+#pragma unroll
+      for (int j = J - 1; j >= 0; --j)
+        if (ky[j] == top && top != 0u) c = static_cast<uint32_t>(ex[j]);
+      const uint32_t win = __reduce_min_sync(0xFFFFFFFFu, c);
+      float sv = 0.0f;
+#pragma unroll
+      for (int j = 0; j < J; ++j)
+        if (static_cast<uint32_t>(ex[j]) == win) {
+          sv = sc[j];
+          ky[j] = 0u;
+        }
+      // the winner's lane holds its score; an exhausted slice offers key 0
+      const float s = __shfl_sync(0xFFFFFFFFu, sv, win == 0xFFFFFFFFu ? 0 : static_cast<int>(win & 31u));
+      if (lane == 0) mine[r] = RouteCand{top, win == 0xFFFFFFFFu ? 0x7FFFFFFF : static_cast<int>(win), s};
+    }
+  }
+  __syncthreads();
+  if (warp < a.M) {
+    const int tt = warp;
+    const RouteCand* cs = cand + tt * 8 * k;
+    const int n = wpt * k;  // <= 8 x 8 (E <= 256 caps k at what 8 blocks hold per slice)
+    constexpr int JM = 8;
+    uint32_t ky[JM];
+    int ex[JM];
+    float sc[JM];
+#pragma unroll
+    for (int j = 0; j < JM; ++j) {
+      const int i = lane + 32 * j;
+      const int sl = i / k, r = i - sl * k;
+      ky[j] = 0u;
+      ex[j] = 0x7FFFFFFF;
+      sc[j] = 0.0f;
+      if (i < n) {
+        const RouteCand c = cs[sl * k + r];
+        ky[j] = c.key;
+        ex[j] = c.e;
+        sc[j] = c.score;
+      }
+    }
+    float total = 0.0f, mine_s = 0.0f;
+    int mine_e = 0;
+    for (int r = 0; r < k; ++r) {
+      uint32_t best = 0u;
+#pragma unroll
+      for (int j = 0; j < JM; ++j) best = max(best, ky[j]);
+      const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, best);
+      uint32_t c = 0xFFFFFFFFu;
+#pragma unroll
+      for (int j = 0; j < JM; ++j)
+        if (ky[j] == top && static_cast<uint32_t>(ex[j]) < c) c = static_cast<uint32_t>(ex[j]);
+      const uint32_t win = __reduce_min_sync(0xFFFFFFFFu, c);
+      float sv = 0.0f;
+      int holder = 0;
+#pragma unroll
+      for (int j = 0; j < JM; ++j)
+        if (ky[j] == top && static_cast<uint32_t>(ex[j]) == win) {
+          sv = sc[j];
+          ky[j] = 0u;
+          holder = 1;
+        }
+      const int src = __ffs(__ballot_sync(0xFFFFFFFFu, holder)) - 1;
+      const float s = __shfl_sync(0xFFFFFFFFu, sv, src < 0 ? 0 : src);
+      total = __fadd_rn(total, s);
+      if (lane == r) {
+        mine_s = s;
+        mine_e = static_cast<int>(win);
+      }
+    }
+    if (lane < k) {
+      const float w = __fmul_rn(__fdiv_rn(mine_s, total), a.scale);
+      const int route = tt * k + lane;
+      S.rid[route] = static_cast<int16_t>(mine_e);
+      atomicOr(&S.tokmask[mine_e], 1ull << tt);
+      if (write_out) {
+        a.ids[route] = mine_e;
+        a.weights[route] = w;
+      }
     }
   }
 }
@@ -258,6 +396,57 @@ __device__ bool fill_b_mx(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk
     }
   }
   if (fid < 2 * kMaxKc) S.wsc[b][fid / kMaxKc][fid % kMaxKc] = wsv;
+  if (fid == 0) S.btag[b] = -1;
+  fence_proxy_async_smem();
+  fill_bar();
+  if (fid == 0) mbar_arrive(&S.bfull[b]);
+  return true;
+}
+
+// GEMM1 chunk from the per-call x image: each (route, K block) row is eight
+// 16-byte copies into the swizzled B layout (cp.async, no registers), its
+// scale one load; the weight scales as in fill_b.
+__device__ bool fill_b_copy(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& ch, int b, int ci, int fid) {
+  const int r = S.ctx_n[2];
+  const int N = P.N;
+  uint8_t* B = S.B[b];
+  const XInfo xi = xinfo(a, S, ch.u);
+  const int nbx = a.H / 128;
+  float wsv = 0.0f;
+  if (fid < 2 * kMaxKc) {
+    const int half = fid / kMaxKc, j = fid % kMaxKc;
+    if (j < ch.kc) {
+      const int rb = (half == 0 ? 0 : a.I / 128) + ch.T / 2;
+      wsv = __ldg(xi.s13 + (static_cast<size_t>(xi.row_e) * (2 * a.I / 128) + rb) * (a.H / 128) + ch.kb0 + j);
+    }
+  }
+  if (ci >= 2) {
+    if (!mbar_wait(&S.mfree[b], ((ci >> 1) - 1) & 1, a.timeout_ns, &S.abort)) {
+      if (!S.abort) tc_error(a, S, kErrRingWait);
+    }
+    fill_bar();
+    if (S.abort) return false;
+  }
+  for (int t = fid; t < r; t += kFillThreads) S.ctx_route[b][t] = S.ctx_route[2][t];
+  if (fid == 0) S.ctx_n[b] = r;
+  const int items = ch.kc * r * 8;
+  for (int w = fid; w < items; w += kFillThreads) {
+    const int p = w >> 3, sub = w & 7;
+    const int t = p % r, j = p / r;
+    const int route = S.ctx_route[2][t];
+    const int tok = xi.shared ? route - a.M * a.top_k : route / a.top_k;
+    cp_async_16(B + j * N * 128 + t * 128 + ((sub ^ (t & 7)) << 4),
+                a.ximg + static_cast<size_t>(tok) * a.H + (ch.kb0 + j) * 128 + sub * 16);
+  }
+  for (int w = fid; w < ch.kc * r; w += kFillThreads) {
+    const int t = w % r, j = w / r;
+    const int route = S.ctx_route[2][t];
+    const int tok = xi.shared ? route - a.M * a.top_k : route / a.top_k;
+    S.xs[b][t][j] = __ldcg(a.ximg_sc + static_cast<size_t>(tok) * nbx + ch.kb0 + j);
+  }
+  if (fid < 2 * kMaxKc) S.wsc[b][fid / kMaxKc][fid % kMaxKc] = wsv;
+  if (fid == 0) S.btag[b] = -1;
+  cp_async_wait_all();
   fence_proxy_async_smem();
   fill_bar();
   if (fid == 0) mbar_arrive(&S.bfull[b]);
@@ -280,6 +469,7 @@ __device__ bool fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
   if constexpr (MX) {
     if (ch.phase == 1) return fill_b_mx(a, S, P, ch, b, ci, fid);
   }
+  if (ch.phase == 1 && P.ximage) return fill_b_copy(a, S, P, ch, b, ci, fid);
   const int r = S.ctx_n[2];
   const int N = P.N;
   uint8_t* B = S.B[b];
@@ -299,9 +489,14 @@ __device__ bool fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
       }
     }
   }
-  const int items = ch.kc * r * 8;
+  // A GEMM2 chunk over the same unit and K range as the one buffer b holds
+  // (the next 128 rows of W2, usually) takes the same quantised hidden rows:
+  // only its weight scales are new.
+  const int tag = ch.phase == 2 ? (ch.u * 64 + ch.kb0) * 32 + ch.kc : -1;
+  const bool reuse = tag >= 0 && S.btag[b] == tag;
+  const int items = reuse ? 0 : ch.kc * r * 8;
   const int K = ch.phase == 1 ? a.H : a.I;
-  constexpr int IPT = 2;  // items per thread per round: all loads first, then quantise
+  constexpr int IPT = 4;  // items per thread per round: all loads first, then quantise
   float v[IPT][16], vn[IPT][16];
   int tt[IPT], jj[IPT], ttn[IPT], jjn[IPT];
   auto load_batch = [&](float (&v)[IPT][16], int (&tt)[IPT], int (&jj)[IPT], int base) {
@@ -386,8 +581,11 @@ __device__ bool fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
     if (S.abort) return false;
   }
   // Buffer b is free: publish the chunk's routes, then quantise.
-  for (int t = fid; t < r; t += kFillThreads) S.ctx_route[b][t] = S.ctx_route[2][t];
-  if (fid == 0) S.ctx_n[b] = r;
+  if (!reuse) {
+    for (int t = fid; t < r; t += kFillThreads) S.ctx_route[b][t] = S.ctx_route[2][t];
+    if (fid == 0) S.ctx_n[b] = r;
+  }
+  if (fid == 0) S.btag[b] = tag;
   // Rounds of IPT items per thread; the next round's loads are in flight
   // while this round is quantised.
   for (int base = 0; base < items; base += kFillThreads * IPT) {
@@ -615,6 +813,33 @@ __device__ void pass_hidden(const TcArgs& a, TcSmem& S, const Chunk& ch) {
   }
 }
 
+// Wait until every CTA has written its share of the x image; the last CTA
+// past the wait re-arms both counters for the next call.
+__device__ bool wait_ximage(const TcArgs& a, TcSmem& S, int fid) {
+  if (fid == 0) {
+    const uint32_t target = gridDim.x;
+    const uint64_t t0 = globaltimer_ns();
+    bool ok = true;
+    while (ld_acquire_gpu(a.xsync) < target) {
+      if (S.abort || globaltimer_ns() - t0 > a.timeout_ns) {
+        ok = false;
+        break;
+      }
+      __nanosleep(64);
+    }
+    if (ok) {
+      if (atomicAdd(a.xsync + 1, 1u) + 1u == target) {
+        atomicExch(a.xsync, 0u);
+        atomicExch(a.xsync + 1, 0u);
+      }
+    } else if (!S.abort) {
+      tc_error(a, S, kErrCrossWait);
+    }
+  }
+  fill_bar();
+  return !S.abort;
+}
+
 // Scaled sum of one chunk's per-K-block partials: y[t] += D[j][t] *
 // (w_scale[j] * x_scale[t][j]) for this thread's row. Loads LD columns per
 // tcgen05.ld, GROUPS groups of them per K block, KB K blocks per wait.
@@ -717,6 +942,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
     mbar_init(&S.final_bar, 1);
     fence_mbar_init();
     S.abort = 0;
+    S.btag[0] = S.btag[1] = -1;
     if (a.E > 0) {
       prefetch_tmap(&a.map13);
       prefetch_tmap(&a.map2);
@@ -742,6 +968,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
 
   // ---- routing and the unique-expert list (routed experts first, then the shared one)
   if (a.E > 0) {
+    if (a.M <= 4 && a.E <= 256 && a.E > 32) {
+      route_split(a, S, warp, lane, blockIdx.x == 0 && a.phase_lo == 1);
+    } else
     for (int t = warp; t < a.M; t += kTcThreads / 32) {
       // Lane l holds experts l + 32 j, j < J: loops sized to the expert count.
       if (a.E <= 64)
@@ -776,10 +1005,43 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
   }
   __syncthreads();
 
+  // Many tokens on one expert: quantise x once per call into the image (every
+  // CTA a share of the (token, K block) groups, one warp per group, the same
+  // arithmetic as fill_b), so the GEMM1 fills only copy rows. With few routes
+  // per expert the per-chunk quantisation is cheaper than the grid-wide wait.
+  const bool ximage = !MX && a.E > 0 && S.rmax > kXImageRoutes && (!a.has_shared || a.sue8m0 == a.ue8m0);
+  if (ximage) {
+    const int nbx = a.H / 128;
+    const int groups = a.M * nbx;
+    for (int g = blockIdx.x * (kTcThreads / 32) + warp; g < groups; g += gridDim.x * (kTcThreads / 32)) {
+      const int t = g / nbx, kb = g - t * nbx;
+      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(a.x + static_cast<size_t>(t) * a.H + kb * 128 + lane * 4));
+      const float v0 = __uint_as_float(raw.x << 16), v1 = __uint_as_float(raw.x & 0xFFFF0000u);
+      const float v2 = __uint_as_float(raw.y << 16), v3 = __uint_as_float(raw.y & 0xFFFF0000u);
+      float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+      float scale = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+      if (a.ue8m0) scale = ue8m0_ceil(scale);
+      const float inv = __fdiv_rn(1.0f, scale);
+      const uint32_t q = f32x2_to_e4m3x2(__fmul_rn(v0, inv), __fmul_rn(v1, inv)) |
+                         (f32x2_to_e4m3x2(__fmul_rn(v2, inv), __fmul_rn(v3, inv)) << 16);
+      *reinterpret_cast<uint32_t*>(a.ximg + static_cast<size_t>(t) * a.H + kb * 128 + lane * 4) = q;
+      if (lane == 0) a.ximg_sc[g] = scale;
+    }
+    __syncthreads();  // every share written before the one release
+    if (tid == 0) {
+      __threadfence();
+      red_release_gpu_add(a.xsync, 1u);
+    }
+  }
+
   Plan P;
   P.U = S.U;
+  P.ximage = ximage;
   P.N = 16 * ((S.rmax + 15) / 16);
   P.kcmax = min(kMaxKc, kTmemBuf / P.N);
+  P.kcmax2 = P.kcmax;
   P.N1 = MX ? 16 * ((4 * S.rmax + 15) / 16) : P.N;
   P.kcmax1 = MX ? min(kMaxKc, kTmemBuf / P.N1) : 0;
   P.c = blockIdx.x;
@@ -966,7 +1228,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
     Cursor cur;
     Chunk ch;
     int ci = 0, ctx_u = -1, ctx_phase = 0;
-    while (cur.next<MX>(P, ch)) {
+    bool ok = true;
+    if (ximage) ok = wait_ximage(a, S, fid);
+    while (ok && cur.next<MX>(P, ch)) {
       const int b = ci & 1;
       if (ch.u != ctx_u) fill_context(a, S, ch.u, fid);
       const bool first2 = ch.phase == 2 && (ch.u != ctx_u || ctx_phase != 2);
@@ -1015,8 +1279,9 @@ static bool make_map(CUtensorMap* map, const void* base, unsigned long long rows
 }
 
 struct TcWorkspace {
-  uint32_t *err, *done, *passed, *cnt1, *cnt2;
-  float *hbuf, *part;
+  uint32_t *err, *done, *passed, *cnt1, *cnt2, *xsync;
+  float *hbuf, *part, *xsc;
+  uint8_t* ximg;
   int ptok;
   size_t zero_bytes;  // error word and counters: must be zero when a call starts
   size_t bytes;
@@ -1029,6 +1294,7 @@ static TcWorkspace tc_layout(void* base, int M, int routes, int H, int I, int E)
   uint8_t* p = static_cast<uint8_t*>(base);
   size_t off = 0;
   w.err = reinterpret_cast<uint32_t*>(p + off);
+  w.xsync = reinterpret_cast<uint32_t*>(p + off + 64);  // two words in the error word's 256-byte unit
   off += 256;
   w.done = reinterpret_cast<uint32_t*>(p + off);
   off += align256(4 * static_cast<size_t>(E));
@@ -1046,6 +1312,10 @@ static TcWorkspace tc_layout(void* base, int M, int routes, int H, int I, int E)
   w.ptok = M < kMaxTokens ? M : kMaxTokens;
   w.part = reinterpret_cast<float*>(p + off);
   off += align256(4 * static_cast<size_t>(waves_cap(w.ptok)) * 2 * kFp8MaxCtas * 2 * w.ptok * 128);
+  w.ximg = p + off;
+  off += align256(static_cast<size_t>(M) * H);
+  w.xsc = reinterpret_cast<float*>(p + off);
+  off += align256(4 * static_cast<size_t>(M) * (H / 128));
   w.bytes = off;
   return w;
 }
@@ -1066,6 +1336,9 @@ static int launch_tc(TcArgs& a, const uint8_t* w13, const uint8_t* w2, const uin
   a.cnt2 = w.cnt2;
   a.hbuf = w.hbuf;
   a.part = w.part;
+  a.ximg = w.ximg;
+  a.ximg_sc = w.xsc;
+  a.xsync = w.xsync;
   a.ptok = w.ptok;
   a.timeout_ns = wait_timeout_ns();
   if (a.E > 0 && (!make_map(&a.map13, w13, static_cast<unsigned long long>(a.E) * 2 * a.I, a.H) ||

@@ -21,7 +21,8 @@ static int fail(const char* what, int U, int G, int W, int lo, int hi, int c) {
 }
 
 template <bool MX>
-static int check(int U, int tiles1, int nb1, int tiles2, int nb2, int G, int W, int lo, int hi, int kcmax, int kcmax1) {
+static int check(int U, int tiles1, int nb1, int tiles2, int nb2, int G, int W, int lo, int hi, int kcmax, int kcmax1,
+                 int kcmax2) {
   // seen[phase][unit][tile][kb]
   std::vector<int> seen[2];
   seen[0].assign(static_cast<size_t>(U) * tiles1 * nb1, 0);
@@ -33,6 +34,7 @@ static int check(int U, int tiles1, int nb1, int tiles2, int nb2, int G, int W, 
     P.kcmax = kcmax;
     P.N1 = 16;
     P.kcmax1 = kcmax1;
+    P.kcmax2 = kcmax2;
     P.c = c;
     P.G = G;
     P.W = W;
@@ -51,7 +53,7 @@ static int check(int U, int tiles1, int nb1, int tiles2, int nb2, int G, int W, 
       if (ch.phase < lo || ch.phase > hi) return fail("phase outside the launch", U, G, W, lo, hi, c);
       const int p = ch.phase - 1;
       const int tl = p == 0 ? tiles1 : tiles2, nb = p == 0 ? nb1 : nb2;
-      const int cap = (MX && ch.phase == 1) ? kcmax1 : kcmax;
+      const int cap = ch.phase == 2 ? kcmax2 : (MX ? kcmax1 : kcmax);
       if (ch.u < 0 || ch.u >= U || ch.T < 0 || ch.T >= tl) return fail("unit or tile out of range", U, G, W, lo, hi, c);
       if (ch.kc < 1 || ch.kc > cap || ch.kb0 < 0 || ch.kb0 + ch.kc > nb)
         return fail("chunk size or K range", U, G, W, lo, hi, c);
@@ -97,8 +99,10 @@ int main() {
           for (const auto& r : ranges)
             for (int kc : {16, 8, 4, 1}) {
               if (W > U || (r[0] == r[1] && W != 1)) continue;
-              if (check<false>(U, s.tiles1, s.nb1, s.tiles2, s.nb2, G, W, r[0], r[1], kc, kc)) return 1;
-              if (check<true>(U, s.tiles1, s.nb1, s.tiles2, s.nb2, G, W, r[0], r[1], kc, kc > 4 ? kc / 4 : 1)) return 1;
+              const int kc2 = kc < 8 ? kc : 8;
+              if (check<false>(U, s.tiles1, s.nb1, s.tiles2, s.nb2, G, W, r[0], r[1], kc, kc, kc2)) return 1;
+              if (check<true>(U, s.tiles1, s.nb1, s.tiles2, s.nb2, G, W, r[0], r[1], kc, kc > 4 ? kc / 4 : 1, kc2))
+                return 1;
               cases += 2;
             }
   std::printf("OK %d\n", cases);

@@ -60,6 +60,34 @@ def test_routed_small_full_parity(fme, cfg_name, M, ue8m0):
     assert_outputs(got, ref)
 
 
+@pytest.mark.parametrize("M,E,k", [(1, 256, 8), (1, 40, 3), (1, 256, 1), (2, 96, 32), (3, 256, 8), (4, 200, 16),
+                                   (4, 33, 32)])
+def test_routing_small_m_with_key_ties(fme, M, E, k):
+    """Up to 4 tokens and 256 experts the kernel splits each token's experts
+    over several warps and merges their picks; ids must equal the oracle's bit
+    for bit, including exact key ties between experts of different 32-expert
+    blocks (equal logits and equal bias: the lower expert id goes first)."""
+    import dataclasses
+    cfg = dataclasses.replace(W.TINY, H=256, I=128, E=E, top_k=k, name=f"route_{E}_{k}")
+    w13h, w2h, s13, s2, x, logits, bias = _device_problem(cfg, M, seed=40 + E + k)
+    tied = [e for e in (3, 35, 67, 99, 131, 163) if e < E]
+    bias[tied] = bias[tied[0]]
+    for t in range(M):
+        logits[t, tied] = logits[t].max() + 0.5
+        if t % 2:
+            logits[t, tied[-1]] = logits[t].max() + 0.25  # a single winner ahead of the tie
+    w13 = torch.from_numpy(w13h.full()).to(DEV)
+    w2 = torch.from_numpy(w2h.full()).to(DEV)
+    xd, ld, bd = _to_dev(cfg, x, logits, bias)
+    out, ids, wts = fme.moe_routed_fp8(xd, ld, bd, w13, torch.from_numpy(s13).to(DEV), w2,
+                                       torch.from_numpy(s2).to(DEV), k, cfg.limit, cfg.scale, cfg.ue8m0)
+    torch.cuda.synchronize()
+    ref, rids, rw, keys = moe_fp8.routed_fp8(x, logits, bias, w13h, s13, w2h, s2, k, cfg.limit, cfg.scale, cfg.ue8m0)
+    assert np.array_equal(ids.cpu().numpy(), rids)  # no excuse: ties are exact, gaps elsewhere are wide
+    assert np.allclose(wts.cpu().numpy(), rw, rtol=1e-6, atol=0)
+    assert_outputs(out.float().cpu().numpy(), ref)
+
+
 def test_routed_top_k_equals_E_and_max_tokens(fme):
     import dataclasses
     cfg = dataclasses.replace(W.TINY, H=256, I=128, E=8, top_k=8, name="topk_all")
