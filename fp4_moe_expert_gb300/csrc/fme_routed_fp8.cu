@@ -77,6 +77,8 @@ struct TcArgs {
   uint8_t* ximg;     // [M, H] x quantised per 128 (E4M3), built once per call when experts take many tokens
   float* ximg_sc;    // [M, H/128] its scales
   uint32_t* xsync;   // [2]: CTAs whose share of the image is written; CTAs past the wait for it
+  int32_t* picks;    // [M, top_k] expert picks, when the CTAs share the routing
+  uint32_t* rsync;   // [2]: tokens routed; CTAs past the wait for them
   float* part;       // [2 phases][kFp8MaxCtas][2 slots][tokens][128 rows] split-tile partials
   int M, H, I, E, top_k;  // E routed experts (0: shared expert only)
   int ptok;          // token rows of one partial slot (min(M, 64))
@@ -199,14 +201,18 @@ struct RouteCand {
   float score;
 };
 
-__device__ void route_split(const TcArgs& a, TcSmem& S, int warp, int lane, bool write_out) {
-  const int wpt = a.M == 1 ? 8 : (a.M == 2 ? 4 : 2);
-  const int t = warp / wpt, sl = warp % wpt;
+// Tokens t0 .. t0 + ntok - 1 (ntok <= 8 / wpt), wpt warps each; E <= 128 wpt.
+// gpicks == nullptr: the picks go to S.rid / S.tokmask; else to gpicks[t][r]
+// in global memory (the routing shared between CTAs).
+__device__ void route_split(const TcArgs& a, TcSmem& S, int warp, int lane, bool write_out, int t0, int ntok, int wpt,
+                            int32_t* gpicks) {
+  const int tl = warp / wpt, sl = warp % wpt;
+  const int t = t0 + tl;
   const int k = a.top_k;
   // candidates [token][slice][k] in the idle B buffer (no fill has started yet)
   RouteCand* cand = reinterpret_cast<RouteCand*>(S.B[0]);
-  if (t < a.M) {
-    constexpr int J = 4;  // expert blocks per slice: 8 blocks (E <= 256) over 2+ warps
+  if (tl < ntok && t < a.M) {
+    constexpr int J = 4;  // expert blocks of 32 per slice: E <= 4 x 32 x wpt
     float sc[J], bs[J];
     uint32_t ky[J];
     int ex[J];
@@ -228,7 +234,7 @@ __device__ void route_split(const TcArgs& a, TcSmem& S, int warp, int lane, bool
       sc[j] = sgm;
       ky[j] = ex[j] < a.E ? ordered_key(__fadd_rn(sgm, bs[j])) : 0u;
     }
-    RouteCand* mine = cand + (t * 8 + sl) * k;
+    RouteCand* mine = cand + (tl * 8 + sl) * k;
     for (int r = 0; r < k; ++r) {
       uint32_t best = 0u;
 #pragma unroll
@@ -252,9 +258,9 @@ __device__ void route_split(const TcArgs& a, TcSmem& S, int warp, int lane, bool
     }
   }
   __syncthreads();
-  if (warp < a.M) {
-    const int tt = warp;
-    const RouteCand* cs = cand + tt * 8 * k;
+  if (warp < ntok && t0 + warp < a.M) {
+    const int tt = t0 + warp;
+    const RouteCand* cs = cand + warp * 8 * k;
     const int n = wpt * k;  // <= 8 x 8 (E <= 256 caps k at what 8 blocks hold per slice)
     constexpr int JM = 8;
     uint32_t ky[JM];
@@ -306,8 +312,12 @@ __device__ void route_split(const TcArgs& a, TcSmem& S, int warp, int lane, bool
     if (lane < k) {
       const float w = __fmul_rn(__fdiv_rn(mine_s, total), a.scale);
       const int route = tt * k + lane;
-      S.rid[route] = static_cast<int16_t>(mine_e);
-      atomicOr(&S.tokmask[mine_e], 1ull << tt);
+      if (gpicks != nullptr) {
+        gpicks[route] = mine_e;
+      } else {
+        S.rid[route] = static_cast<int16_t>(mine_e);
+        atomicOr(&S.tokmask[mine_e], 1ull << tt);
+      }
       if (write_out) {
         a.ids[route] = mine_e;
         a.weights[route] = w;
@@ -968,8 +978,50 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
 
   // ---- routing and the unique-expert list (routed experts first, then the shared one)
   if (a.E > 0) {
-    if (a.M <= 4 && a.E <= 256 && a.E > 32) {
-      route_split(a, S, warp, lane, blockIdx.x == 0 && a.phase_lo == 1);
+    const bool dist = a.E > 64 && ((a.E > 256 && a.M >= 2) || a.M > 8);
+    const int wpt = a.M == 1 ? 8 : (a.M == 2 ? 4 : 2);
+    if (!dist && a.M <= 4 && a.E > 32 && a.E <= 128 * wpt) {
+      route_split(a, S, warp, lane, blockIdx.x == 0 && a.phase_lo == 1, 0, a.M, wpt, nullptr);
+    } else if (dist) {
+      // Many tokens or experts: CTA c routes tokens c, c + G, ... with all its
+      // warps, publishes the picks, and every CTA reads all of them back.
+      int mine = 0;
+      for (int t = blockIdx.x; t < a.M; t += gridDim.x) {
+        route_split(a, S, warp, lane, a.phase_lo == 1, t, 1, 8, a.picks);
+        __syncthreads();
+        ++mine;
+      }
+      if (tid == 0) {
+        if (mine > 0) {
+          __threadfence();
+          red_release_gpu_add(a.rsync, static_cast<uint32_t>(mine));
+        }
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_gpu(a.rsync) < static_cast<uint32_t>(a.M)) {
+          if (globaltimer_ns() - t0 > a.timeout_ns) {
+            tc_error(a, S, kErrCrossWait);
+            break;
+          }
+          __nanosleep(64);
+        }
+      }
+      __syncthreads();
+      if (!S.abort) {
+        for (int i = tid; i < a.M * a.top_k; i += kTcThreads) {
+          const int e = __ldcg(a.picks + i);
+          if (e >= 0 && e < a.E) {
+            S.rid[i] = static_cast<int16_t>(e);
+            atomicOr(&S.tokmask[e], 1ull << (i / a.top_k));
+          } else {
+            atomicOr(a.err, kErrRoute);
+          }
+        }
+        // the last CTA past the wait re-arms both counters for the next call
+        if (tid == 0 && atomicAdd(a.rsync + 1, 1u) + 1u == gridDim.x) {
+          atomicExch(a.rsync, 0u);
+          atomicExch(a.rsync + 1, 0u);
+        }
+      }
     } else
     for (int t = warp; t < a.M; t += kTcThreads / 32) {
       // Lane l holds experts l + 32 j, j < J: loops sized to the expert count.
@@ -1279,7 +1331,8 @@ static bool make_map(CUtensorMap* map, const void* base, unsigned long long rows
 }
 
 struct TcWorkspace {
-  uint32_t *err, *done, *passed, *cnt1, *cnt2, *xsync;
+  uint32_t *err, *done, *passed, *cnt1, *cnt2, *xsync, *rsync;
+  int32_t* picks;
   float *hbuf, *part, *xsc;
   uint8_t* ximg;
   int ptok;
@@ -1295,6 +1348,7 @@ static TcWorkspace tc_layout(void* base, int M, int routes, int H, int I, int E)
   size_t off = 0;
   w.err = reinterpret_cast<uint32_t*>(p + off);
   w.xsync = reinterpret_cast<uint32_t*>(p + off + 64);  // two words in the error word's 256-byte unit
+  w.rsync = reinterpret_cast<uint32_t*>(p + off + 128);  // two more
   off += 256;
   w.done = reinterpret_cast<uint32_t*>(p + off);
   off += align256(4 * static_cast<size_t>(E));
@@ -1316,6 +1370,8 @@ static TcWorkspace tc_layout(void* base, int M, int routes, int H, int I, int E)
   off += align256(static_cast<size_t>(M) * H);
   w.xsc = reinterpret_cast<float*>(p + off);
   off += align256(4 * static_cast<size_t>(M) * (H / 128));
+  w.picks = reinterpret_cast<int32_t*>(p + off);
+  off += align256(4 * static_cast<size_t>(M) * kMaxTopK);
   w.bytes = off;
   return w;
 }
@@ -1338,6 +1394,8 @@ static int launch_tc(TcArgs& a, const uint8_t* w13, const uint8_t* w2, const uin
   a.part = w.part;
   a.ximg = w.ximg;
   a.ximg_sc = w.xsc;
+  a.picks = w.picks;
+  a.rsync = w.rsync;
   a.xsync = w.xsync;
   a.ptok = w.ptok;
   a.timeout_ns = wait_timeout_ns();

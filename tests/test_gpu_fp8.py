@@ -61,16 +61,20 @@ def test_routed_small_full_parity(fme, cfg_name, M, ue8m0):
 
 
 @pytest.mark.parametrize("M,E,k", [(1, 256, 8), (1, 40, 3), (1, 256, 1), (2, 96, 32), (3, 256, 8), (4, 200, 16),
-                                   (4, 33, 32)])
+                                   (4, 33, 32), (1, 1024, 32), (2, 300, 8), (5, 896, 16), (9, 128, 8),
+                                   (17, 1024, 32)])
 def test_routing_small_m_with_key_ties(fme, M, E, k):
-    """Up to 4 tokens and 256 experts the kernel splits each token's experts
-    over several warps and merges their picks; ids must equal the oracle's bit
-    for bit, including exact key ties between experts of different 32-expert
-    blocks (equal logits and equal bias: the lower expert id goes first)."""
+    """The kernel routes in three ways: up to 4 tokens (one token up to 1024
+    experts) it splits each token's experts over several warps of every CTA and
+    merges their picks; with more tokens or experts each CTA routes its own
+    share of the tokens that way and all CTAs read every pick back; otherwise a
+    warp routes a token. ids must equal the oracle's bit for bit in all three,
+    including exact key ties between experts of different 32-expert blocks
+    (equal logits and equal bias: the lower expert id goes first)."""
     import dataclasses
     cfg = dataclasses.replace(W.TINY, H=256, I=128, E=E, top_k=k, name=f"route_{E}_{k}")
     w13h, w2h, s13, s2, x, logits, bias = _device_problem(cfg, M, seed=40 + E + k)
-    tied = [e for e in (3, 35, 67, 99, 131, 163) if e < E]
+    tied = [e for e in (3, 35, 67, 99, 131, 163, 291, 899) if e < E]
     bias[tied] = bias[tied[0]]
     for t in range(M):
         logits[t, tied] = logits[t].max() + 0.5
