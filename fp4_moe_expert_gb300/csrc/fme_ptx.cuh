@@ -205,6 +205,44 @@ __device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint6
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Instruction descriptor of tcgen05.mma kind::mxf8f6f4.block_scale with E4M3
+// A and B, FP32 accumulation, UE8M0 scale factors (bit 23), shape M x N, and
+// the scale-factor byte sfid (0..3) of each 32-bit scale cell for A (bits
+// 29-30) and B (bits 4-5).
+__host__ __device__ constexpr uint32_t mxf8_idesc(int M, int N, uint32_t sfid) {
+  return (sfid << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(M >> 4) << 24) | (sfid << 29);
+}
+
+// D[tmem] (+)= (A . 2^(sfa - 127)) x (B . 2^(sfb - 127))^T per 32-value K block
+// (scale_vec::1X), A and B E4M3 from shared memory, the E8M0 scales in tensor
+// memory at sfa / sfb. Issued by one thread.
+__device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %6, 0; tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p; }" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copies 32 rows of 16 bytes from shared memory into tensor memory columns
+// taddr .. taddr + 3 (row i -> lane i) of every lane quadrant.
+__device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Shared-memory descriptor of 16-byte rows stored one after another, no
+// swizzle: 8-row core matrices 128 bytes apart.
+__device__ __forceinline__ uint64_t rows16_desc(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(128u >> 4) << 16;
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  return d;
+}
+
 // Arrive on an mbarrier once every tcgen05 operation this thread issued so far completes.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))

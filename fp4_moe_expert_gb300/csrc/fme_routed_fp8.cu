@@ -48,6 +48,20 @@ constexpr int kAStageBytes = 128 * 128;  // one 128-row x 128-byte K block of we
 constexpr int kBBufBytes = 256 * 128;    // K blocks x N token rows x 128 bytes <= 256 rows
 constexpr int kTmemCols = 512;
 constexpr int kTmemBuf = 256;            // two accumulator buffers
+// The MX kernel keeps its scale vectors in tensor memory beside two
+// 192-column accumulator buffers. A block-scaled MMA reads its scale factors
+// from a 4-column-aligned address (byte sf_id of each 32-bit cell; B tokens
+// 32 .. 63 one column further), so every K block takes 4 columns: the
+// weights' (all 2^0) in columns 384..387, B buffer b's token scales from
+// 388 + 60 b, K block j at + 4 j (at most 15 K blocks). Its fill stages those
+// cells in the B buffer from 24 KB on (a chunk's codes take at most 192
+// columns x 128 bytes = 24 KB), 512 bytes per K block.
+template <bool MX>
+__host__ __device__ constexpr int tmem_buf() { return MX ? 192 : kTmemBuf; }
+constexpr uint32_t kSfaCol = 384;
+constexpr uint32_t kSfbCol = 388;
+constexpr uint32_t kSfbBuf = 60;
+constexpr int kMxSfStage = 24 * 1024;
 constexpr int kMaxKc = 16;
 struct TcArgs {
   CUtensorMap map13;   // routed W13 as [E * 2I rows, H bytes], box 64 rows x 128 bytes
@@ -107,6 +121,7 @@ struct TcSmem {
   int16_t ulist[kMaxExperts];
   int16_t ctx_route[3][kMaxTokens];  // routes of each B buffer's expert, in token order; [2]: the fill's next
   int btag[2];                       // what each B buffer holds: a GEMM2 (unit, K range), or -1
+  alignas(1024) uint32_t sfa_one[128];  // 32 rows x 16 bytes of 2^0 scales (MX kernel)
   int ctx_n[3];
   int16_t seg_route[kMaxTokens];     // the accumulate warps' copy for the current segment
   int seg_n;
@@ -117,6 +132,7 @@ struct TcSmem {
 };
 
 constexpr size_t kTcSmemBytes = sizeof(TcSmem) + 1024;
+static_assert(kTcSmemBytes <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ void tc_error(const TcArgs& a, TcSmem& S, uint32_t bit) {
   atomicOr(a.err, bit);
@@ -358,17 +374,20 @@ __device__ void fill_context(const TcArgs& a, TcSmem& S, int u, int fid) {
   fill_bar();
 }
 
-// MXFP8 input, GEMM1 chunk: token t takes four B rows, 4 t + s holding the
-// E4M3 codes of its 32-value block s of each K block (zeros elsewhere), so one
-// accumulator column per (token, 32-value block) comes out of the usual four
-// K = 32 MMAs of a K block. The four E8M0 bytes of (t, K block j) go to
-// S.xs[b][t][j] as they are (byte s = block s); the accumulate warps apply
-// w_scale x 2^(e - 127) per column. Routed experts only (the MX entry has no
+// MXFP8 input, GEMM1 chunk: one B row per route, the token's E4M3 codes as
+// they are (cp.async into the swizzled layout); the four E8M0 bytes of each
+// (route, K block) -- one per 32-value block -- are staged for the MMA
+// thread, which copies them into tensor memory (tcgen05.cp) where the
+// block-scaled MMA applies them to each 32-value partial. Cell (K block j,
+// route t) is column 4 j + t / 32, lane t % 32 of the buffer's scale columns,
+// staged as copy j (512 bytes), row t % 32, word t / 32. The activation scale
+// of the accumulate step is then 1. Routed experts only (the MX entry has no
 // shared expert).
 __device__ bool fill_b_mx(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& ch, int b, int ci, int fid) {
   const int r = S.ctx_n[2];
-  const int N1 = P.N1;
+  const int N = P.N;
   uint8_t* B = S.B[b];
+  uint32_t* stage = reinterpret_cast<uint32_t*>(B + kMxSfStage);
   const XInfo xi = xinfo(a, S, ch.u);
   float wsv = 0.0f;
   if (fid < 2 * kMaxKc) {
@@ -387,26 +406,26 @@ __device__ bool fill_b_mx(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk
   }
   for (int t = fid; t < r; t += kFillThreads) S.ctx_route[b][t] = S.ctx_route[2][t];
   if (fid == 0) S.ctx_n[b] = r;
-  const int items = ch.kc * r * 32;  // (K block, token, block s, 16-byte chunk of the row)
+  const int items = ch.kc * r * 8;
   for (int w = fid; w < items; w += kFillThreads) {
-    const int p = w >> 5, sub = w & 31;
+    const int p = w >> 3, sub = w & 7;
     const int t = p % r, j = p / r;
-    const int sblk = sub >> 3, c16 = sub & 7;
-    const int row = 4 * t + sblk;
     const int tok = S.ctx_route[2][t] / a.top_k;
-    uint4 q = make_uint4(0u, 0u, 0u, 0u);
-    if ((c16 >> 1) == sblk)
-      q = __ldg(reinterpret_cast<const uint4*>(a.xq + static_cast<size_t>(tok) * a.H + (ch.kb0 + j) * 128 + c16 * 16));
-    *reinterpret_cast<uint4*>(B + j * N1 * 128 + row * 128 + ((c16 ^ (row & 7)) << 4)) = q;
-    if (sub == 0) {
-      const uint8_t* e = a.xsc + static_cast<size_t>(tok) * (a.H / 32) + (ch.kb0 + j) * 4;
-      const uint32_t packed = static_cast<uint32_t>(__ldg(e)) | (static_cast<uint32_t>(__ldg(e + 1)) << 8) |
-                              (static_cast<uint32_t>(__ldg(e + 2)) << 16) | (static_cast<uint32_t>(__ldg(e + 3)) << 24);
-      reinterpret_cast<uint32_t*>(S.xs[b][t])[j] = packed;
-    }
+    cp_async_16(B + j * N * 128 + t * 128 + ((sub ^ (t & 7)) << 4),
+                a.xq + static_cast<size_t>(tok) * a.H + (ch.kb0 + j) * 128 + sub * 16);
+  }
+  for (int w = fid; w < ch.kc * r; w += kFillThreads) {
+    const int t = w % r, j = w / r;
+    const int tok = S.ctx_route[2][t] / a.top_k;
+    const uint8_t* e = a.xsc + static_cast<size_t>(tok) * (a.H / 32) + (ch.kb0 + j) * 4;
+    const uint32_t packed = static_cast<uint32_t>(__ldg(e)) | (static_cast<uint32_t>(__ldg(e + 1)) << 8) |
+                            (static_cast<uint32_t>(__ldg(e + 2)) << 16) | (static_cast<uint32_t>(__ldg(e + 3)) << 24);
+    stage[j * 128 + (t & 31) * 4 + (t >> 5)] = packed;
+    S.xs[b][t][j] = 1.0f;
   }
   if (fid < 2 * kMaxKc) S.wsc[b][fid / kMaxKc][fid % kMaxKc] = wsv;
   if (fid == 0) S.btag[b] = -1;
+  cp_async_wait_all();
   fence_proxy_async_smem();
   fill_bar();
   if (fid == 0) mbar_arrive(&S.bfull[b]);
@@ -885,49 +904,6 @@ __device__ __forceinline__ void accumulate(uint32_t tbase, int N, int kc, int r,
   }
 }
 
-// The MX kernel's GEMM1 chunk: column 4 t + s of K block j holds token t's
-// partial over 32-value block s; y[t] += D * (w_scale[j] * 2^(e - 127)) for
-// s = 0..3 in turn, e = byte s of xs[t][j]. LDT tokens (4 LDT columns) per
-// tcgen05.ld, GROUPS groups of them, KB K blocks per wait.
-template <int LDT, int GROUPS, int KB, int TOK>
-__device__ __forceinline__ void accumulate_mx(uint32_t tbase, int N1, int kc, int r, const float* ws,
-                                              const float (&xs)[kMaxTokens][kMaxKc], float (&y)[TOK]) {
-  constexpr int LD = 4 * LDT;
-#pragma unroll
-  for (int j0 = 0; j0 < kMaxKc; j0 += KB) {
-    if (j0 < kc) {
-#pragma unroll
-      for (int g = 0; g < GROUPS; ++g) {
-        if (g * LDT < r) {
-          uint32_t v[KB][LD];
-#pragma unroll
-          for (int jb = 0; jb < KB; ++jb)
-            if (j0 + jb < kc) tmem_ld<LD>(tbase + (j0 + jb) * N1 + g * LD, v[jb]);
-          tc_wait_ld();
-#pragma unroll
-          for (int jb = 0; jb < KB; ++jb) {
-            if (j0 + jb < kc) {
-#pragma unroll
-              for (int tt = 0; tt < LDT; ++tt) {
-                const int t = g * LDT + tt;
-                if (t < r) {
-                  const uint32_t e4 = __float_as_uint(xs[t][j0 + jb]);
-#pragma unroll
-                  for (int sb = 0; sb < 4; ++sb) {
-                    const uint32_t e = (e4 >> (8 * sb)) & 0xFFu;
-                    const float c = __fmul_rn(ws[j0 + jb], __uint_as_float(e == 0 ? 0x00400000u : e << 23));
-                    y[t] = fmaf(__uint_as_float(v[jb][4 * tt + sb]), c, y[t]);
-                  }
-                }
-              }
-            }
-          }
-        }
-      }
-    }
-  }
-}
-
 // ---------------------------------------------------------------- kernel
 // TOK: token capacity of the accumulators (16 when M <= 16, else 64): the
 // per-token loops are unrolled to it, so the small case keeps its code small
@@ -967,6 +943,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
     tmem_relinquish();
   }
   for (int e = tid; e < a.E; e += kTcThreads) S.tokmask[e] = 0ull;
+  if (MX) {
+    if (tid < 128) S.sfa_one[tid] = 0x7F7F7F7Fu;  // E8M0 2^0 in every byte
+    fence_proxy_async_smem();
+  }
   // The chain's second kernel reads only the inputs the first one read after
   // its own wait (logits, bias, weights) until its fill waits for the hidden
   // rows; every other launch waits for its predecessor here.
@@ -1092,10 +1072,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
   P.U = S.U;
   P.ximage = ximage;
   P.N = 16 * ((S.rmax + 15) / 16);
-  P.kcmax = min(kMaxKc, kTmemBuf / P.N);
+  P.kcmax = min(kMaxKc, tmem_buf<MX>() / P.N);
   P.kcmax2 = P.kcmax;
-  P.N1 = MX ? 16 * ((4 * S.rmax + 15) / 16) : P.N;
-  P.kcmax1 = MX ? min(kMaxKc, kTmemBuf / P.N1) : 0;
+  P.N1 = P.N;
+  P.kcmax1 = P.kcmax;
   P.c = blockIdx.x;
   P.G = gridDim.x;
   P.W = a.phase_lo == a.phase_hi ? 1 : min(P.U, a.has_shared ? layer_waves(a.ptok) : max_waves(a.ptok));
@@ -1164,7 +1144,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = f8_idesc(128, P.N);
-      const uint32_t idesc1 = MX ? f8_idesc(128, P.N1) : idesc;
+      if (MX) {
+        // The weights' scales: 2^0 for every row (their FP32 block scales are
+        // applied by the accumulate warps).
+        tc_cp_32x128b_x4(tmem + kSfaCol, rows16_desc(smem_u32(S.sfa_one)));
+      }
       Cursor cur;
       Chunk ch;
       int k = 0, ci = 0;
@@ -1178,6 +1162,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
         }
         tc_fence_after();
         const uint32_t bbase = smem_u32(S.B[b]);
+        const bool mx1 = MX && ch.phase == 1;
+        const uint32_t sfb = tmem + kSfbCol + kSfbBuf * static_cast<uint32_t>(b);
+        if (mx1) {
+          // this chunk's token scales into tensor memory, ahead of its MMAs
+          for (int q = 0; q < ch.kc; ++q)
+            tc_cp_32x128b_x4(sfb + 4 * q, rows16_desc(bbase + kMxSfStage + 512 * q));
+        }
         for (int j = 0; j < ch.kc; ++j, ++k) {
           const int s = k % kTcStages;
           if (!mbar_wait(&S.full[s], (k / kTcStages) & 1, a.timeout_ns, &S.abort)) {
@@ -1187,14 +1178,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
           }
           tc_fence_after();
           const uint32_t abase = smem_u32(S.A[s]);
-          // MX GEMM1: N1 rows of B (four per token), one column per (token, 32-value block).
-          const bool mx1 = MX && ch.phase == 1;
-          const int nc = mx1 ? P.N1 : P.N;
-          const uint32_t d = tmem + b * kTmemBuf + j * nc;
+          const uint32_t d = tmem + b * tmem_buf<MX>() + j * P.N;
+          if (mx1) {
+            // MX GEMM1: each 32-value partial scaled by its token's E8M0 byte kk
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc_mma_f8(d, sw128_desc(abase + 32 * kk), sw128_desc(bbase + j * nc * 128 + 32 * kk),
-                      mx1 ? idesc1 : idesc, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_mxf8(d, sw128_desc(abase + 32 * kk), sw128_desc(bbase + j * P.N * 128 + 32 * kk),
+                          mxf8_idesc(128, P.N, static_cast<uint32_t>(kk)), tmem + kSfaCol, sfb + 4 * j,
+                          kk > 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_f8(d, sw128_desc(abase + 32 * kk), sw128_desc(bbase + j * P.N * 128 + 32 * kk), idesc,
+                        kk > 0 ? 1u : 0u);
+          }
           tc_commit(&S.empty[s]);
         }
         if (!ok) break;
@@ -1227,18 +1224,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
       if (S.abort) break;
       tc_fence_after();
       const int r = S.ctx_n[b];
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16) + b * kTmemBuf;
-      if (MX && ch.phase == 1) {
-        const float* wsp = S.wsc[b][half];
-        if (r == 1)
-          accumulate_mx<1, 1, 8>(tbase, P.N1, ch.kc, r, wsp, S.xs[b], y);
-        else if (r <= 4)
-          accumulate_mx<4, 1, 2>(tbase, P.N1, ch.kc, r, wsp, S.xs[b], y);
-        else if (TOK == 16 || r <= 16)
-          accumulate_mx<4, 4, 1>(tbase, P.N1, ch.kc, r, wsp, S.xs[b], y);
-        else if constexpr (TOK > 16)
-          accumulate_mx<4, TOK / 4, 1>(tbase, P.N1, ch.kc, r, wsp, S.xs[b], y);
-      } else {
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16) + b * tmem_buf<MX>();
+      {
         float ws[kMaxKc];
 #pragma unroll
         for (int j = 0; j < kMaxKc; ++j) ws[j] = S.wsc[b][ch.phase == 1 ? half : 0][j];
