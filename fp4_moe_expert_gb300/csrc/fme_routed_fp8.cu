@@ -186,31 +186,14 @@ __device__ __forceinline__ void epi_bar() { named_bar_sync(1, 128); }
 __device__ __forceinline__ void fill_bar() { named_bar_sync(2, kFillThreads); }
 
 // ---------------------------------------------------------------- routing
-// One warp routes token t (route_topk) and records its picks.
-template <int J>
-__device__ void route_token(const TcArgs& a, TcSmem& S, int t, int lane, bool write_out) {
-  int e;
-  float w;
-  route_topk<J>(a.logits, a.logits_f32 != 0, a.bias, a.E, a.top_k, a.scale, t, lane, e, w);
-  if (lane < a.top_k) {
-    const int route = t * a.top_k + lane;
-    S.rid[route] = static_cast<int16_t>(e);
-    atomicOr(&S.tokmask[e], 1ull << t);
-    if (write_out) {
-      a.ids[route] = e;
-      a.weights[route] = w;
-    }
-  }
-}
-
-// Up to 4 tokens and 256 experts: the 8 warps split each token's experts
-// (wpt = 8, 4 or 2 warps per token, expert blocks of 32 dealt round-robin),
-// each warp picks its top_k by the rule of route_topk (largest key, lowest
-// expert among equals) into shared memory, then warp t merges token t's
-// candidates by the same rule and forms the weights exactly as route_topk
-// (float sum of the picked scores in pick order, divide, times scale). The
-// picks and weights are those of route_topk bit for bit; the rounds of
-// warp reductions are shorter (one or two keys per lane instead of eight).
+// Routing ("mega_moe" _MegaKernel.top_k_pick): sigmoid scores (accurate
+// expf, IEEE divide), keys score + bias as monotone uint32, the top_k keys
+// with the lowest expert first among equal keys, weights score / (float sum
+// of the picked scores in pick order) * scale. The 8 warps of a CTA split a
+// token's experts (wpt = 8, 4 or 2 warps per token, expert blocks of 32 dealt
+// round-robin), each warp picks its top_k by that rule into shared memory,
+// then one warp per token merges the candidates by the same rule; the merge
+// gives the same picks as one pass over all experts.
 struct RouteCand {
   uint32_t key;
   int e;
@@ -958,11 +941,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
 
   // ---- routing and the unique-expert list (routed experts first, then the shared one)
   if (a.E > 0) {
-    const bool dist = a.E > 64 && ((a.E > 256 && a.M >= 2) || a.M > 8);
     const int wpt = a.M == 1 ? 8 : (a.M == 2 ? 4 : 2);
-    if (!dist && a.M <= 4 && a.E > 32 && a.E <= 128 * wpt) {
+    if (a.M <= 4 && a.E <= 128 * wpt) {
       route_split(a, S, warp, lane, blockIdx.x == 0 && a.phase_lo == 1, 0, a.M, wpt, nullptr);
-    } else if (dist) {
+    } else {
       // Many tokens or experts: CTA c routes tokens c, c + G, ... with all its
       // warps, publishes the picks, and every CTA reads all of them back.
       int mine = 0;
@@ -1002,17 +984,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
           atomicExch(a.rsync + 1, 0u);
         }
       }
-    } else
-    for (int t = warp; t < a.M; t += kTcThreads / 32) {
-      // Lane l holds experts l + 32 j, j < J: loops sized to the expert count.
-      if (a.E <= 64)
-        route_token<2>(a, S, t, lane, blockIdx.x == 0 && a.phase_lo == 1);
-      else if (a.E <= 256)
-        route_token<8>(a, S, t, lane, blockIdx.x == 0 && a.phase_lo == 1);
-      else if (a.E <= 512)
-        route_token<16>(a, S, t, lane, blockIdx.x == 0 && a.phase_lo == 1);
-      else
-        route_token<kMaxExperts / 32>(a, S, t, lane, blockIdx.x == 0 && a.phase_lo == 1);
     }
     __syncthreads();
     if (warp == 0) {
