@@ -125,6 +125,7 @@ struct NvSmem {
   int16_t sid[kMaxTokens * kMaxTopK];  // every route's local expert, -1 when not local
   uint32_t tmem_base;
   int U;
+  int direct;  // every token has at most one local slot: y is written by the GEMM2 epilogue
   volatile int abort;
 };
 
@@ -350,6 +351,19 @@ __device__ void nv_finish2(const NvArgs& a, NvSmem<TOK>& S, int u, int T2, const
                            int etid) {
   const int r0 = S.uoff[u], r = S.uoff[u + 1] - r0;
   const int m = 128 * T2 + row;
+  if (S.direct) {
+    // The slot is its token's only local one: y = bf16(w * bf16(o)), exactly
+    // the scatter's sum of one term.
+#pragma unroll
+    for (int i = 0; i < TOK; ++i)
+      if (i < r) {
+        const int route = S.sroute[r0 + i];
+        const float wt = a.route ? __ldcg(a.tw_out + route) : __ldg(a.tw + route);
+        const float o = __bfloat162float(__float2bfloat16_rn(y[i]));
+        a.y[static_cast<size_t>(S.stok[r0 + i]) * a.H + m] = __float2bfloat16_rn(__fadd_rn(0.0f, __fmul_rn(wt, o)));
+      }
+    return;
+  }
 #pragma unroll
   for (int i = 0; i < TOK; ++i)
     if (i < r) a.obuf[static_cast<size_t>(S.sroute[r0 + i]) * a.H + m] = __float2bfloat16_rn(y[i]);
@@ -563,11 +577,19 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
       S.sid[i] = static_cast<int16_t>(le >= 0 && le < a.L ? le : -1);
     }
   }
+  if (tid == 0) S.direct = 1;
   __syncthreads();
   // ---- local slots and the unit list
   for (int i = tid; i < a.M * a.top_k; i += kNvThreads) {
     const int le = S.sid[i];
     if (le >= 0) atomicOr(&S.tokmask[le], 1ull << (i / a.top_k));
+  }
+  // Direct mode when no token has two local slots (then y[t] = bf16(w * o) of
+  // its one slot, or zero): the GEMM2 epilogue writes y, no scatter pass.
+  for (int t = tid; t < a.M; t += kNvThreads) {
+    int n = 0;
+    for (int r = 0; r < a.top_k; ++r) n += S.sid[t * a.top_k + r] >= 0;
+    if (n > 1) S.direct = 0;
   }
   __syncthreads();
   if (tid == 0) red_release_gpu_add(a.sync, 1u);  // this CTA's share of the x image is written
@@ -865,6 +887,17 @@ __global__ void __launch_bounds__(kNvThreads, 1) nvfp4_tc_kernel(const __grid_co
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kNvTmemCols);
 
+  if (S.direct) {
+    // Tokens without a local slot get zero rows (a share of the rows per CTA).
+    const int chunks = a.H / 8;
+    for (int w = c * kNvThreads + tid; w < a.M * chunks; w += G * kNvThreads) {
+      const int tt = w / chunks;
+      bool any = false;
+      for (int r = 0; r < a.top_k; ++r) any |= S.sid[tt * a.top_k + r] >= 0;
+      if (!any) *reinterpret_cast<uint4*>(a.y + static_cast<size_t>(tt) * a.H + 8 * (w % chunks)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    return;
+  }
   // ---- scatter: y[t, m] = bf16(sum over t's local picks, ascending, of w * o)
   const uint32_t tiles2 = static_cast<uint32_t>(U) * static_cast<uint32_t>(a.H / 128);
   if (tid == 0 && !S.abort) nv_wait_ge(a, S.abort, a.sync + 2, tiles2);
