@@ -7,8 +7,9 @@
 // forbids device allocations after start-up, or capture-time paths where an
 // allocation would be recorded or would fail. They cannot provide the
 // workspace fme_moe_routed_fp8 needs. This entry point uses scratch that
-// lives in this file instead: a fixed device array that every GPU which
-// loads the library holds until the process exits.
+// lives in this file instead: a fixed device array that a GPU holds from the
+// moment this file's module is loaded there (lazily, by default: the first
+// call on that GPU) until the process exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -22,10 +23,11 @@
 
 namespace {
 
-// Largest workspace the variant can serve: 16 MiB. That covers, e.g., the
-// DeepSeek-V3 shape (H = 7168, I = 2048, 256 experts, top_k 8) up to M = 32
-// tokens. Larger requests are rejected with FME_EUNSUPPORTED.
-constexpr size_t kScratchBytes = size_t(16) << 20;
+// Largest workspace the variant can serve: 64 MiB. That covers, e.g., the
+// DeepSeek-V3 shape (H = 7168, I = 2048, 256 experts, top_k 8) up to M = 63
+// tokens and the Latent-MoE shape (H = 3584, 896 experts, top_k 16) up to
+// M = 32. Larger requests are rejected with FME_EUNSUPPORTED.
+constexpr size_t kScratchBytes = size_t(64) << 20;
 
 // The scratch itself. In host code `g_scratch` only names a host-side
 // stand-in, never the device memory: host code must take the device address
@@ -113,7 +115,7 @@ extern "C" int fme_moe_routed_fp8_noalloc(const void* x, const void* logits, int
     return fme::set_last_error(FME_EINVAL, "bad sizes M=%d H=%d I=%d E=%d top_k=%d", M, H, I, E, top_k);
   if (need > kScratchBytes)
     return fme::set_last_error(FME_EUNSUPPORTED,
-                               "needs %zu bytes of scratch; the no-allocation variant holds %zu (16 MiB): "
+                               "needs %zu bytes of scratch; the no-allocation variant holds %zu (64 MiB): "
                                "use fme_moe_routed_fp8 with a caller workspace",
                                need, kScratchBytes);
   int dev = 0;

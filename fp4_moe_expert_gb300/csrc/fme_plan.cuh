@@ -20,13 +20,18 @@ FME_HD constexpr int plan_min(int a, int b) { return a < b ? a : b; }
 // one wave's GEMM1 -> GEMM2 hand-over (last tiles finishing, hidden rows
 // re-quantised) overlaps the next wave's weight stream, and each CTA's work
 // mixes experts hit by different token counts. Every wave adds split tiles,
-// each with a partial round trip. Measured on the DeepSeek-V3 shape: three
-// waves pay off at 5-8 tokens (M = 8: 414 -> 389 us); at 1-4 tokens two
-// waves were slower than one. With the shared expert as one more unit (the
-// one-launch layer, run as one launch up to 4 tokens) two waves pay off at
-// 3-4 tokens (M = 4: 269 -> 244 us).
-FME_HD constexpr int max_waves(int ptok) { return ptok > 4 && ptok <= 8 ? 3 : 1; }
-FME_HD constexpr int layer_waves(int ptok) { return ptok > 2 && ptok <= 4 ? 2 : 1; }
+// each with a partial round trip. Measured on the DeepSeek-V3 shape (256
+// experts, top 8; L2 flushed, W = 1 / 2 / 3 in microseconds):
+//   routed  M = 4: 222 / 224 / 228   M = 6: 293 / 294 / 300   M = 7: 356 / 343 / 332
+//           M = 8: 396 / 384 / 367   M = 12: 558 / 532 / 525   M = 24: 918 / 910 / 866
+//   + shared M = 3: 205 / 193 / 194  M = 4: 267 / 236 / 232   M = 5: 281 / 267 / 275
+//           M = 6: 324 / 304 / 304   M = 8: 406 / 382 / 373   M = 16: 783 / 711 / 683
+// (one wave at 1-2 tokens either way). The shared expert is unit 0 of the
+// one-launch layer, so it streams in the first wave.
+FME_HD constexpr int max_waves(int ptok) { return ptok >= 7 ? 3 : 1; }
+FME_HD constexpr int layer_waves(int ptok) {
+  return ptok <= 2 ? 1 : (ptok == 3 || ptok == 5 ? 2 : 3);
+}
 // Waves the partial-sum region is sized for, any call.
 FME_HD constexpr int waves_cap(int ptok) {
   return max_waves(ptok) > layer_waves(ptok) ? max_waves(ptok) : layer_waves(ptok);

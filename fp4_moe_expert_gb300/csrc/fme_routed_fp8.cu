@@ -118,7 +118,7 @@ struct TcSmem {
   uint64_t bfull[2], accfull[2], tmemfree[2], mfree[2], final_bar;
   unsigned long long tokmask[kMaxExperts];
   int16_t rid[kMaxTokens * kMaxTopK];
-  int16_t ulist[kMaxExperts];
+  int16_t ulist[kMaxExperts + 1];  // [0]: the shared expert, when present
   int16_t ctx_route[3][kMaxTokens];  // routes of each B buffer's expert, in token order; [2]: the fill's next
   int btag[2];                       // what each B buffer holds: a GEMM2 (unit, K range), or -1
   alignas(1024) uint32_t sfa_one[128];  // 32 rows x 16 bytes of 2^0 scales (MX kernel)
@@ -139,8 +139,8 @@ __device__ __forceinline__ void tc_error(const TcArgs& a, TcSmem& S, uint32_t bi
   S.abort = 1;
 }
 
-// What differs per work expert: the routed experts of the unique list, then
-// (when present) the shared expert as the last unit, routed to every token.
+// What differs per work expert: (when present) the shared expert as unit 0,
+// routed to every token, then the routed experts of the unique list.
 // The shared expert follows "shared_expert" (gate rows first, BF16 gate_up and
 // h, re-quant by multiplying with the inverse); routed experts follow
 // "mega_moe" (up rows first, FP32 h, re-quant by dividing).
@@ -158,7 +158,7 @@ struct XInfo {
 
 __device__ __forceinline__ XInfo xinfo(const TcArgs& a, const TcSmem& S, int u) {
   XInfo x;
-  x.shared = a.has_shared && u == S.U - 1;
+  x.shared = a.has_shared && u == 0;
   if (x.shared) {
     x.id = a.E;
     x.row_e = 0;
@@ -331,7 +331,7 @@ __device__ void fill_context(const TcArgs& a, TcSmem& S, int u, int fid) {
   constexpr int b = 2;
   if (fid < 32) {
     const int lane = fid;
-    if (a.has_shared && u == S.U - 1) {
+    if (a.has_shared && u == 0) {
       // The shared expert's rows follow the routed ones in hbuf: M*top_k + t.
       for (int t = lane; t < a.M; t += 32) S.ctx_route[b][t] = static_cast<int16_t>(a.M * a.top_k + t);
       if (lane == 0) S.ctx_n[b] = a.M;
@@ -688,7 +688,7 @@ __device__ void finish_gemm2(const TcArgs& a, TcSmem& S, const Chunk& ch, int b,
                              int row) {
   const int r = S.seg_n;
   const int m = 128 * ch.T + row;
-  const bool shared = a.has_shared && ch.u == S.U - 1;
+  const bool shared = a.has_shared && ch.u == 0;
   // Routed rows go to out[route]; the shared expert's (routes M*top_k + t) to sout[t].
   __nv_bfloat16* dst = shared ? a.sout : a.out;
   const int row0 = shared ? a.M * a.top_k : 0;
@@ -990,7 +990,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
     }
     __syncthreads();
     if (warp == 0) {
-      int U = 0, rmax = 0;
+      // The shared expert, when present, is unit 0 (its weights stream in the
+      // first wave, so its GEMM1 -> GEMM2 hand-over overlaps the routed
+      // experts' stream); the routed experts follow in ascending order.
+      int U = a.has_shared ? 1 : 0, rmax = 0;
+      if (lane == 0 && a.has_shared) S.ulist[0] = -1;
       for (int b = 0; b < a.E; b += 32) {
         const int e = b + lane;
         const unsigned long long m = e < a.E ? S.tokmask[e] : 0ull;
@@ -1001,7 +1005,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
         rmax = max(rmax, static_cast<int>(__reduce_max_sync(0xFFFFFFFFu, static_cast<uint32_t>(__popcll(m)))));
       }
       if (lane == 0) {
-        S.U = U + a.has_shared;
+        S.U = U;
         S.rmax = a.has_shared ? max(rmax, a.M) : rmax;
       }
     }
@@ -1337,13 +1341,10 @@ static TcWorkspace tc_layout(void* base, int M, int routes, int H, int I, int E)
   return w;
 }
 
-// lay_routes / lay_slots: hidden rows and counter slots of the workspace
-// layout (by default this call's own).
 static int launch_tc(TcArgs& a, const uint8_t* w13, const uint8_t* w2, const uint8_t* sw13, const uint8_t* sw2,
-                     void* workspace, size_t workspace_bytes, cudaStream_t st, int lay_routes = -1,
-                     int lay_slots = -1) {
-  const int routes = lay_routes >= 0 ? lay_routes : a.M * a.top_k + (a.has_shared ? a.M : 0);
-  const TcWorkspace w = tc_layout(workspace, a.M, routes, a.H, a.I, lay_slots >= 0 ? lay_slots : a.E + 1);
+                     void* workspace, size_t workspace_bytes, cudaStream_t st) {
+  const int routes = a.M * a.top_k + (a.has_shared ? a.M : 0);
+  const TcWorkspace w = tc_layout(workspace, a.M, routes, a.H, a.I, a.E + 1);
   if (workspace == nullptr || workspace_bytes < w.bytes)
     return set_last_error(FME_EWORKSPACE, "workspace of %zu bytes needed, %zu given", w.bytes, workspace_bytes);
   a.err = w.err;
@@ -1389,9 +1390,6 @@ static int launch_tc(TcArgs& a, const uint8_t* w13, const uint8_t* w2, const uin
   return FME_OK;
 }
 
-static int layer_launch(const RoutedFp8& r, const SharedFp8& sh, int M, int H, int I, void* workspace,
-                        size_t workspace_bytes, cudaStream_t st, int lay_routes, int lay_slots);
-
 // Routed calls as a two-kernel chain instead of one persistent launch
 // (FME_FP8_CHAIN=1): kept to compare the two schedules, off by default.
 static bool fp8_chain_enabled() {
@@ -1404,23 +1402,6 @@ int layer_fp8(const RoutedFp8& r, const SharedFp8& sh, int M, int H, int I, void
   // The MXFP8-input kernel reads its tokens from xq only: no shared expert beside it.
   if (r.xq != nullptr && sh.w13 != nullptr)
     return set_last_error(FME_EINVAL, "MXFP8 input with a shared expert is not supported");
-  // Above 4 tokens the shared expert as the last unit of the routed schedule
-  // costs more than it saves (M = 8: 490 us in one launch against 418 us for
-  // the two calls): run it alone, then the routed experts, on the stream.
-  // Both launches use the one-launch call's workspace layout (the shared
-  // expert alone takes counter slot 0, zero before and after it), and each
-  // leaves the zeroed prefix zero for the next.
-  if (r.E > 0 && sh.w13 != nullptr && M > 4) {
-    const int lay_routes = M * r.top_k + M, lay_slots = r.E + 1;
-    const int err = layer_launch(RoutedFp8{}, sh, M, H, I, workspace, workspace_bytes, st, lay_routes, lay_slots);
-    if (err != FME_OK) return err;
-    return layer_launch(r, SharedFp8{}, M, H, I, workspace, workspace_bytes, st, lay_routes, lay_slots);
-  }
-  return layer_launch(r, sh, M, H, I, workspace, workspace_bytes, st, -1, -1);
-}
-
-static int layer_launch(const RoutedFp8& r, const SharedFp8& sh, int M, int H, int I, void* workspace,
-                        size_t workspace_bytes, cudaStream_t st, int lay_routes, int lay_slots) {
   TcArgs a;
   memset(&a, 0, sizeof(a));
   a.phase_lo = 1;
@@ -1462,11 +1443,11 @@ static int layer_launch(const RoutedFp8& r, const SharedFp8& sh, int M, int H, i
     // programmatic dependent launch (the same workspace layout; the second
     // kernel re-arms the hidden counters the first one raised).
     a.phase_hi = 1;
-    const int err = launch_tc(a, r.w13, r.w2, sh.w13, sh.w2, workspace, workspace_bytes, st, lay_routes, lay_slots);
+    const int err = launch_tc(a, r.w13, r.w2, sh.w13, sh.w2, workspace, workspace_bytes, st);
     if (err != FME_OK) return err;
     a.phase_lo = a.phase_hi = 2;
   }
-  return launch_tc(a, r.w13, r.w2, sh.w13, sh.w2, workspace, workspace_bytes, st, lay_routes, lay_slots);
+  return launch_tc(a, r.w13, r.w2, sh.w13, sh.w2, workspace, workspace_bytes, st);
 }
 
 // Counter slots are sized for the routed experts plus the shared expert

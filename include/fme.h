@@ -132,13 +132,15 @@ int fme_moe_routed_fp8_mx(const uint8_t* xq, const uint8_t* xscales, const void*
  * plug-in whose host forbids device allocations after start-up, paths that
  * run while a graph is being captured), so they cannot hand over a workspace.
  * This variant takes the same arguments minus the workspace and uses an
- * 16 MiB scratch array compiled into libfme.so instead; every GPU that loads
- * the library holds that array until the process exits. It allocates
+ * 64 MiB scratch array compiled into libfme.so instead. A GPU holds that
+ * array from the moment the module that defines it is loaded there (with
+ * CUDA's default lazy loading, the variant's first call on that GPU) until
+ * the process exits. It allocates
  * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
  *
- * - Size limit: the call must need at most 16 MiB of workspace
- *   (fme_moe_routed_fp8_workspace <= 16777216; e.g. the DeepSeek-V3 shape
- *   H = 7168, I = 2048, top_k = 8 up to M = 32 tokens). Larger requests
+ * - Size limit: the call must need at most 64 MiB of workspace
+ *   (fme_moe_routed_fp8_workspace <= 67108864; e.g. the DeepSeek-V3 shape
+ *   H = 7168, I = 2048, top_k = 8 up to M = 63 tokens). Larger requests
  *   return FME_EUNSUPPORTED.
  * - First call per device: it looks up the array's device address with that
  *   device current. Make that first call before any stream capture. The
