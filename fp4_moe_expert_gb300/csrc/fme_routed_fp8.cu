@@ -1341,10 +1341,13 @@ static TcWorkspace tc_layout(void* base, int M, int routes, int H, int I, int E)
   return w;
 }
 
+// lay_routes / lay_slots: hidden rows and counter slots of the workspace
+// layout (by default this call's own).
 static int launch_tc(TcArgs& a, const uint8_t* w13, const uint8_t* w2, const uint8_t* sw13, const uint8_t* sw2,
-                     void* workspace, size_t workspace_bytes, cudaStream_t st) {
-  const int routes = a.M * a.top_k + (a.has_shared ? a.M : 0);
-  const TcWorkspace w = tc_layout(workspace, a.M, routes, a.H, a.I, a.E + 1);
+                     void* workspace, size_t workspace_bytes, cudaStream_t st, int lay_routes = -1,
+                     int lay_slots = -1) {
+  const int routes = lay_routes >= 0 ? lay_routes : a.M * a.top_k + (a.has_shared ? a.M : 0);
+  const TcWorkspace w = tc_layout(workspace, a.M, routes, a.H, a.I, lay_slots >= 0 ? lay_slots : a.E + 1);
   if (workspace == nullptr || workspace_bytes < w.bytes)
     return set_last_error(FME_EWORKSPACE, "workspace of %zu bytes needed, %zu given", w.bytes, workspace_bytes);
   a.err = w.err;
@@ -1397,11 +1400,33 @@ static bool fp8_chain_enabled() {
   return env != nullptr && env[0] == '1';
 }
 
+static int layer_launch(const RoutedFp8& r, const SharedFp8& sh, int M, int H, int I, void* workspace,
+                        size_t workspace_bytes, cudaStream_t st, int lay_routes, int lay_slots);
+
 int layer_fp8(const RoutedFp8& r, const SharedFp8& sh, int M, int H, int I, void* workspace, size_t workspace_bytes,
               cudaStream_t st) {
   // The MXFP8-input kernel reads its tokens from xq only: no shared expert beside it.
   if (r.xq != nullptr && sh.w13 != nullptr)
     return set_last_error(FME_EINVAL, "MXFP8 input with a shared expert is not supported");
+  // Above 16 tokens the shared unit, every token on one expert, is far more
+  // fill, accumulate and epilogue work per weight byte than the routed units,
+  // and the CTAs holding its slices set the launch's time (DeepSeek-V3 shape:
+  // M = 32 1394 us in one launch against 1056 + 109 us for the two calls). It
+  // then runs alone, followed by the routed experts, on the stream. Both
+  // launches use the one-launch call's workspace layout (the shared expert
+  // alone takes counter slot 0, zero before and after it), and each leaves
+  // the zeroed prefix zero for the next.
+  if (r.E > 0 && sh.w13 != nullptr && M > 16) {
+    const int lay_routes = M * r.top_k + M, lay_slots = r.E + 1;
+    const int err = layer_launch(RoutedFp8{}, sh, M, H, I, workspace, workspace_bytes, st, lay_routes, lay_slots);
+    if (err != FME_OK) return err;
+    return layer_launch(r, SharedFp8{}, M, H, I, workspace, workspace_bytes, st, lay_routes, lay_slots);
+  }
+  return layer_launch(r, sh, M, H, I, workspace, workspace_bytes, st, -1, -1);
+}
+
+static int layer_launch(const RoutedFp8& r, const SharedFp8& sh, int M, int H, int I, void* workspace,
+                        size_t workspace_bytes, cudaStream_t st, int lay_routes, int lay_slots) {
   TcArgs a;
   memset(&a, 0, sizeof(a));
   a.phase_lo = 1;
@@ -1443,11 +1468,11 @@ int layer_fp8(const RoutedFp8& r, const SharedFp8& sh, int M, int H, int I, void
     // programmatic dependent launch (the same workspace layout; the second
     // kernel re-arms the hidden counters the first one raised).
     a.phase_hi = 1;
-    const int err = launch_tc(a, r.w13, r.w2, sh.w13, sh.w2, workspace, workspace_bytes, st);
+    const int err = launch_tc(a, r.w13, r.w2, sh.w13, sh.w2, workspace, workspace_bytes, st, lay_routes, lay_slots);
     if (err != FME_OK) return err;
     a.phase_lo = a.phase_hi = 2;
   }
-  return launch_tc(a, r.w13, r.w2, sh.w13, sh.w2, workspace, workspace_bytes, st);
+  return launch_tc(a, r.w13, r.w2, sh.w13, sh.w2, workspace, workspace_bytes, st, lay_routes, lay_slots);
 }
 
 // Counter slots are sized for the routed experts plus the shared expert

@@ -201,12 +201,13 @@ size_t fme_shared_expert_fp8_workspace(int M, int H, int I);
  * part fme_shared_expert_fp8 ("shared_expert"), each with its own rounding
  * rules, weight layout (routed: up rows first; shared: gate rows first) and
  * clamp. The "shared_expert" page runs its two GEMVs as separate small kernels
- * beside the mega MoE kernel, sharing its SMs; here, up to 4 tokens, the
- * shared expert is one more unit of work in the routed kernel's schedule, so
- * its 44 MB of weights stream in the same pass as the routed experts' and no
- * second launch or GEMM1 -> GEMM2 drain is paid for it. Above 4 tokens that
- * costs more than it saves, and the call issues two launches on the stream:
- * the shared expert alone, then the routed experts. Every token routes to it.
+ * beside the mega MoE kernel, sharing its SMs; here, up to 16 tokens, the
+ * shared expert is one more unit of work in the routed kernel's schedule
+ * (the first), so its 44 MB of weights stream in the same pass as the routed
+ * experts' and no second launch or GEMM1 -> GEMM2 drain is paid for it. Above
+ * 16 tokens its per-byte work (every token on one unit) would hold up the
+ * launch, and the call issues two launches on the stream: the shared expert
+ * alone, then the routed experts. Every token routes to it.
  *
  * Arguments: those of fme_moe_routed_fp8 (x, logits, bias, routed weights,
  * M, H, I, E, top_k, limit, scale, ue8m0, out, ids, weights), plus the shared
@@ -215,7 +216,7 @@ size_t fme_shared_expert_fp8_workspace(int M, int H, int I);
  * shared_limit (> 0, +inf allowed) and scale flag shared_ue8m0, and its
  * output shared_out [M, H] BF16. The shared expert has the routed experts'
  * H and I. ids and weights equal those of fme_moe_routed_fp8 bit for bit;
- * out and shared_out meet the same tolerances. Up to 4 tokens they can differ
+ * out and shared_out meet the same tolerances. Up to 16 tokens they can differ
  * from the separate calls in the last bit of a few elements: the K blocks of a
  * tile are split over CTAs by the total work, which the extra unit changes,
  * and that changes the FP32 summation order.

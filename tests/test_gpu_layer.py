@@ -72,7 +72,7 @@ def _check_layer(fme, cfg, scfg, M, seed, ws=None, shared_ws=None):
     _close(sout, sout2, "shared")
 
 
-@pytest.mark.parametrize("M", [1, 4, 5, 64])
+@pytest.mark.parametrize("M", [1, 4, 5, 16, 17, 64])
 @pytest.mark.parametrize("shared_ue8m0", [False, True])
 def test_layer_small_matches_oracle_and_separate_calls(fme, M, shared_ue8m0):
     scfg = W.SharedConfig("small_shared", W.RAGGED.H, W.RAGGED.I, 5.0, shared_ue8m0)
@@ -93,6 +93,18 @@ def test_layer_workspace_shared_with_routed_calls(fme):
     sws = fme.Workspace(fme.shared_expert_fp8_workspace(8, cfg.H, cfg.I), DEV)
     for step, M in enumerate((8, 3, 8, 1)):
         _check_layer(fme, cfg, scfg, M, seed=40 + step, ws=ws, shared_ws=sws)
+
+
+def test_layer_one_and_two_launch_calls_share_a_workspace(fme):
+    """Above 16 tokens the layer call runs the shared expert, then the routed
+    experts, as two launches; calls on either side of that line, in any order,
+    share one workspace sized for the largest."""
+    cfg = W.RAGGED
+    scfg = W.SharedConfig("small_shared", cfg.H, cfg.I, 7.0, False)
+    ws = fme.Workspace(fme.moe_layer_fp8_workspace(32, cfg.H, cfg.I, cfg.E, cfg.top_k), DEV)
+    sws = fme.Workspace(fme.shared_expert_fp8_workspace(32, cfg.H, cfg.I), DEV)
+    for step, M in enumerate((32, 8, 17, 16, 1)):
+        _check_layer(fme, cfg, scfg, M, seed=50 + step, ws=ws, shared_ws=sws)
 
 
 def test_layer_dsv3_full_size(fme):
