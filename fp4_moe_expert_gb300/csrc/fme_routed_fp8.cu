@@ -401,8 +401,13 @@ __device__ bool fill_b_mx(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk
     const int t = w % r, j = w / r;
     const int tok = S.ctx_route[2][t] / a.top_k;
     const uint8_t* e = a.xsc + static_cast<size_t>(tok) * (a.H / 32) + (ch.kb0 + j) * 4;
-    const uint32_t packed = static_cast<uint32_t>(__ldg(e)) | (static_cast<uint32_t>(__ldg(e + 1)) << 8) |
-                            (static_cast<uint32_t>(__ldg(e + 2)) << 16) | (static_cast<uint32_t>(__ldg(e + 3)) << 24);
+    // The four bytes in one load when the array is 4-byte aligned (rows are
+    // H / 32 bytes, a multiple of 4); bytes [e, e + 3] little-endian either way.
+    const uint32_t packed = (reinterpret_cast<uintptr_t>(a.xsc) & 3u) == 0u
+                                ? __ldg(reinterpret_cast<const uint32_t*>(e))
+                                : static_cast<uint32_t>(__ldg(e)) | (static_cast<uint32_t>(__ldg(e + 1)) << 8) |
+                                      (static_cast<uint32_t>(__ldg(e + 2)) << 16) |
+                                      (static_cast<uint32_t>(__ldg(e + 3)) << 24);
     stage[j * 128 + (t & 31) * 4 + (t >> 5)] = packed;
     S.xs[b][t][j] = 1.0f;
   }
@@ -638,20 +643,21 @@ __device__ void finish_gemm1(const TcArgs& a, TcSmem& S, const Chunk& ch, int b,
   const bool shared = xi.shared;
   const int q = row & 63;
   const float L = xi.limit;
-  for (int g = 0; g * 16 < r; ++g) {
+  constexpr int GS = TOK < 16 ? TOK : 16;  // tokens per pass through shared memory
+  for (int g = 0; g * GS < r; ++g) {
 #pragma unroll
-    for (int gg = 0; gg < TOK / 16; ++gg) {
+    for (int gg = 0; gg < TOK / GS; ++gg) {
       if (gg == g) {
 #pragma unroll
-        for (int t = 0; t < 16; ++t) S.ysm[t][row] = y[gg * 16 + t];
+        for (int t = 0; t < GS; ++t) S.ysm[t][row] = y[gg * GS + t];
       }
     }
     epi_bar();
     if (row < 64) {
-      const int n = min(16, r - g * 16);
+      const int n = min(GS, r - g * GS);
 #pragma unroll 1
       for (int t = 0; t < n; ++t) {
-        const int route = S.seg_route[g * 16 + t];
+        const int route = S.seg_route[g * GS + t];
         const float first = S.ysm[t][q], sec = S.ysm[t][q + 64];
         float h;
         if (!shared) {
@@ -891,9 +897,9 @@ __device__ __forceinline__ void accumulate(uint32_t tbase, int N, int kc, int r,
 }
 
 // ---------------------------------------------------------------- kernel
-// TOK: token capacity of the accumulators (16 when M <= 16, else 64): the
-// per-token loops are unrolled to it, so the small case keeps its code small
-// enough to stay in the instruction caches.
+// TOK: token capacity of the accumulators (8, 16, 32 or 64: the smallest that
+// holds M): the per-token loops are unrolled to it, so the smaller cases keep
+// their code small enough to stay in the instruction caches.
 template <int TOK, bool MX>
 __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_constant__ TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -1211,6 +1217,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
           accumulate<1, 1, 16>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
         else if (r <= 4)
           accumulate<4, 1, 8>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
+        else if constexpr (TOK == 8)
+          accumulate<8, 1, 4>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
         else if (TOK == 16 || r <= 16)
           accumulate<16, 1, 2>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
         else if constexpr (TOK > 16)
@@ -1374,9 +1382,16 @@ static int launch_tc(TcArgs& a, const uint8_t* w13, const uint8_t* w2, const uin
   if (cudaGetDevice(&dev) != cudaSuccess) return set_last_error(FME_ECUDA, "cudaGetDevice failed");
   const int sms = device_sm_count(dev);
   if (sms <= 0) return set_last_error(FME_ECUDA, "cannot query the SM count");
-  // M <= 16 tokens: the 16-token variant (every expert then has <= 16 rows).
-  auto kernel = a.xq != nullptr ? (a.M <= 16 ? fp8_moe_tc_kernel<16, true> : fp8_moe_tc_kernel<kMaxTokens, true>)
-                                 : (a.M <= 16 ? fp8_moe_tc_kernel<16, false> : fp8_moe_tc_kernel<kMaxTokens, false>);
+  // The smallest token capacity that holds M (every expert then has <= M rows).
+  auto kernel = a.xq != nullptr
+                    ? (a.M <= 8 ? fp8_moe_tc_kernel<8, true>
+                                : (a.M <= 16 ? fp8_moe_tc_kernel<16, true>
+                                             : (a.M <= 32 ? fp8_moe_tc_kernel<32, true>
+                                                          : fp8_moe_tc_kernel<kMaxTokens, true>)))
+                    : (a.M <= 8 ? fp8_moe_tc_kernel<8, false>
+                                : (a.M <= 16 ? fp8_moe_tc_kernel<16, false>
+                                             : (a.M <= 32 ? fp8_moe_tc_kernel<32, false>
+                                                          : fp8_moe_tc_kernel<kMaxTokens, false>)));
   if (!ensure_smem_attr(dev, reinterpret_cast<const void*>(kernel), kTcSmemBytes)) return FME_ECUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sms < kFp8MaxCtas ? sms : kFp8MaxCtas);

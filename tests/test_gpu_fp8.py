@@ -51,7 +51,7 @@ def _run_small(fme, cfg, M, seed, top_k=None, **over):
     return got, ref, ids.cpu().numpy(), rids
 
 
-@pytest.mark.parametrize("cfg_name,M", [("tiny_fp8", 1), ("ragged_fp8", 5)])
+@pytest.mark.parametrize("cfg_name,M", [("tiny_fp8", 1), ("ragged_fp8", 5), ("ragged_fp8", 24)])
 @pytest.mark.parametrize("ue8m0", [False, True])
 def test_routed_small_full_parity(fme, cfg_name, M, ue8m0):
     import dataclasses

@@ -53,7 +53,7 @@ def _run(fme, cfg, M, seed, w13h, w2h, s13, s2, dev_weights=None, routes=None, r
     return out, ids
 
 
-@pytest.mark.parametrize("cfg_name,M", [("tiny_fp8", 1), ("ragged_fp8", 5), ("ragged_fp8", 16)])
+@pytest.mark.parametrize("cfg_name,M", [("tiny_fp8", 1), ("ragged_fp8", 5), ("ragged_fp8", 16), ("ragged_fp8", 24)])
 @pytest.mark.parametrize("ue8m0", [False, True])
 def test_mx_small_full_parity(fme, cfg_name, M, ue8m0):
     cfg = dataclasses.replace(W.FP8_CONFIGS[cfg_name], ue8m0=ue8m0)
