@@ -897,9 +897,10 @@ __device__ __forceinline__ void accumulate(uint32_t tbase, int N, int kc, int r,
 }
 
 // ---------------------------------------------------------------- kernel
-// TOK: token capacity of the accumulators (8, 16, 32 or 64: the smallest that
-// holds M): the per-token loops are unrolled to it, so the smaller cases keep
-// their code small enough to stay in the instruction caches.
+// TOK: token capacity of the accumulators (1, 4, 8, 16, 32 or 64: the
+// smallest that holds M; the MXFP8-token kernel starts at 8): the per-token
+// loops are unrolled to it, so the smaller cases keep their code small enough
+// to stay in the instruction caches.
 template <int TOK, bool MX>
 __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_constant__ TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -1213,16 +1214,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
         float ws[kMaxKc];
 #pragma unroll
         for (int j = 0; j < kMaxKc; ++j) ws[j] = S.wsc[b][ch.phase == 1 ? half : 0][j];
-        if (r == 1)
+        // Load widths by this chunk's route count, none wider than TOK.
+        if (TOK == 1 || r == 1) {
           accumulate<1, 1, 16>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
-        else if (r <= 4)
-          accumulate<4, 1, 8>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
-        else if constexpr (TOK == 8)
+        } else if (TOK == 4 || r <= 4) {
+          if constexpr (TOK >= 4) accumulate<4, 1, 8>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
+        } else if constexpr (TOK == 8) {
           accumulate<8, 1, 4>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
-        else if (TOK == 16 || r <= 16)
-          accumulate<16, 1, 2>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
-        else if constexpr (TOK > 16)
-          accumulate<16, TOK / 16, 1>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
+        } else if (TOK == 16 || r <= 16) {
+          if constexpr (TOK >= 16) accumulate<16, 1, 2>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
+        } else {
+          if constexpr (TOK > 16) accumulate<16, TOK / 16, 1>(tbase, P.N, ch.kc, r, ws, S.xs[b], y);
+        }
       }
       tc_fence_before();
       if (seg_first) {
@@ -1388,7 +1391,9 @@ static int launch_tc(TcArgs& a, const uint8_t* w13, const uint8_t* w2, const uin
                                 : (a.M <= 16 ? fp8_moe_tc_kernel<16, true>
                                              : (a.M <= 32 ? fp8_moe_tc_kernel<32, true>
                                                           : fp8_moe_tc_kernel<kMaxTokens, true>)))
-                    : (a.M <= 8 ? fp8_moe_tc_kernel<8, false>
+                    : (a.M == 1 ? fp8_moe_tc_kernel<1, false>
+                                : a.M <= 4 ? fp8_moe_tc_kernel<4, false>
+                                : a.M <= 8 ? fp8_moe_tc_kernel<8, false>
                                 : (a.M <= 16 ? fp8_moe_tc_kernel<16, false>
                                              : (a.M <= 32 ? fp8_moe_tc_kernel<32, false>
                                                           : fp8_moe_tc_kernel<kMaxTokens, false>)));
