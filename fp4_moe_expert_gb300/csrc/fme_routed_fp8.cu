@@ -898,9 +898,10 @@ __device__ __forceinline__ void accumulate(uint32_t tbase, int N, int kc, int r,
 
 // ---------------------------------------------------------------- kernel
 // TOK: token capacity of the accumulators (1, 4, 8, 16, 32 or 64: the
-// smallest that holds M; the MXFP8-token kernel starts at 8): the per-token
-// loops are unrolled to it, so the smaller cases keep their code small enough
-// to stay in the instruction caches.
+// smallest that holds M): the per-token loops are unrolled to it, so the
+// smaller cases keep their code small enough to stay in the instruction
+// caches, and code that cannot run at that capacity (the x image, the
+// distributed router at one token) is left out.
 template <int TOK, bool MX>
 __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_constant__ TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -952,7 +953,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
   // ---- routing and the unique-expert list (routed experts first, then the shared one)
   if (a.E > 0) {
     const int wpt = a.M == 1 ? 8 : (a.M == 2 ? 4 : 2);
-    if (a.M <= 4 && a.E <= 128 * wpt) {
+    static_assert(kMaxExperts <= 128 * 8, "one token always takes the split router");
+    if (TOK == 1 || (a.M <= 4 && a.E <= 128 * wpt)) {
       route_split(a, S, warp, lane, blockIdx.x == 0 && a.phase_lo == 1, 0, a.M, wpt, nullptr);
     } else {
       // Many tokens or experts: CTA c routes tokens c, c + G, ... with all its
@@ -1026,7 +1028,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
   // CTA a share of the (token, K block) groups, one warp per group, the same
   // arithmetic as fill_b), so the GEMM1 fills only copy rows. With few routes
   // per expert the per-chunk quantisation is cheaper than the grid-wide wait.
-  const bool ximage = !MX && a.E > 0 && S.rmax > kXImageRoutes && (!a.has_shared || a.sue8m0 == a.ue8m0);
+  const bool ximage =
+      !MX && TOK > kXImageRoutes && a.E > 0 && S.rmax > kXImageRoutes && (!a.has_shared || a.sue8m0 == a.ue8m0);
   if (ximage) {
     const int nbx = a.H / 128;
     const int groups = a.M * nbx;
@@ -1387,7 +1390,9 @@ static int launch_tc(TcArgs& a, const uint8_t* w13, const uint8_t* w2, const uin
   if (sms <= 0) return set_last_error(FME_ECUDA, "cannot query the SM count");
   // The smallest token capacity that holds M (every expert then has <= M rows).
   auto kernel = a.xq != nullptr
-                    ? (a.M <= 8 ? fp8_moe_tc_kernel<8, true>
+                    ? (a.M == 1 ? fp8_moe_tc_kernel<1, true>
+                                : a.M <= 4 ? fp8_moe_tc_kernel<4, true>
+                                : a.M <= 8 ? fp8_moe_tc_kernel<8, true>
                                 : (a.M <= 16 ? fp8_moe_tc_kernel<16, true>
                                              : (a.M <= 32 ? fp8_moe_tc_kernel<32, true>
                                                           : fp8_moe_tc_kernel<kMaxTokens, true>)))
