@@ -135,14 +135,16 @@ template <int TOK>
 constexpr size_t nv_smem_bytes() {
   return sizeof(NvSmem<TOK>) + 1024 > 120 * 1024 ? sizeof(NvSmem<TOK>) + 1024 : 120 * 1024;
 }
-static_assert(nv_smem_bytes<16>() <= 232448 && nv_smem_bytes<64>() <= 232448, "shared memory per CTA");
-static_assert(128 + 32 * NvCfg<16>::kSfBuf <= kNvTmemCols && 128 + 32 * NvCfg<64>::kSfBuf <= kNvTmemCols,
-              "tensor memory columns");
-// Swizzled TMA destinations (128-byte swizzle) start on 1024-byte boundaries.
-static_assert(offsetof(NvSmem<16>, R) % 1024 == 0 && offsetof(NvSmem<64>, R) % 1024 == 0, "ring alignment");
-// A second CTA on the SM would wait in its TMEM allocation while the first
-// may wait on it through the cross-CTA counters: shared memory keeps it out.
-static_assert(nv_smem_bytes<16>() > 233472 / 2 && nv_smem_bytes<64>() > 233472 / 2, "one CTA per SM");
+template <int TOK>
+constexpr bool nv_fits() {
+  // Shared memory per CTA; tensor memory columns; swizzled TMA destinations
+  // (128-byte swizzle) on 1024-byte boundaries; and one CTA per SM: a second
+  // CTA would wait in its TMEM allocation while the first may wait on it
+  // through the cross-CTA counters, so shared memory keeps it out.
+  return nv_smem_bytes<TOK>() <= 232448 && 128 + 32 * NvCfg<TOK>::kSfBuf <= kNvTmemCols &&
+         offsetof(NvSmem<TOK>, R) % 1024 == 0 && nv_smem_bytes<TOK>() > 233472 / 2;
+}
+static_assert(nv_fits<16>() && nv_fits<32>() && nv_fits<64>(), "NVFP4 kernel resources");
 
 __device__ __forceinline__ void nv_epi_bar() { named_bar_sync(1, 128); }
 
@@ -991,7 +993,7 @@ static NvWorkspace nv_layout(void* base, int M, int H, int N, int L, int top_k) 
   NvWorkspace w;
   uint8_t* p = static_cast<uint8_t*>(base);
   size_t off = 0;
-  w.tok = M <= 16 ? 16 : kMaxTokens;
+  w.tok = M <= 16 ? 16 : (M <= 32 ? 32 : kMaxTokens);  // token capacity of the kernel
   w.Rp = M * top_k > w.tok ? M * top_k : w.tok;  // at least one box of rows
   w.err = reinterpret_cast<uint32_t*>(p + off);
   w.sync = w.err + 1;  // words 1..6 of the first 256 bytes
@@ -1102,7 +1104,7 @@ int routed_nvfp4(const void* x, const int32_t* ids, const float* weights, const 
       !nv_map(&a.maph, w.himg, nb2 * w.Rp, 128, 128, w.tok, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !nv_map(&a.maphs, w.hsc, nb2 * w.Rp, 16, 16, w.tok, CU_TENSOR_MAP_SWIZZLE_NONE))
     return set_last_error(FME_ECUDA, "cuTensorMapEncodeTiled failed or unavailable");
-  return w.tok == 16 ? nv_launch<16>(a, st) : nv_launch<kMaxTokens>(a, st);
+  return w.tok == 16 ? nv_launch<16>(a, st) : (w.tok == 32 ? nv_launch<32>(a, st) : nv_launch<kMaxTokens>(a, st));
 }
 
 }  // namespace fme

@@ -50,7 +50,7 @@ ODD = W.Nvfp4Config("nvfp4_odd", 384, 640, 7, 14, 2, 3, float("inf"), (9,))
 
 
 @pytest.mark.parametrize("cfg,M", [(SMALL, 5), (RAGGED, 7), (dataclasses.replace(SMALL, limit=2.0), 6),
-                                   (ODD, 9), (ODD, 33)])
+                                   (ODD, 9), (ODD, 24), (ODD, 33)])
 def test_nvfp4_small_full_parity(fme, cfg, M):
     got, ref, ids = _run(fme, cfg, M, seed=41)
     local = ((ids >= cfg.e0) & (ids < cfg.e0 + cfg.L)).any(axis=1)
@@ -106,7 +106,8 @@ def test_ue8m0_unpack_matches_oracle_and_detects_mismatch(fme):
 
 
 # ---------------------------------------------------------------- fused routing
-@pytest.mark.parametrize("cfg,M,logits_bf16", [(SMALL, 5, False), (RAGGED, 7, True), (ODD, 33, False)])
+@pytest.mark.parametrize("cfg,M,logits_bf16", [(SMALL, 5, False), (RAGGED, 7, True), (ODD, 20, True),
+                                                (ODD, 33, False)])
 def test_nvfp4_fused_routing_matches_oracle_and_unfused_call(fme, cfg, M, logits_bf16):
     from tests.parity import assert_routing
     w13h, s13h, w2h, s2h = _host_weights(cfg, 51)
