@@ -7,8 +7,10 @@
 
 #ifdef __CUDACC__
 #define FME_HD __host__ __device__
+#define FME_HD_COLD __host__ __device__ __noinline__
 #else
 #define FME_HD
+#define FME_HD_COLD
 #endif
 
 namespace fme {
@@ -37,25 +39,111 @@ FME_HD constexpr int waves_cap(int ptok) {
   return max_waves(ptok) > layer_waves(ptok) ? max_waves(ptok) : layer_waves(ptok);
 }
 
+// ---------------------------------------------------------------- slot costs
+// A slot (one K block of one tile of one unit) streams the same weight bytes
+// whatever the unit, but its fill, accumulate and epilogue work grows with the
+// unit's token rows r. Up to kLightRows rows that work hides under the stream
+// and a slot costs kLightRows; a heavy unit's slot costs min(r, 64): the
+// split below balances these costs instead of slot counts. The heavy units
+// are listed in ascending unit order: unit hu[i] with extra cost he[i] =
+// min(r, 64) - kLightRows per slot, hce[i] = he[0] + .. + he[i - 1] (nh + 1
+// entries). At most kMaxHeavy of them; a call with more splits by slot counts.
+constexpr int kLightRows = 8;
+constexpr int kMaxHeavy = 64;
+struct Heavy {
+  int nh = 0;
+  const int16_t* hu = nullptr;
+  const uint16_t* he = nullptr;
+  const uint32_t* hce = nullptr;
+  // Heavy units before unit u.
+  FME_HD int before(int u) const {
+    int lo = 0, hi = nh;
+    while (lo < hi) {
+      const int m = (lo + hi) >> 1;
+      if (hu[m] < u) lo = m + 1; else hi = m;
+    }
+    return lo;
+  }
+};
+
 // ---------------------------------------------------------------- work plan
 // The units are cut into W waves of consecutive units. The slots of one
 // (wave, phase) -- units x tiles x K blocks, at most 1025 x 128 x 64 = 8.4M --
-// are split over Ge = min(G, n) CTAs: CTA c < Ge owns [n*c/Ge, n*(c+1)/Ge),
-// never empty; CTAs c >= Ge own nothing. The products stay below 8.4M x 161
-// < 2^32, so unsigned 32-bit arithmetic is exact.
+// are split over Ge = min(G, n) CTAs into contiguous slices, never empty;
+// CTAs c >= Ge own nothing.
+// - By slot count (no heavy unit in the wave): CTA c < Ge owns
+//   [n*c/Ge, n*(c+1)/Ge). The products stay below 8.4M x 161 < 2^32, so
+//   unsigned 32-bit arithmetic is exact.
+// - By cost: slot x starts at cost position pos(x) (the costs of the slots
+//   before it), the wave's total is Wt, and CTA c owns the slots with
+//   c*Wt <= pos(x)*Ge < (c+1)*Wt. Every slice holds a slot when no slot costs
+//   more than floor(Wt / Ge); a wave where one does splits by slot count.
+//   pos(x) <= 8.4M x 64, so 64-bit products are exact.
+// The cost-weighted split of one (wave, phase) of n slots, tn per unit, from
+// unit u0: see PhasePlan. Out of line and with their arguments by value, so a
+// kernel that never splits by cost carries neither their code nor a PhasePlan
+// in memory.
+struct CostSplit {
+  const Heavy* hv;
+  uint32_t ce0;  // hv->hce at the wave's first unit
+  uint64_t Wt;   // the wave's total cost
+  int n, tn, u0, Ge;
+  // Cost position of the first slot of unit u (u0 <= u <= u0 + n / tn).
+  FME_HD uint64_t ustart(int u) const {
+    return static_cast<uint64_t>(tn) * (static_cast<uint64_t>(kLightRows) * static_cast<uint32_t>(u - u0) +
+                                        hv->hce[hv->before(u)] - ce0);
+  }
+  FME_HD uint32_t slot_cost(int u) const {
+    const int h = hv->before(u);
+    return kLightRows + ((h < hv->nh && hv->hu[h] == u) ? hv->he[h] : 0u);
+  }
+  FME_HD uint64_t pos(int x) const {
+    const int u = u0 + x / tn, o = x - (u - u0) * tn;
+    return ustart(u) + static_cast<uint64_t>(o) * slot_cost(u);
+  }
+};
+// The first slot at or past cost ceil(c * Wt / Ge): its unit is the last one
+// that starts at or before that cost.
+FME_HD_COLD inline int lo_of_by_cost(CostSplit cs, int c) {
+  const uint64_t T = (static_cast<uint64_t>(c) * cs.Wt + static_cast<uint64_t>(cs.Ge) - 1) /
+                     static_cast<uint64_t>(cs.Ge);
+  int lo = 0, hi = cs.n / cs.tn - 1;
+  while (lo < hi) {
+    const int m = (lo + hi + 1) >> 1;
+    if (cs.ustart(cs.u0 + m) <= T) lo = m; else hi = m - 1;
+  }
+  const int u = cs.u0 + lo;
+  const uint64_t cost = cs.slot_cost(u);
+  const uint64_t o = (T - cs.ustart(u) + cost - 1) / cost;
+  const int x = lo * cs.tn + static_cast<int>(o);
+  return x < cs.n ? x : cs.n;
+}
+FME_HD_COLD inline int cta_of_by_cost(CostSplit cs, int x) {
+  return static_cast<int>(cs.pos(x) * static_cast<uint64_t>(cs.Ge) / cs.Wt);
+}
+
 struct PhasePlan {
   int n, lo, hi;
   int Ge, tiles, nb;
   int w, u0;  // wave and its first unit
+  const Heavy* hv;  // nullptr: split by slot count
+  uint32_t ce0;     // hv->hce at the wave's first unit
+  uint64_t Wt;      // the wave's total cost
+  FME_HD CostSplit cost() const { return CostSplit{hv, ce0, Wt, n, tiles * nb, u0, Ge}; }
   FME_HD int lo_of(int c) const {
-    return c >= Ge ? n : static_cast<int>(static_cast<uint32_t>(n) * static_cast<uint32_t>(c) /
-                                          static_cast<uint32_t>(Ge));
+    if (c >= Ge) return n;
+    if (hv == nullptr)
+      return static_cast<int>(static_cast<uint32_t>(n) * static_cast<uint32_t>(c) / static_cast<uint32_t>(Ge));
+    return lo_of_by_cost(cost(), c);
   }
   // The CTA whose slice holds slot x.
   FME_HD int cta_of(int x) const {
-    return static_cast<int>((static_cast<uint32_t>(x + 1) * static_cast<uint32_t>(Ge) + static_cast<uint32_t>(n) - 1u) /
-                            static_cast<uint32_t>(n)) - 1;
+    if (hv == nullptr)
+      return static_cast<int>((static_cast<uint32_t>(x + 1) * static_cast<uint32_t>(Ge) + static_cast<uint32_t>(n) -
+                               1u) / static_cast<uint32_t>(n)) - 1;
+    return cta_of_by_cost(cost(), x);
   }
+  FME_HD uint64_t pos(int x) const { return cost().pos(x); }
 };
 
 struct Plan {
@@ -65,6 +153,7 @@ struct Plan {
   int phase_lo, phase_hi;  // phases this launch runs
   int N1, kcmax1;  // the MX kernel's GEMM1 B rows (four per token) and K blocks per chunk
   int tiles[2], nb[2];  // per unit: GEMM1 64-row tiles x H/128 K blocks; GEMM2 128-row tiles x I/128
+  const Heavy* hv = nullptr;  // nullptr or no heavy unit: every split by slot count
   FME_HD int wave_lo(int w) const { return U * w / W; }
   // Stage q of 2W: GEMM1 of wave 0, then GEMM1(w + 1) / GEMM2(w) pairs, then
   // the last GEMM2.
@@ -90,6 +179,24 @@ struct Plan {
     pp.w = w;
     pp.u0 = u0;
     pp.Ge = plan_min(G, pp.n);
+    pp.hv = nullptr;
+    pp.ce0 = 0;
+    pp.Wt = 0;
+    if (hv != nullptr && hv->nh > 0) {
+      // Split this wave by cost when it holds a heavy unit and no slot costs
+      // more than a slice's share.
+      const int h0 = hv->before(u0), h1 = hv->before(u1);
+      uint32_t emax = 0;
+      for (int h = h0; h < h1; ++h) emax = hv->he[h] > emax ? hv->he[h] : emax;
+      const uint64_t Wt = static_cast<uint64_t>(t * nbp) * (static_cast<uint64_t>(kLightRows) *
+                                                                  static_cast<uint32_t>(u1 - u0) +
+                                                              hv->hce[h1] - hv->hce[h0]);
+      if (h1 > h0 && kLightRows + emax <= Wt / static_cast<uint64_t>(pp.Ge)) {
+        pp.hv = hv;
+        pp.ce0 = hv->hce[h0];
+        pp.Wt = Wt;
+      }
+    }
     if (c >= pp.Ge) {
       pp.lo = pp.hi = pp.n;
     } else {

@@ -119,6 +119,10 @@ struct TcSmem {
   unsigned long long tokmask[kMaxExperts];
   int16_t rid[kMaxTokens * kMaxTopK];
   int16_t ulist[kMaxExperts + 1];  // [0]: the shared expert, when present
+  Heavy heavy;  // the heavy units of the cost-weighted split (at most the shared one)
+  int16_t hu[1];
+  uint16_t he[1];
+  uint32_t hce[2];
   int16_t ctx_route[3][kMaxTokens];  // routes of each B buffer's expert, in token order; [2]: the fill's next
   int btag[2];                       // what each B buffer holds: a GEMM2 (unit, K range), or -1
   alignas(1024) uint32_t sfa_one[128];  // 32 rows x 16 bytes of 2^0 scales (MX kernel)
@@ -1017,10 +1021,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
         S.U = U;
         S.rmax = a.has_shared ? max(rmax, a.M) : rmax;
       }
+      if constexpr (TOK > kLightRows) {
+        // The one-launch layer's shared unit holds every token: above
+        // kLightRows tokens its slots carry more fill, accumulate and
+        // epilogue work than the routed units' and the split weighs them so
+        // (M = 16: 683 -> 664 us). Routed units with many tokens measured no
+        // better weighted (Latent shape, M = 16 / 32: 395 / 608 against 405 /
+        // 616 us) and stay unweighted.
+        if (lane == 0) {
+          const int nh = a.has_shared && a.M > kLightRows ? 1 : 0;
+          S.hu[0] = 0;
+          S.he[0] = static_cast<uint16_t>(min(a.M, 64) - kLightRows);
+          S.hce[0] = 0;
+          S.hce[1] = S.he[0];
+          S.heavy.nh = nh;
+          S.heavy.hu = S.hu;
+          S.heavy.he = S.he;
+          S.heavy.hce = S.hce;
+        }
+      }
     }
   } else if (tid == 0) {
     S.U = 1;  // shared expert only
     S.rmax = a.M;
+    S.heavy.nh = 0;
   }
   __syncthreads();
 
@@ -1066,6 +1090,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
   // shared memory (M = 4: 213 -> 210 us; at 8 tokens, where the waves overlap
   // the hand-over, the longer chunks measured faster).
   P.kcmax2 = TOK <= 4 ? min(P.kcmax, kTcStages) : P.kcmax;
+  // Up to kLightRows tokens no unit is heavy: those kernels split by slot
+  // counts only and hold none of the cost-weighted code.
+  P.hv = TOK > kLightRows ? &S.heavy : nullptr;
   P.N1 = P.N;
   P.kcmax1 = P.kcmax;
   P.c = blockIdx.x;

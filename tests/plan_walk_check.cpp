@@ -4,8 +4,11 @@
 // cover every (phase, unit, tile, K block) slot of the launched phases exactly
 // once, in chunks of 1..kcmax K blocks inside one tile, each slot on the CTA
 // cta_of names, a split tile's first K blocks at the end of its first
-// contributor's slice, and no slot of a phase the launch does not run.
+// contributor's slice, and no slot of a phase the launch does not run. With
+// heavy units (a cost-weighted split) every slice of every stage must also be
+// non-empty, and a slice's cost must stay within one slot of its share.
 // Prints "OK <cases>" or the first failure; exit status 0 only on success.
+#include <cstdint>
 #include <cstdio>
 #include <vector>
 
@@ -22,7 +25,7 @@ static int fail(const char* what, int U, int G, int W, int lo, int hi, int c) {
 
 template <bool MX>
 static int check(int U, int tiles1, int nb1, int tiles2, int nb2, int G, int W, int lo, int hi, int kcmax, int kcmax1,
-                 int kcmax2) {
+                 int kcmax2, const fme::Heavy& hv) {
   // seen[phase][unit][tile][kb]
   std::vector<int> seen[2];
   seen[0].assign(static_cast<size_t>(U) * tiles1 * nb1, 0);
@@ -35,6 +38,7 @@ static int check(int U, int tiles1, int nb1, int tiles2, int nb2, int G, int W, 
     P.N1 = 16;
     P.kcmax1 = kcmax1;
     P.kcmax2 = kcmax2;
+    P.hv = &hv;
     P.c = c;
     P.G = G;
     P.W = W;
@@ -73,6 +77,37 @@ static int check(int U, int tiles1, int nb1, int tiles2, int nb2, int G, int W, 
       last_phase = ch.phase;
     }
   }
+  // Every stage's slices: contiguous, non-empty, and by cost within one slot
+  // of an equal share.
+  {
+    Plan P{};
+    P.U = U;
+    P.hv = &hv;
+    P.c = 0;
+    P.G = G;
+    P.W = W;
+    P.phase_lo = 1;
+    P.phase_hi = 2;
+    P.tiles[0] = tiles1;
+    P.nb[0] = nb1;
+    P.tiles[1] = tiles2;
+    P.nb[1] = nb2;
+    for (int w = 0; w < W; ++w)
+      for (int ph = 1; ph <= 2; ++ph) {
+        const fme::PhasePlan pp = P.plan(w, ph);
+        if (pp.lo_of(0) != 0 || pp.lo_of(pp.Ge) != pp.n) return fail("slices do not cover the stage", U, G, W, ph, ph, -1);
+        for (int c = 0; c < pp.Ge; ++c) {
+          const int a = pp.lo_of(c), b = pp.lo_of(c + 1);
+          if (b <= a) return fail("empty slice", U, G, W, ph, ph, c);
+          if (pp.cta_of(a) != c || pp.cta_of(b - 1) != c) return fail("cta_of at a slice edge", U, G, W, ph, ph, c);
+          if (pp.hv != nullptr) {
+            const uint64_t cost = (b < pp.n ? pp.pos(b) : pp.Wt) - pp.pos(a);
+            const uint64_t share = pp.Wt / static_cast<uint64_t>(pp.Ge);
+            if (cost + 64 < share || cost > share + 64 + 1) return fail("slice cost off its share", U, G, W, ph, ph, c);
+          }
+        }
+      }
+  }
   for (int p = 0; p < 2; ++p) {
     const bool run = p + 1 >= lo && p + 1 <= hi;
     for (int v : seen[p])
@@ -100,10 +135,31 @@ int main() {
             for (int kc : {16, 8, 4, 1}) {
               if (W > U || (r[0] == r[1] && W != 1)) continue;
               const int kc2 = kc < 8 ? kc : 8;
-              if (check<false>(U, s.tiles1, s.nb1, s.tiles2, s.nb2, G, W, r[0], r[1], kc, kc, kc2)) return 1;
-              if (check<true>(U, s.tiles1, s.nb1, s.tiles2, s.nb2, G, W, r[0], r[1], kc, kc > 4 ? kc / 4 : 1, kc2))
-                return 1;
-              cases += 2;
+              // no heavy unit; unit 0 heavy (a one-launch layer's shared
+              // expert); every third unit heavy, costs up to 64 rows a slot
+              for (int pattern = 0; pattern < 3; ++pattern) {
+                std::vector<int16_t> hu;
+                std::vector<uint16_t> he;
+                for (int u = 0; u < U && static_cast<int>(hu.size()) < fme::kMaxHeavy; ++u) {
+                  const bool heavy = pattern == 1 ? u == 0 : (pattern == 2 && u % 3 == 1);
+                  if (heavy) {
+                    hu.push_back(static_cast<int16_t>(u));
+                    he.push_back(static_cast<uint16_t>(pattern == 1 ? 56 : 1 + (u * 7) % 56));
+                  }
+                }
+                std::vector<uint32_t> hce(hu.size() + 1, 0);
+                for (size_t i = 0; i < hu.size(); ++i) hce[i + 1] = hce[i] + he[i];
+                fme::Heavy hv;
+                hv.nh = static_cast<int>(hu.size());
+                hv.hu = hu.data();
+                hv.he = he.data();
+                hv.hce = hce.data();
+                if (check<false>(U, s.tiles1, s.nb1, s.tiles2, s.nb2, G, W, r[0], r[1], kc, kc, kc2, hv)) return 1;
+                if (check<true>(U, s.tiles1, s.nb1, s.tiles2, s.nb2, G, W, r[0], r[1], kc, kc > 4 ? kc / 4 : 1, kc2,
+                                hv))
+                  return 1;
+                cases += 2;
+              }
             }
   std::printf("OK %d\n", cases);
   return 0;
