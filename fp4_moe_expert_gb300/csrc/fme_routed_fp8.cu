@@ -124,6 +124,7 @@ struct TcSmem {
   uint16_t he[1];
   uint32_t hce[2];
   int16_t ctx_route[3][kMaxTokens];  // routes of each B buffer's expert, in token order; [2]: the fill's next
+  int16_t ctx_tok[kMaxTokens];       // the tokens of ctx_route[2]
   int btag[2];                       // what each B buffer holds: a GEMM2 (unit, K range), or -1
   alignas(1024) uint32_t sfa_one[128];  // 32 rows x 16 bytes of 2^0 scales (MX kernel)
   int ctx_n[3];
@@ -337,7 +338,10 @@ __device__ void fill_context(const TcArgs& a, TcSmem& S, int u, int fid) {
     const int lane = fid;
     if (a.has_shared && u == 0) {
       // The shared expert's rows follow the routed ones in hbuf: M*top_k + t.
-      for (int t = lane; t < a.M; t += 32) S.ctx_route[b][t] = static_cast<int16_t>(a.M * a.top_k + t);
+      for (int t = lane; t < a.M; t += 32) {
+        S.ctx_route[b][t] = static_cast<int16_t>(a.M * a.top_k + t);
+        S.ctx_tok[t] = static_cast<int16_t>(t);
+      }
       if (lane == 0) S.ctx_n[b] = a.M;
     } else {
       const int e = S.ulist[u];
@@ -351,7 +355,9 @@ __device__ void fill_context(const TcArgs& a, TcSmem& S, int u, int fid) {
           int r = 0;
           for (int k = 0; k < a.top_k; ++k)
             if (S.rid[t * a.top_k + k] == e) r = k;
-          S.ctx_route[b][base + __popc(bal & ((1u << lane) - 1u))] = static_cast<int16_t>(t * a.top_k + r);
+          const int i = base + __popc(bal & ((1u << lane) - 1u));
+          S.ctx_route[b][i] = static_cast<int16_t>(t * a.top_k + r);
+          S.ctx_tok[i] = static_cast<int16_t>(t);
         }
         base += __popc(bal);
       }
@@ -360,6 +366,28 @@ __device__ void fill_context(const TcArgs& a, TcSmem& S, int u, int fid) {
   }
   fill_bar();
 }
+
+// A chunk's items, row (route) t and K block j of its r rows x kc K blocks,
+// rows fastest: item p = j * r + t. A thread that steps through them `step`
+// at a time keeps (t, j) and advances by (step % r, step / r), so no item costs
+// a division by r.
+struct ItemWalk {
+  int t, j, dt, dj, r;
+  __device__ __forceinline__ ItemWalk(int p0, int step, int rows) : r(rows) {
+    j = p0 / rows;
+    t = p0 - j * rows;
+    dj = step / rows;
+    dt = step - dj * rows;
+  }
+  __device__ __forceinline__ void next() {
+    t += dt;
+    j += dj;
+    if (t >= r) {
+      t -= r;
+      ++j;
+    }
+  }
+};
 
 // MXFP8 input, GEMM1 chunk: one B row per route, the token's E4M3 codes as
 // they are (cp.async into the swizzled layout); the four E8M0 bytes of each
@@ -370,8 +398,9 @@ __device__ void fill_context(const TcArgs& a, TcSmem& S, int u, int fid) {
 // staged as copy j (512 bytes), row t % 32, word t / 32. The activation scale
 // of the accumulate step is then 1. Routed experts only (the MX entry has no
 // shared expert).
+template <int TOK>
 __device__ bool fill_b_mx(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& ch, int b, int ci, int fid) {
-  const int r = S.ctx_n[2];
+  const int r = TOK == 1 ? 1 : S.ctx_n[2];  // one token: one route per unit
   const int N = P.N;
   uint8_t* B = S.B[b];
   uint32_t* stage = reinterpret_cast<uint32_t*>(B + kMxSfStage);
@@ -394,16 +423,20 @@ __device__ bool fill_b_mx(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk
   for (int t = fid; t < r; t += kFillThreads) S.ctx_route[b][t] = S.ctx_route[2][t];
   if (fid == 0) S.ctx_n[b] = r;
   const int items = ch.kc * r * 8;
-  for (int w = fid; w < items; w += kFillThreads) {
-    const int p = w >> 3, sub = w & 7;
-    const int t = p % r, j = p / r;
-    const int tok = S.ctx_route[2][t] / a.top_k;
-    cp_async_16(B + j * N * 128 + t * 128 + ((sub ^ (t & 7)) << 4),
-                a.xq + static_cast<size_t>(tok) * a.H + (ch.kb0 + j) * 128 + sub * 16);
+  {
+    ItemWalk it(fid >> 3, kFillThreads / 8, r);
+    const int sub = fid & 7;
+    for (int w = fid; w < items; w += kFillThreads, it.next()) {
+      const int t = it.t, j = it.j;
+      const int tok = S.ctx_tok[t];
+      cp_async_16(B + j * N * 128 + t * 128 + ((sub ^ (t & 7)) << 4),
+                  a.xq + static_cast<size_t>(tok) * a.H + (ch.kb0 + j) * 128 + sub * 16);
+    }
   }
-  for (int w = fid; w < ch.kc * r; w += kFillThreads) {
-    const int t = w % r, j = w / r;
-    const int tok = S.ctx_route[2][t] / a.top_k;
+  ItemWalk iw(fid, kFillThreads, r);
+  for (int w = fid; w < ch.kc * r; w += kFillThreads, iw.next()) {
+    const int t = iw.t, j = iw.j;
+    const int tok = S.ctx_tok[t];
     const uint8_t* e = a.xsc + static_cast<size_t>(tok) * (a.H / 32) + (ch.kb0 + j) * 4;
     // The four bytes in one load when the array is 4-byte aligned (rows are
     // H / 32 bytes, a multiple of 4); bytes [e, e + 3] little-endian either way.
@@ -451,18 +484,20 @@ __device__ bool fill_b_copy(const TcArgs& a, TcSmem& S, const Plan& P, const Chu
   for (int t = fid; t < r; t += kFillThreads) S.ctx_route[b][t] = S.ctx_route[2][t];
   if (fid == 0) S.ctx_n[b] = r;
   const int items = ch.kc * r * 8;
-  for (int w = fid; w < items; w += kFillThreads) {
-    const int p = w >> 3, sub = w & 7;
-    const int t = p % r, j = p / r;
-    const int route = S.ctx_route[2][t];
-    const int tok = xi.shared ? route - a.M * a.top_k : route / a.top_k;
-    cp_async_16(B + j * N * 128 + t * 128 + ((sub ^ (t & 7)) << 4),
-                a.ximg + static_cast<size_t>(tok) * a.H + (ch.kb0 + j) * 128 + sub * 16);
+  {
+    ItemWalk it(fid >> 3, kFillThreads / 8, r);
+    const int sub = fid & 7;
+    for (int w = fid; w < items; w += kFillThreads, it.next()) {
+      const int t = it.t, j = it.j;
+      const int tok = S.ctx_tok[t];
+      cp_async_16(B + j * N * 128 + t * 128 + ((sub ^ (t & 7)) << 4),
+                  a.ximg + static_cast<size_t>(tok) * a.H + (ch.kb0 + j) * 128 + sub * 16);
+    }
   }
-  for (int w = fid; w < ch.kc * r; w += kFillThreads) {
-    const int t = w % r, j = w / r;
-    const int route = S.ctx_route[2][t];
-    const int tok = xi.shared ? route - a.M * a.top_k : route / a.top_k;
+  ItemWalk iw(fid, kFillThreads, r);
+  for (int w = fid; w < ch.kc * r; w += kFillThreads, iw.next()) {
+    const int t = iw.t, j = iw.j;
+    const int tok = S.ctx_tok[t];
     S.xs[b][t][j] = __ldcg(a.ximg_sc + static_cast<size_t>(tok) * nbx + ch.kb0 + j);
   }
   if (fid < 2 * kMaxKc) S.wsc[b][fid / kMaxKc][fid % kMaxKc] = wsv;
@@ -485,13 +520,13 @@ __device__ bool fill_b_copy(const TcArgs& a, TcSmem& S, const Plan& P, const Chu
 // The scales and the first batch of activations are loaded before waiting
 // for buffer b (chunk ci - 2's accumulators read), hiding their latency.
 // Returns false when the wait gave up.
-template <bool MX>
+template <int TOK, bool MX>
 __device__ bool fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& ch, int b, int ci, int fid) {
   if constexpr (MX) {
-    if (ch.phase == 1) return fill_b_mx(a, S, P, ch, b, ci, fid);
+    if (ch.phase == 1) return fill_b_mx<TOK>(a, S, P, ch, b, ci, fid);
   }
   if (ch.phase == 1 && P.ximage) return fill_b_copy(a, S, P, ch, b, ci, fid);
-  const int r = S.ctx_n[2];
+  const int r = TOK == 1 ? 1 : S.ctx_n[2];  // one token: one route per unit
   const int N = P.N;
   uint8_t* B = S.B[b];
   const XInfo xi = xinfo(a, S, ch.u);
@@ -523,20 +558,25 @@ __device__ bool fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
   constexpr int IPT = 2;
   float v[IPT][16], vn[IPT][16];
   int tt[IPT], jj[IPT], ttn[IPT], jjn[IPT];
+  // Item w = base + q * kFillThreads + fid: 16-byte piece w & 7 of item
+  // (row, K block) w >> 3, walked per q without dividing by r.
+  ItemWalk walk[IPT] = {ItemWalk(fid >> 3, kFillThreads * IPT / 8, r),
+                        ItemWalk(kFillThreads / 8 + (fid >> 3), kFillThreads * IPT / 8, r)};
+  static_assert(IPT == 2, "one walk per item of a round");
   auto load_batch = [&](float (&v)[IPT][16], int (&tt)[IPT], int (&jj)[IPT], int base) {
 #pragma unroll
     for (int q = 0; q < IPT; ++q) {
       const int w = base + q * kFillThreads + fid;
-      const int p = w >> 3, sub = w & 7;
+      const int sub = w & 7;
       tt[q] = -1;
       jj[q] = 0;
       if (w < items) {
-        tt[q] = p % r;
-        jj[q] = p / r;
+        tt[q] = walk[q].t;
+        jj[q] = walk[q].j;
         const int route = S.ctx_route[2][tt[q]];
         const int col = (ch.kb0 + jj[q]) * 128 + sub * 16;
         if (ch.phase == 1) {
-          const int tok = xi.shared ? route - a.M * a.top_k : route / a.top_k;
+          const int tok = S.ctx_tok[tt[q]];
           const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(tok) * K + col);
           const uint4 q0 = __ldg(src), q1 = __ldg(src + 1);
           const uint32_t wd[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
@@ -560,6 +600,7 @@ __device__ bool fill_b(const TcArgs& a, TcSmem& S, const Plan& P, const Chunk& c
 #pragma unroll
         for (int k = 0; k < 16; ++k) v[q][k] = 0.0f;
       }
+      walk[q].next();
     }
   };
   auto store_batch = [&](int base) {  // quantises v (tt, jj) of the round at `base`
@@ -1299,7 +1340,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
       if (first2 && !wait_hidden(a, S, P, ch, fid)) break;
       ctx_u = ch.u;
       ctx_phase = ch.phase;
-      if (!fill_b<MX>(a, S, P, ch, b, ci, fid)) break;
+      if (!fill_b<TOK, MX>(a, S, P, ch, b, ci, fid)) break;
       if (first2 && fid == 0) pass_hidden(a, S, ch);
       ++ci;
     }
