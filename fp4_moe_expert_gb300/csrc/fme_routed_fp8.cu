@@ -208,8 +208,10 @@ struct RouteCand {
 // Tokens t0 .. t0 + ntok - 1 (ntok <= 8 / wpt), wpt warps each; E <= 128 wpt.
 // gpicks == nullptr: the picks go to S.rid / S.tokmask; else to gpicks[t][r]
 // in global memory (the routing shared between CTAs).
+template <int WPT = 0>  // warps per token when known at compile time (else wpt)
 __device__ void route_split(const TcArgs& a, TcSmem& S, int warp, int lane, bool write_out, int t0, int ntok, int wpt,
                             int32_t* gpicks) {
+  if constexpr (WPT > 0) wpt = WPT;
   const int tl = warp / wpt, sl = warp % wpt;
   const int t = t0 + tl;
   const int k = a.top_k;
@@ -272,13 +274,12 @@ __device__ void route_split(const TcArgs& a, TcSmem& S, int warp, int lane, bool
     float sc[JM];
 #pragma unroll
     for (int j = 0; j < JM; ++j) {
-      const int i = lane + 32 * j;
-      const int sl = i / k, r = i - sl * k;
+      const int i = lane + 32 * j;  // slice i / k, rank i % k
       ky[j] = 0u;
       ex[j] = 0x7FFFFFFF;
       sc[j] = 0.0f;
       if (i < n) {
-        const RouteCand c = cs[sl * k + r];
+        const RouteCand c = cs[i];
         ky[j] = c.key;
         ex[j] = c.e;
         sc[j] = c.score;
@@ -999,7 +1000,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
   if (a.E > 0) {
     const int wpt = a.M == 1 ? 8 : (a.M == 2 ? 4 : 2);
     static_assert(kMaxExperts <= 128 * 8, "one token always takes the split router");
-    if (TOK == 1 || (a.M <= 4 && a.E <= 128 * wpt)) {
+    if constexpr (TOK == 1) {
+      route_split<8>(a, S, warp, lane, blockIdx.x == 0 && a.phase_lo == 1, 0, 1, 8, nullptr);
+    } else if (a.M <= 4 && a.E <= 128 * wpt) {
       route_split(a, S, warp, lane, blockIdx.x == 0 && a.phase_lo == 1, 0, a.M, wpt, nullptr);
     } else {
       // Many tokens or experts: CTA c routes tokens c, c + G, ... with all its
@@ -1138,7 +1141,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
   P.kcmax1 = P.kcmax;
   P.c = blockIdx.x;
   P.G = gridDim.x;
-  P.W = a.phase_lo == a.phase_hi ? 1 : min(P.U, a.has_shared ? layer_waves(a.ptok) : max_waves(a.ptok));
+  // (One token: one wave either way, known here so the schedule folds.)
+  P.W = TOK == 1 || a.phase_lo == a.phase_hi ? 1
+                                             : min(P.U, a.has_shared ? layer_waves(a.ptok) : max_waves(a.ptok));
+  static_assert(max_waves(1) == 1 && layer_waves(1) == 1, "one wave at one token");
   P.phase_lo = a.phase_lo;
   P.phase_hi = a.phase_hi;
   P.tiles[0] = a.I / 64;
