@@ -39,6 +39,29 @@ FME_HD constexpr int waves_cap(int ptok) {
   return max_waves(ptok) > layer_waves(ptok) ? max_waves(ptok) : layer_waves(ptok);
 }
 
+// ---------------------------------------------------------------- fill items
+// A chunk's items, row (route) t and K block j of its r rows x kc K blocks,
+// rows fastest: item p = j * r + t. A thread that steps through them `step`
+// at a time keeps (t, j) and advances by (step % r, step / r), so no item costs
+// a division by r.
+struct ItemWalk {
+  int t, j, dt, dj, r;
+  FME_HD ItemWalk(int p0, int step, int rows) : r(rows) {
+    j = p0 / rows;
+    t = p0 - j * rows;
+    dj = step / rows;
+    dt = step - dj * rows;
+  }
+  FME_HD void next() {
+    t += dt;
+    j += dj;
+    if (t >= r) {
+      t -= r;
+      ++j;
+    }
+  }
+};
+
 // ---------------------------------------------------------------- slot costs
 // A slot (one K block of one tile of one unit) streams the same weight bytes
 // whatever the unit, but its fill, accumulate and epilogue work grows with the

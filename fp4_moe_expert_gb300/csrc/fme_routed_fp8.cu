@@ -368,28 +368,6 @@ __device__ void fill_context(const TcArgs& a, TcSmem& S, int u, int fid) {
   fill_bar();
 }
 
-// A chunk's items, row (route) t and K block j of its r rows x kc K blocks,
-// rows fastest: item p = j * r + t. A thread that steps through them `step`
-// at a time keeps (t, j) and advances by (step % r, step / r), so no item costs
-// a division by r.
-struct ItemWalk {
-  int t, j, dt, dj, r;
-  __device__ __forceinline__ ItemWalk(int p0, int step, int rows) : r(rows) {
-    j = p0 / rows;
-    t = p0 - j * rows;
-    dj = step / rows;
-    dt = step - dj * rows;
-  }
-  __device__ __forceinline__ void next() {
-    t += dt;
-    j += dj;
-    if (t >= r) {
-      t -= r;
-      ++j;
-    }
-  }
-};
-
 // MXFP8 input, GEMM1 chunk: one B row per route, the token's E4M3 codes as
 // they are (cp.async into the swizzled layout); the four E8M0 bytes of each
 // (route, K block) -- one per 32-value block -- are staged for the MMA

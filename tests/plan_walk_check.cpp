@@ -116,7 +116,23 @@ static int check(int U, int tiles1, int nb1, int tiles2, int nb2, int G, int W, 
   return 0;
 }
 
+// The fill warps' division-free walk over a chunk's (row, K block) items.
+static int check_item_walk() {
+  for (int r = 1; r <= 64; ++r)
+    for (int step : {1, 3, 8, 16, 64, 128})
+      for (int p0 = 0; p0 < step + 9; ++p0) {
+        fme::ItemWalk w(p0, step, r);
+        for (int k = 0, p = p0; k < 300; ++k, p += step, w.next())
+          if (w.t != p % r || w.j != p / r) {
+            std::printf("FAIL item walk: r=%d step=%d p0=%d item %d\n", r, step, p0, p);
+            return 1;
+          }
+      }
+  return 0;
+}
+
 int main() {
+  if (check_item_walk()) return 1;
   struct Shape { int tiles1, nb1, tiles2, nb2; };
   const Shape shapes[] = {{32, 56, 56, 16},   // DeepSeek-V3: I 2048, H 7168
                           {32, 28, 28, 16},   // latent: H 3584

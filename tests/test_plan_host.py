@@ -2,7 +2,9 @@
 tests/plan_walk_check.cpp against the kernel's own schedule header
 (fme_plan.cuh, host and device code) and runs it. Every CTA's chunk walk must
 cover each (phase, unit, tile, K block) slot of the launched phases exactly
-once, for one launch and for the two-kernel chain's phase ranges."""
+once, for one launch and for the two-kernel chain's phase ranges, with slices by
+slot count and by cost; and the fill warps' division-free walk over a chunk's
+(row, K block) items must match p % r, p / r."""
 
 import os
 import shutil
