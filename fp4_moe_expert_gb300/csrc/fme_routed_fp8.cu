@@ -974,7 +974,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fp8_moe_tc_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
 
-  // ---- routing and the unique-expert list (routed experts first, then the shared one)
+  // ---- routing and the unit list (the shared expert first, when present, then the routed ones)
   if (a.E > 0) {
     const int wpt = a.M == 1 ? 8 : (a.M == 2 ? 4 : 2);
     static_assert(kMaxExperts <= 128 * 8, "one token always takes the split router");
