@@ -59,9 +59,10 @@ struct NvCfg {
   // Packed-weight ring: 64-80 KB in flight per SM. Deeper rings measured
   // slower (more weight rows open at once in DRAM: 10 stages took M = 8 from
   // 56 to 62 us, 8 stages M = 64 from 177 to 205 us); the activation operand
-  // comes from L2 and needs only a short ring of its own.
+  // comes from L2 and needs only a short ring of its own: 6 stages from 32
+  // tokens up (M = 64: 182.9 -> 180.9 us against 4; 8 took it to 211 us).
   static constexpr int kStages = TOK == 16 ? 4 : 5;
-  static constexpr int kBStages = 4;
+  static constexpr int kBStages = TOK == 16 ? 4 : 6;
   static constexpr int kSfBuf = 4;                // scale-vector buffers in tensor memory
   static constexpr int kBBytes = TOK * 128;       // TOK rows of 128 packed bytes (256 values)
   static constexpr int kBsBytes = TOK * 16;       // their 16 group scales
