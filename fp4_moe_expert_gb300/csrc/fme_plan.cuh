@@ -34,10 +34,24 @@ FME_HD constexpr int max_waves(int ptok) { return ptok >= 7 ? 3 : 1; }
 FME_HD constexpr int layer_waves(int ptok) {
   return ptok <= 2 ? 1 : (ptok == 3 || ptok == 5 ? 2 : 3);
 }
-// Waves the partial-sum region is sized for, any call.
+// Waves the partial-sum region is sized for: the most any call with up to
+// ptok token rows may take, so the workspace never shrinks as M grows and one
+// sized for M serves every smaller token count.
 FME_HD constexpr int waves_cap(int ptok) {
-  return max_waves(ptok) > layer_waves(ptok) ? max_waves(ptok) : layer_waves(ptok);
+  int cap = 1;
+  for (int p = 1; p <= ptok; ++p) {
+    cap = max_waves(p) > cap ? max_waves(p) : cap;
+    cap = layer_waves(p) > cap ? layer_waves(p) : cap;
+  }
+  return cap;
 }
+constexpr bool waves_cap_holds() {
+  for (int p = 1; p <= 64; ++p)
+    if (waves_cap(p) < max_waves(p) || waves_cap(p) < layer_waves(p) || (p > 1 && waves_cap(p) < waves_cap(p - 1)))
+      return false;
+  return true;
+}
+static_assert(waves_cap_holds(), "the partial-sum region holds every call's waves and grows with M");
 
 // ---------------------------------------------------------------- fill items
 // A chunk's items, row (route) t and K block j of its r rows x kc K blocks,

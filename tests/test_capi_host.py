@@ -174,6 +174,24 @@ def test_layer_validation_and_workspace(fme):
     assert _layer(fme, wsb=64) in (-6, -4)
 
 
+def test_workspace_sizes_grow_with_tokens_and_fit_the_documented_limits(fme):
+    """A workspace sized for M serves every smaller token count, the layer's
+    holds the routed call's, and the no-allocation variant's 64 MiB scratch
+    covers what its header says: DeepSeek-V3 up to 63 tokens, Latent up to 32."""
+    for H, I, E, k in ((7168, 2048, 256, 8), (3584, 2048, 896, 16), (1024, 384, 40, 3)):
+        prev = 0
+        for M in range(1, 65):
+            routed = fme.moe_routed_fp8_workspace(M, H, I, E, k)
+            assert routed >= prev
+            assert fme.moe_layer_fp8_workspace(M, H, I, E, k) >= routed
+            prev = routed
+    limit = 64 << 20
+    assert fme.moe_routed_fp8_workspace(63, 7168, 2048, 256, 8) <= limit
+    assert fme.moe_routed_fp8_workspace(64, 7168, 2048, 256, 8) > limit
+    assert fme.moe_routed_fp8_workspace(32, 3584, 2048, 896, 16) <= limit
+    assert fme.moe_routed_fp8_workspace(64, 3584, 2048, 896, 16) > limit
+
+
 def test_noalloc_checks_arguments_before_touching_its_scratch(fme):
     """The allocation-free variant runs fme_moe_routed_fp8's host checks before
     any CUDA call, so these rejections need no GPU."""
